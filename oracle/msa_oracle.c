@@ -1,0 +1,406 @@
+/*
+ * msa_oracle.c -- plain CPU reference of block-sparse paged decode attention.
+ *
+ * TEST INFRASTRUCTURE.  Only the test suite, the package smoke check and the
+ * benchmark's CPU-baseline leg call this code; the library never does.  It
+ * shares no code, header, table or helper with the CUDA path.
+ *
+ * Sources.  The method is described in prose on three TensorRT-LLM pull
+ * request pages about MiniMax-M3 serving:
+ *   [M3-DECODE]  "MiniMax-M3 NVFP4 low-latency decode megakernel for
+ *                modeling_v2 for Blackwell", sections "The TP4 decode target",
+ *                "The TP8 decode target" and "Step-loop runtime hooks";
+ *   [M31-RUBIN]  "Add Rubin (sm_107) MiniMax-M3.1 low-latency decode targets",
+ *                section "Items and numerics", section "Disclosures and known
+ *                gaps", and its commit messages on the MSA selector/decode
+ *                hooks, the long-context select, the prefill select tile and
+ *                the q8kv4 indexer over an NVFP4 index-K mirror;
+ *   [M3-P128]    "MiniMax-M3: native P128 draft KV view for the NVFP4 hybrid
+ *                cache", section "Description".
+ * The pages fix the structure (index score, per-block max, top-k block
+ * selection with a smaller-index tie-break and an ascending -1-padded table,
+ * GQA attention over the selected 128-token pages) but print no formula.
+ * Where they are silent this file takes the plainest reading, marked READING.
+ *
+ * Everything is computed in double precision with plain loops, one token at
+ * a time, in the order the definition states.  No blocking, no fusion.
+ *
+ * Layouts are those of the synthetic-input module (row-major, Hi = 1 index
+ * head):
+ *   q_idx       bf16 bits  [T][Di]
+ *   idxk_pool   bf16 bits  [pages][P][Di]      or NVFP4 bytes [pages][P][Di/2]
+ *   idxk_scales E4M3 codes [pages][P][Di/16]   (NVFP4 only)
+ *   q           bf16 bits  [T][Hq][D]
+ *   kv_pool     bf16 bits or E4M3 codes [pages][2][Hkv][P][D]  (K then V)
+ *   block_table int32      [R][max_blocks]
+ *   seq_lens    int32      [R]
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+typedef struct oracle_shape {
+    int32_t num_requests;
+    int32_t q_per_req;
+    int32_t num_q_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t index_dim;
+    int32_t page_size;
+    int32_t num_pages;
+    int32_t max_blocks;
+    int32_t topk;
+    int32_t kv_fp8;      /* 0: bf16 K/V; 1: E4M3 K/V with per-tensor scales */
+    int32_t index_nvfp4; /* 0: bf16 index keys; 1: NVFP4 codes + E4M3 scales */
+    double softmax_scale;
+    double k_scale;
+    double v_scale;
+} oracle_shape;
+
+enum {
+    ORACLE_OK = 0,
+    ORACLE_BAD_PAGE = 1,
+    ORACLE_BAD_SEQ_LEN = 2,
+    ORACLE_BAD_SELECTION = 3,
+    ORACLE_NO_MEMORY = 4,
+};
+
+/* ---- element decoders --------------------------------------------------- */
+
+/* bf16: the upper 16 bits of an IEEE binary32. */
+double oracle_bf16(uint16_t bits)
+{
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* FP8 E4M3 ("fn" variant: no infinities, S.1111.111 is NaN): 1 sign bit,
+ * 4 exponent bits with bias 7, 3 mantissa bits; exponent 0 is subnormal.
+ * [M31-RUBIN] "Items and numerics" and [M3-DECODE] "The TP4 decode target"
+ * use FP8 KV; the pages name the format only. */
+double oracle_e4m3(uint8_t code)
+{
+    int sign = code >> 7;
+    int e = (code >> 3) & 15;
+    int m = code & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);          /* m/8 * 2^(1-7) */
+    else
+        v = ldexp((double)(8 + m), e - 10); /* (1 + m/8) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+/* FP4 E2M1: 1 sign bit, 2 exponent bits with bias 1, 1 mantissa bit;
+ * exponent 0 is subnormal (0 or 0.5).  The NVFP4 index-K pages of
+ * [M31-RUBIN] (indexer_kv_dtype='nvfp4') hold these codes. */
+double oracle_e2m1(uint8_t nibble)
+{
+    int sign = (nibble >> 3) & 1;
+    int e = (nibble >> 1) & 3;
+    int m = nibble & 1;
+    double v;
+    if (e == 0)
+        v = 0.5 * m;
+    else
+        v = ldexp((double)(2 + m), e - 2); /* (1 + m/2) * 2^(e-1) */
+    return sign ? -v : v;
+}
+
+/* ---- paged gather ------------------------------------------------------- */
+
+/* Page holding logical block b of request r, or -1 if the table entry is out
+ * of the pool.  [M3-P128] "Description": one block table row per request
+ * maps each 128-token block to its page. */
+static int64_t page_of(const oracle_shape *s, const int32_t *block_table, int r, int64_t b)
+{
+    if (b < 0 || b >= s->max_blocks)
+        return -1;
+    int64_t page = block_table[(int64_t)r * s->max_blocks + b];
+    if (page < 0 || page >= s->num_pages)
+        return -1;
+    return page;
+}
+
+/* Index key of token `tok` of `page`, dimension d, dequantised.
+ * READING for NVFP4 (the pages give no byte layout): dimension 2i is the
+ * low nibble of byte i, one E4M3 scale covers 16 consecutive dimensions,
+ * and there is no second-level (global) scale. */
+static double index_key(const oracle_shape *s, const void *pool, const uint8_t *scales,
+                        int64_t page, int tok, int d)
+{
+    int64_t row = page * s->page_size + tok;
+    if (!s->index_nvfp4)
+        return oracle_bf16(((const uint16_t *)pool)[row * s->index_dim + d]);
+    uint8_t byte = ((const uint8_t *)pool)[row * (s->index_dim / 2) + d / 2];
+    uint8_t code = (d & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
+    double scale = oracle_e4m3(scales[row * (s->index_dim / 16) + d / 16]);
+    return oracle_e2m1(code) * scale;
+}
+
+static double kv_elem(const oracle_shape *s, const void *kv_pool, int64_t page, int kv, int g,
+                      int tok, int d)
+{
+    int64_t idx = (((page * 2 + kv) * s->num_kv_heads + g) * (int64_t)s->page_size + tok)
+                      * s->head_dim + d;
+    if (!s->kv_fp8)
+        return oracle_bf16(((const uint16_t *)kv_pool)[idx]);
+    return oracle_e4m3(((const uint8_t *)kv_pool)[idx]) * (kv ? s->v_scale : s->k_scale);
+}
+
+/* Causal limit: query token j of request r sees positions 0 .. seq_len+j-1.
+ * READING: a speculative step appends q_per_req tokens; token j is the j-th
+ * of them, so seq_lens[r] counts the positions its first token sees. */
+static int64_t visible(const oracle_shape *s, const int32_t *seq_lens, int t)
+{
+    int r = t / s->q_per_req, j = t % s->q_per_req;
+    return (int64_t)seq_lens[r] + j;
+}
+
+static int check_request(const oracle_shape *s, const int32_t *seq_lens, int r)
+{
+    int64_t cached = (int64_t)seq_lens[r] + s->q_per_req - 1;
+    if (seq_lens[r] < 1)
+        return ORACLE_BAD_SEQ_LEN;
+    if ((cached + s->page_size - 1) / s->page_size > s->max_blocks)
+        return ORACLE_BAD_SEQ_LEN;
+    return ORACLE_OK;
+}
+
+/* ---- (a) index score and per-block max ---------------------------------- */
+
+/* out[b] = max over visible positions pos of block b of the dot product of
+ * the token's index query with the index key at pos; -inf for a block with
+ * no visible position.  [M3-DECODE] "The TP4 decode target" (index scorer
+ * over index-K pages) and [M31-RUBIN] prefill-select commit (per-block
+ * "proxy" max score).  READING: the score is the plain dot product (no
+ * weights, activation or scaling appear on the pages). */
+int oracle_block_scores(const oracle_shape *s, const uint16_t *q_idx, const void *idxk_pool,
+                        const uint8_t *idxk_scales, const int32_t *block_table,
+                        const int32_t *seq_lens, int t, double *out)
+{
+    int r = t / s->q_per_req;
+    int rc = check_request(s, seq_lens, r);
+    if (rc)
+        return rc;
+    for (int b = 0; b < s->max_blocks; ++b)
+        out[b] = -INFINITY;
+    int64_t L = visible(s, seq_lens, t);
+    const uint16_t *qi = q_idx + (int64_t)t * s->index_dim;
+    for (int64_t pos = 0; pos < L; ++pos) {
+        int64_t b = pos / s->page_size;
+        int64_t page = page_of(s, block_table, r, b);
+        if (page < 0)
+            return ORACLE_BAD_PAGE;
+        double score = 0.0;
+        for (int d = 0; d < s->index_dim; ++d)
+            score += oracle_bf16(qi[d])
+                     * index_key(s, idxk_pool, idxk_scales, page, (int)(pos % s->page_size), d);
+        if (score > out[b])
+            out[b] = score;
+    }
+    return ORACLE_OK;
+}
+
+/* ---- (b) top-k block selection ------------------------------------------ */
+
+static const double *g_sort_scores; /* qsort context; guarded by the caller */
+
+static int by_score_then_index(const void *pa, const void *pb)
+{
+    int a = *(const int *)pa, b = *(const int *)pb;
+    double sa = g_sort_scores[a], sb = g_sort_scores[b];
+    if (sa > sb)
+        return -1;
+    if (sa < sb)
+        return 1;
+    return (a > b) - (a < b);
+}
+
+static int ascending(const void *pa, const void *pb)
+{
+    int a = *(const int *)pa, b = *(const int *)pb;
+    return (a > b) - (a < b);
+}
+
+/* Order blocks 0..n_valid-1 by score descending and, on equal scores, by
+ * block index ascending ([M3-DECODE] "The TP4 decode target": ties go to
+ * the smaller block); keep the first min(k, n_valid); write them in
+ * ascending block order followed by -1 up to k ([M31-RUBIN] q8kv4 indexer
+ * commit: "the ascending, -1-padded contract").  READING: only blocks that
+ * hold a visible position (finite score) are candidates. */
+int oracle_select(const double *scores, int n_valid, int k, int32_t *sel)
+{
+    int *order = (int *)malloc(sizeof(int) * (size_t)(n_valid > 0 ? n_valid : 1));
+    if (!order)
+        return ORACLE_NO_MEMORY;
+    for (int b = 0; b < n_valid; ++b)
+        order[b] = b;
+#ifdef _OPENMP
+#pragma omp critical(oracle_qsort)
+#endif
+    {
+        g_sort_scores = scores;
+        qsort(order, (size_t)n_valid, sizeof(int), by_score_then_index);
+    }
+    int keep = n_valid < k ? n_valid : k;
+    qsort(order, (size_t)keep, sizeof(int), ascending);
+    for (int i = 0; i < k; ++i)
+        sel[i] = i < keep ? order[i] : -1;
+    free(order);
+    return ORACLE_OK;
+}
+
+/* ---- (c) attention over the selected pages ------------------------------ */
+
+/* For every query head h (KV head g = h / (Hq/Hkv); READING: consecutive
+ * query heads share a KV head) attend over the visible positions of the
+ * selected blocks:
+ *   z_pos = softmax_scale * sum_d q[t,h,d] * K[g,pos,d]
+ *   O     = sum_pos e^(z_pos - M) V[g,pos,:] / sum_pos e^(z_pos - M)
+ *   LSE   = M + ln sum_pos e^(z_pos - M),   M = max_pos z_pos
+ * READING: the pages never define the LSE; this is the natural log of the
+ * softmax denominator of the scaled logits.  FP8 K and V are dequantised
+ * with their own per-tensor scale.  [M31-RUBIN] "Items and numerics"
+ * checks the split-K merge against a float64 reference; this is that
+ * reference with no split at all.  sel holds block indices (ascending,
+ * -1 padded), as produced by oracle_select. */
+int oracle_attend(const oracle_shape *s, const uint16_t *q, const void *kv_pool,
+                  const int32_t *block_table, const int32_t *seq_lens, int t,
+                  const int32_t *sel, double *out, double *lse)
+{
+    int r = t / s->q_per_req;
+    int rc = check_request(s, seq_lens, r);
+    if (rc)
+        return rc;
+    int64_t L = visible(s, seq_lens, t);
+    int P = s->page_size, D = s->head_dim;
+    int group = s->num_q_heads / s->num_kv_heads;
+
+    /* positions attended: the visible positions of the selected blocks */
+    int64_t npos = 0;
+    int64_t *pos_page = (int64_t *)malloc(sizeof(int64_t) * (size_t)s->topk * P);
+    int *pos_tok = (int *)malloc(sizeof(int) * (size_t)s->topk * P);
+    double *z = (double *)malloc(sizeof(double) * (size_t)s->topk * P);
+    if (!pos_page || !pos_tok || !z) {
+        free(pos_page); free(pos_tok); free(z);
+        return ORACLE_NO_MEMORY;
+    }
+    for (int i = 0; i < s->topk; ++i) {
+        int32_t b = sel[i];
+        if (b < 0)
+            continue;
+        int64_t page = page_of(s, block_table, r, b);
+        if (page < 0 || (int64_t)b * P >= L) {
+            free(pos_page); free(pos_tok); free(z);
+            return page < 0 ? ORACLE_BAD_PAGE : ORACLE_BAD_SELECTION;
+        }
+        for (int tok = 0; tok < P; ++tok) {
+            if ((int64_t)b * P + tok >= L)
+                break;
+            pos_page[npos] = page;
+            pos_tok[npos] = tok;
+            ++npos;
+        }
+    }
+
+    for (int h = 0; h < s->num_q_heads; ++h) {
+        int g = h / group;
+        const uint16_t *qh = q + ((int64_t)t * s->num_q_heads + h) * D;
+        double M = -INFINITY;
+        for (int64_t n = 0; n < npos; ++n) {
+            double acc = 0.0;
+            for (int d = 0; d < D; ++d)
+                acc += oracle_bf16(qh[d]) * kv_elem(s, kv_pool, pos_page[n], 0, g, pos_tok[n], d);
+            z[n] = s->softmax_scale * acc;
+            if (z[n] > M)
+                M = z[n];
+        }
+        double denom = 0.0;
+        double *o = out + (int64_t)h * D;
+        for (int d = 0; d < D; ++d)
+            o[d] = 0.0;
+        for (int64_t n = 0; n < npos; ++n) {
+            double w = exp(z[n] - M);
+            denom += w;
+            for (int d = 0; d < D; ++d)
+                o[d] += w * kv_elem(s, kv_pool, pos_page[n], 1, g, pos_tok[n], d);
+        }
+        for (int d = 0; d < D; ++d)
+            o[d] /= denom;
+        lse[h] = M + log(denom);
+    }
+    free(pos_page);
+    free(pos_tok);
+    free(z);
+    return ORACLE_OK;
+}
+
+/* ---- the whole step ------------------------------------------------------ */
+
+/* Runs (a), (b) and (c) for each token in tokens[0..n_tokens) and writes
+ * row i of every output for tokens[i]:
+ *   block_scores [n][max_blocks] float (every score is exact in binary32:
+ *                integer-valued or NVFP4 inputs; the test suite checks this)
+ *   selected     [n][topk]
+ *   out          [n][Hq][D] double,  lse [n][Hq] double
+ * num_threads > 1 spreads tokens over OpenMP threads (each token is still
+ * computed by one thread in the same order). */
+int oracle_decode_step(const oracle_shape *s, const uint16_t *q_idx, const void *idxk_pool,
+                       const uint8_t *idxk_scales, const uint16_t *q, const void *kv_pool,
+                       const int32_t *block_table, const int32_t *seq_lens,
+                       const int32_t *tokens, int n_tokens, int num_threads,
+                       float *block_scores, int32_t *selected, double *out, double *lse)
+{
+    int err = ORACLE_OK;
+#ifdef _OPENMP
+    if (num_threads < 1)
+        num_threads = 1;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads)
+#endif
+    for (int i = 0; i < n_tokens; ++i) {
+        int t = tokens[i];
+        double *bs = (double *)malloc(sizeof(double) * (size_t)s->max_blocks);
+        int rc = bs ? ORACLE_OK : ORACLE_NO_MEMORY;
+        if (!rc)
+            rc = oracle_block_scores(s, q_idx, idxk_pool, idxk_scales, block_table, seq_lens, t, bs);
+        if (!rc) {
+            int64_t L = visible(s, seq_lens, t);
+            int n_valid = (int)((L + s->page_size - 1) / s->page_size);
+            for (int b = 0; b < s->max_blocks; ++b)
+                block_scores[(int64_t)i * s->max_blocks + b] = (float)bs[b];
+            rc = oracle_select(bs, n_valid, s->topk, selected + (int64_t)i * s->topk);
+        }
+        if (!rc)
+            rc = oracle_attend(s, q, kv_pool, block_table, seq_lens, t,
+                               selected + (int64_t)i * s->topk,
+                               out + (int64_t)i * s->num_q_heads * s->head_dim,
+                               lse + (int64_t)i * s->num_q_heads);
+        free(bs);
+        if (rc) {
+#ifdef _OPENMP
+#pragma omp critical(oracle_err)
+#endif
+            err = rc;
+        }
+    }
+    return err;
+}
+
+/* Threads the OpenMP runtime would use by default (1 without OpenMP). */
+int oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
