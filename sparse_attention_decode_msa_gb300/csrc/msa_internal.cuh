@@ -1,0 +1,282 @@
+// msa_internal.cuh -- shared definitions of the kernels and the C-ABI layer.
+//
+// Device helpers are thin inline-PTX wrappers around sm_90+/sm_100 family
+// instructions (mbarrier, cp.async.bulk.tensor, ldmatrix, mma.sync,
+// packed fp8/fp4 converts).  Nothing here is a math-library routine.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "msa.h"
+
+namespace msa {
+
+constexpr int kPage = 128;       // tokens per page (P128)
+constexpr int kDim = 128;        // head_dim and index_dim
+constexpr int kGroup = 16;       // query heads per KV head
+constexpr int kMaxTokens = 8192; // T = R * q_per_req
+constexpr int kMaxBlocks = 16384;
+constexpr int kMaxTopk = 256;
+constexpr int kMaxQPerReq = 64;
+constexpr int kMaxRequests = 8192;
+constexpr int kDefaultCtaBound = 1024; // workspace bound on default persistent decode CTAs
+
+// Bits of the workspace error word.
+enum : uint32_t {
+    kErrPage = 1u,      // block table entry outside [0, num_pages)
+    kErrSeqLen = 2u,    // seq_len < 1, or cached blocks > max_blocks_per_seq
+    kErrSelection = 4u, // selected block id not a visible block of the token
+    kErrTimeout = 8u,   // a bounded wait ran out
+};
+
+// Bytes of one decode partial: o[16][128] then m[16], l[16] (fp32).
+constexpr size_t kPartialFloats = size_t(kGroup) * kDim + 2 * kGroup;
+constexpr size_t kPartialBytes = kPartialFloats * sizeof(float);
+
+struct WorkspaceLayout {
+    size_t scores_off;   // fp32 [T][maxB] (decode_step when block_scores == NULL)
+    size_t selected_off; // int32 [T][k]   (decode_step when selected == NULL)
+    size_t partial_off;  // decode partial slots
+    int64_t slots;
+    size_t total;
+};
+
+struct ScoreParams {
+    const uint16_t *q_idx;  // bf16 bits [T][Di]
+    const uint8_t *idxk;    // bf16 [pages][P][Di] or nvfp4 bytes [pages][P][Di/2]
+    const uint8_t *scales;  // E4M3 [pages][P][Di/16] (nvfp4)
+    const int32_t *block_table;
+    const int32_t *seq_lens;
+    float *block_scores;    // [T][maxB]
+    uint32_t *err;
+    int R, nq, maxB, num_pages;
+};
+
+struct SelectParams {
+    const float *block_scores;
+    const int32_t *seq_lens;
+    int32_t *selected;
+    uint32_t *err;
+    int R, nq, maxB, k;
+};
+
+struct DecodeParams {
+    const uint16_t *q; // bf16 bits [T][Hq][D]
+    const int32_t *block_table;
+    const int32_t *seq_lens;
+    const int32_t *selected; // [T][k]
+    uint16_t *out;           // bf16 bits [T][Hq][D]
+    float *lse;              // [T][Hq]
+    float *partial;          // slots of kPartialFloats
+    uint32_t *err;
+    int R, nq, T, Hkv, maxB, k, num_pages;
+    float scale_log2; // softmax_scale * log2(e) (* k_scale for FP8 keys)
+    float v_scale;    // 1 for bf16 values
+};
+
+// Host launchers (return the first CUDA error of the launch sequence).
+cudaError_t launch_index_score(const ScoreParams &p, int index_dtype, int num_sms,
+                               cudaStream_t stream);
+cudaError_t launch_select(const SelectParams &p, cudaStream_t stream);
+cudaError_t launch_sparse_decode(const DecodeParams &p, const void *kv_pool, int kv_dtype,
+                                 int ctas, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
+// device helpers
+
+#ifdef __CUDACC__
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void set_error(uint32_t *err, uint32_t bits)
+{
+    atomicOr(err, bits);
+}
+
+// ---- mbarrier ------------------------------------------------------------
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of the barrier; false if it did not complete
+// within ~2^31 SM clocks (about a second).
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const long long start = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - start > (1ll << 31))
+            return false;
+    }
+    return true;
+}
+
+// ---- TMA ------------------------------------------------------------------
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---- ldmatrix / mma -------------------------------------------------------
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+// D += A * B, m16n8k16, bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// D += A * B, m16n8k16, f16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                        uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// ---- conversions ------------------------------------------------------------
+
+// Two E4M3 codes (low byte -> low half) to f16x2.  Exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes)
+{
+    uint32_t out;
+    asm("{\n .reg .b16 t;\n cvt.u16.u32 t, %1;\n cvt.rn.f16x2.e4m3x2 %0, t;\n}\n"
+        : "=r"(out)
+        : "r"(two_codes));
+    return out;
+}
+
+// Two E2M1 codes in one byte (low nibble -> low half) to f16x2.  Exact.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte)
+{
+    uint32_t out;
+    asm("{\n .reg .b8 t;\n cvt.u8.u32 t, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;\n}\n"
+        : "=r"(out)
+        : "r"(byte));
+    return out;
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// f32 pair -> bf16x2 (lo from `lo`), round to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
+{
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// f32 pair -> f16x2 (lo from `lo`), round to nearest even.
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi)
+{
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// bf16x2 -> f16x2 via f32 (exact for values representable in both).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v)
+{
+    float lo = __uint_as_float(v << 16);
+    float hi = __uint_as_float(v & 0xFFFF0000u);
+    return pack_f16(lo, hi);
+}
+
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Monotone map of a float's bits to an unsigned key (larger float, larger key).
+__device__ __forceinline__ uint32_t order_key(float f)
+{
+    uint32_t u = __float_as_uint(f);
+    return u ^ ((u >> 31) ? 0xFFFFFFFFu : 0x80000000u);
+}
+
+__device__ __forceinline__ int ceil_div(int a, int b)
+{
+    return (a + b - 1) / b;
+}
+
+#endif // __CUDACC__
+
+} // namespace msa

@@ -1,0 +1,126 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol the header
+declares, sizes workspaces, and rejects bad shapes and arguments on the host
+before anything reaches the device."""
+
+import os
+import re
+
+import pytest
+
+import sparse_attention_decode_msa_gb300 as msa
+from sparse_attention_decode_msa_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "msa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return msa.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"^\s*(?:msa_status|size_t|const char \*)\s*(msa_\w+)\s*\(", text, re.M)
+
+
+def shape(**kw):
+    base = dict(num_requests=8, q_per_req=4, num_kv_heads=4, num_pages=4096,
+                max_blocks_per_seq=256, topk=16)
+    base.update(kw)
+    return msa.make_shape(**base)
+
+
+def test_header_declares_the_entry_points():
+    names = set(declared_functions())
+    assert {"msa_workspace_bytes", "msa_workspace_init", "msa_index_score", "msa_select_topk",
+            "msa_sparse_decode", "msa_decode_step", "msa_check_device_status",
+            "msa_status_string"} <= names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_exported_symbols_are_in_the_dynamic_table(lib):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in declared_functions():
+        assert name in exported, name
+
+
+def test_status_strings(lib):
+    assert msa.status_string(0) == "MSA_OK"
+    assert msa.status_string(2) == "MSA_ERR_UNSUPPORTED"
+    assert msa.status_string(99) == "MSA_ERR_UNKNOWN"
+
+
+def test_workspace_bytes_cover_the_layout(lib):
+    s = shape()
+    n = msa.msa_workspace_bytes(s)
+    T, maxB, k = 32, 256, 16
+    # error word + block scores + selection + (default CTA bound + units) partial slots
+    slot = (16 * 128 + 32) * 4
+    assert n >= 256 + T * maxB * 4 + T * k * 4 + (1024 + T * 4) * slot
+    assert n % 256 == 0
+    s.decode_ctas = 8
+    assert msa.msa_workspace_bytes(s) < n
+
+
+@pytest.mark.parametrize("field,value", [
+    ("head_dim", 64), ("index_dim", 64), ("page_size", 64), ("num_q_heads", 32),
+    ("num_index_heads", 2), ("kv_dtype", 2), ("index_dtype", 1), ("q_per_req", 65),
+    ("topk", 257), ("max_blocks_per_seq", 16385),
+])
+def test_unsupported_shapes_are_rejected(lib, field, value):
+    s = shape()
+    setattr(s, field, value)
+    assert msa.msa_workspace_bytes(s) == 0
+    st = lib.msa_index_score(msa.ctypes.byref(s), *([None] * 7), 0, None)
+    assert st == msa.MSA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("field,value", [
+    ("num_requests", -1), ("q_per_req", 0), ("topk", 0), ("num_pages", 0),
+    ("max_blocks_per_seq", 0), ("decode_ctas", -3),
+])
+def test_invalid_shapes_are_rejected(lib, field, value):
+    s = shape()
+    setattr(s, field, value)
+    assert msa.msa_workspace_bytes(s) == 0
+    st = lib.msa_decode_step(msa.ctypes.byref(s), *([None] * 11), None, 0, None)
+    assert st == msa.MSA_ERR_INVALID_ARGUMENT
+
+
+def test_null_and_misaligned_pointers_are_rejected_on_the_host(lib):
+    s = shape()
+    ws_bytes = msa.msa_workspace_bytes(s)
+    fake = 0x10000  # never dereferenced: validation fails first
+    args = [fake] * 7
+    # no workspace
+    assert lib.msa_sparse_decode(msa.ctypes.byref(s), *args, None, ws_bytes, None) == 1
+    # workspace too small
+    assert lib.msa_sparse_decode(msa.ctypes.byref(s), *args, fake, ws_bytes - 1, None) == 1
+    # a null input
+    bad = list(args)
+    bad[1] = None
+    assert lib.msa_sparse_decode(msa.ctypes.byref(s), *bad, fake, ws_bytes, None) == 1
+    # a misaligned input
+    bad = list(args)
+    bad[0] = fake + 2
+    assert lib.msa_sparse_decode(msa.ctypes.byref(s), *bad, fake, ws_bytes, None) == 1
+    # NVFP4 index keys need their scales
+    s4 = shape(index_dtype=2)
+    assert lib.msa_index_score(msa.ctypes.byref(s4), fake, fake, None, fake, fake, fake, fake,
+                               msa.msa_workspace_bytes(s4), None) == 1
+
+
+def test_zero_requests_is_a_validated_no_op(lib):
+    s = shape(num_requests=0)
+    ws_bytes = msa.msa_workspace_bytes(s)
+    fake = 0x10000
+    assert lib.msa_decode_step(msa.ctypes.byref(s), *([fake] * 11), fake, ws_bytes, None) == 0

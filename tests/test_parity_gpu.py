@@ -1,0 +1,276 @@
+"""Parity of the CUDA path with the CPU oracle, stage by stage and fused.
+
+Tolerances (the workload contract): block scores and selected tables are
+bit-exact; the bf16 output is within 4e-3 max abs of the float64 oracle and
+the LSE within 1e-4 * max(|lse|, 1).
+"""
+
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from sparse_attention_decode_msa_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+OUT_ATOL = 4e-3
+LSE_RTOL = 1e-4
+THREADS = max(1, min(32, os.cpu_count() or 1))
+
+
+@pytest.fixture(scope="session")
+def torch_cuda():
+    import torch
+
+    import sparse_attention_decode_msa_gb300 as msa
+    from sparse_attention_decode_msa_gb300 import build
+
+    build.build()
+    msa.load()
+    torch.cuda.init()
+    return torch
+
+
+def device_problem(pb, **kw):
+    from sparse_attention_decode_msa_gb300.runner import DeviceProblem
+
+    return DeviceProblem(pb, **kw)
+
+
+def assert_scores_equal(pb, gpu_bs, ref_bs, tokens):
+    nb = pb.blocks_per_request()
+    for i, t in enumerate(tokens):
+        n = int(nb[t // pb.q_per_req])
+        got, want = gpu_bs[t, :n], ref_bs[i, :n]
+        assert np.array_equal(got, want), (t, np.flatnonzero(got != want)[:8])
+
+
+def assert_attention_close(gpu_out, gpu_lse, ref_out, ref_lse, tokens):
+    out = gpu_out[tokens]
+    lse = gpu_lse[tokens]
+    assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
+    err = np.abs(out - ref_out).max()
+    assert err <= OUT_ATOL, f"max |dO| = {err}"
+    lerr = (np.abs(lse - ref_lse) / np.maximum(np.abs(ref_lse), 1.0)).max()
+    assert lerr <= LSE_RTOL, f"max rel |dLSE| = {lerr}"
+
+
+def check_device_ok(dp):
+    import sparse_attention_decode_msa_gb300 as msa
+
+    assert msa.msa_check_device_status(dp.ws) == msa.MSA_OK
+
+
+# ---------------------------------------------------------------------------
+# stage by stage, small copies of the five workloads
+
+
+@pytest.mark.parametrize("idx", range(5))
+def test_index_score_is_bit_exact(torch_cuda, idx):
+    pb = synth.make_small_workload(idx)
+    dp = device_problem(pb)
+    dp.index_score()
+    res = dp.results()
+    ref = oracle.decode_step(pb, threads=THREADS)
+    assert_scores_equal(pb, res["block_scores"], ref["block_scores"], range(pb.num_tokens))
+    check_device_ok(dp)
+
+
+@pytest.mark.parametrize("idx", range(5))
+def test_select_is_bit_exact_on_oracle_scores(torch_cuda, idx):
+    torch = torch_cuda
+    pb = synth.make_small_workload(idx)
+    ref = oracle.decode_step(pb, threads=THREADS)
+    dp = device_problem(pb)
+    bs = torch.from_numpy(ref["block_scores"][:, None, :].copy()).cuda()
+    dp.select(block_scores=bs)
+    res = dp.results()
+    assert np.array_equal(res["selected"], ref["selected"])
+    check_device_ok(dp)
+
+
+@pytest.mark.parametrize("idx", range(5))
+def test_sparse_decode_matches_oracle_on_oracle_selection(torch_cuda, idx):
+    torch = torch_cuda
+    pb = synth.make_small_workload(idx)
+    ref = oracle.decode_step(pb, threads=THREADS)
+    dp = device_problem(pb)
+    sel = torch.from_numpy(ref["selected"][:, None, :].copy()).cuda()
+    dp.sparse_decode(selected=sel)
+    res = dp.results()
+    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens))
+    check_device_ok(dp)
+
+
+@pytest.mark.parametrize("idx", range(5))
+def test_decode_step_matches_oracle(torch_cuda, idx):
+    pb = synth.make_small_workload(idx)
+    ref = oracle.decode_step(pb, threads=THREADS)
+    dp = device_problem(pb)
+    dp.decode_step()
+    res = dp.results()
+    tokens = range(pb.num_tokens)
+    assert_scores_equal(pb, res["block_scores"], ref["block_scores"], tokens)
+    assert np.array_equal(res["selected"], ref["selected"])
+    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], tokens)
+    check_device_ok(dp)
+
+
+# ---------------------------------------------------------------------------
+# the five workloads at full size, in the launch configuration the benchmark times
+
+
+@pytest.mark.parametrize("idx", range(5))
+def test_full_workload(torch_cuda, idx):
+    pb = synth.make_workload(idx)
+    dp = device_problem(pb)
+    dp.decode_step(keep_intermediates=True)
+    res = dp.results()
+    # every token: scores, selection; attention on every token of the small
+    # workloads and on a seeded sample of the big ones
+    T = pb.num_tokens
+    rng = np.random.default_rng(1234 + idx)
+    tokens = np.arange(T) if T <= 64 else np.sort(rng.choice(T, size=64, replace=False))
+    ref = oracle.decode_step(pb, tokens=tokens, threads=THREADS)
+    assert_scores_equal(pb, res["block_scores"], ref["block_scores"], tokens)
+    assert np.array_equal(res["selected"][tokens], ref["selected"])
+    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], tokens)
+    assert np.all(np.isfinite(res["out"])) and np.all(np.isfinite(res["lse"]))
+    check_device_ok(dp)
+
+
+# ---------------------------------------------------------------------------
+# properties and edge cases
+
+
+@pytest.mark.parametrize("idx", [1, 3])
+@pytest.mark.parametrize("ctas", [1, 2, 5, 37, 152, 600])
+def test_result_does_not_depend_on_the_split(torch_cuda, idx, ctas):
+    pb = synth.make_small_workload(idx)
+    ref = oracle.decode_step(pb, threads=THREADS)
+    dp = device_problem(pb, decode_ctas=ctas)
+    dp.decode_step()
+    res = dp.results()
+    assert np.array_equal(res["selected"], ref["selected"])
+    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens))
+    check_device_ok(dp)
+
+
+def test_repeated_steps_are_bitwise_identical(torch_cuda):
+    pb = synth.make_small_workload(2)
+    dp = device_problem(pb)
+    dp.decode_step()
+    a = dp.results()
+    dp.decode_step()
+    b = dp.results()
+    for key in a:
+        assert np.array_equal(a[key], b[key], equal_nan=True), key
+
+
+def test_select_random_rows_with_heavy_ties(torch_cuda):
+    torch = torch_cuda
+    import sparse_attention_decode_msa_gb300 as msa
+
+    rng = np.random.default_rng(77)
+    for k, maxB, R in [(1, 40, 64), (16, 1024, 48), (33, 700, 20), (256, 3000, 12), (7, 9216, 4)]:
+        seq_lens = rng.integers(1, maxB * 128 + 1, size=R).astype(np.int32)
+        scores = rng.integers(-3, 4, size=(R, 1, maxB)).astype(np.float32)
+        shape = msa.make_shape(num_requests=R, q_per_req=1, num_kv_heads=1, num_pages=1,
+                               max_blocks_per_seq=maxB, topk=k)
+        ws_bytes = msa.msa_workspace_bytes(shape)
+        ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+        sel = torch.empty((R, 1, k), dtype=torch.int32, device="cuda")
+        msa.msa_select_topk(shape, torch.from_numpy(scores).cuda(),
+                            torch.from_numpy(seq_lens).cuda(), sel, ws, ws_bytes)
+        got = sel.cpu().numpy()[:, 0]
+        for r in range(R):
+            n = -(-int(seq_lens[r]) // 128)
+            order = sorted(range(n), key=lambda b: (-scores[r, 0, b], b))
+            want = sorted(order[:k]) + [-1] * max(0, k - n)
+            assert got[r].tolist() == want, (k, maxB, r)
+        assert msa.msa_check_device_status(ws) == msa.MSA_OK
+
+
+def test_short_contexts_pad_with_minus_one_and_single_position(torch_cuda):
+    pb = synth.make_problem(name="short", contexts=[1, 2, 129, 300, 1000], q_per_req=1,
+                            num_kv_heads=2, topk=8, seed=21)
+    ref = oracle.decode_step(pb)
+    dp = device_problem(pb)
+    dp.decode_step()
+    res = dp.results()
+    assert res["selected"][0].tolist() == [0] + [-1] * 7
+    assert np.array_equal(res["selected"], ref["selected"])
+    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens))
+
+
+def test_page_aligned_contexts_and_dense_coverage(torch_cuda):
+    # contexts that are multiples of 128 and top-k covering every block (dense attention)
+    pb = synth.make_problem(name="aligned", contexts=[1024, 2048, 128], q_per_req=2,
+                            num_kv_heads=1, topk=16, seed=22)
+    ref = oracle.decode_step(pb)
+    dp = device_problem(pb)
+    dp.decode_step()
+    res = dp.results()
+    assert np.array_equal(res["selected"], ref["selected"])
+    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens))
+
+
+def test_all_zero_index_keys_tie_everywhere(torch_cuda):
+    pb = synth.make_problem(name="zeros", contexts=[5000, 3000], q_per_req=3, num_kv_heads=1,
+                            topk=16, seed=23)
+    pb.idxk_pool[:] = 0
+    ref = oracle.decode_step(pb)
+    dp = device_problem(pb)
+    dp.decode_step()
+    res = dp.results()
+    assert np.all(res["selected"] == np.arange(16))
+    assert np.array_equal(res["selected"], ref["selected"])
+    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens))
+
+
+def test_max_topk_and_wide_block_table(torch_cuda):
+    pb = synth.make_problem(name="wide", contexts=[40000], q_per_req=2, num_kv_heads=1,
+                            topk=256, max_blocks=4000, seed=24)
+    ref = oracle.decode_step(pb, threads=THREADS)
+    dp = device_problem(pb)
+    dp.decode_step()
+    res = dp.results()
+    assert np.array_equal(res["selected"], ref["selected"])
+    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens))
+
+
+def test_large_speculative_step(torch_cuda):
+    pb = synth.make_problem(name="nq64", contexts=[3000], q_per_req=64, num_kv_heads=1, topk=8,
+                            index_range=(-2, 2), seed=25)
+    ref = oracle.decode_step(pb, threads=THREADS)
+    dp = device_problem(pb)
+    dp.decode_step()
+    res = dp.results()
+    assert_scores_equal(pb, res["block_scores"], ref["block_scores"], range(pb.num_tokens))
+    assert np.array_equal(res["selected"], ref["selected"])
+    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens))
+
+
+def test_bad_page_id_is_reported_not_faulted(torch_cuda):
+    import sparse_attention_decode_msa_gb300 as msa
+
+    pb = synth.make_problem(name="badpage", contexts=[700], q_per_req=1, num_kv_heads=1, topk=4,
+                            seed=26)
+    pb.block_table[0, 2] = pb.num_pages + 5   # out of the pool: the kernels must not read it
+    dp = device_problem(pb)
+    dp.decode_step()
+    assert msa.msa_check_device_status(dp.ws) == msa.MSA_ERR_DEVICE_CHECK
+    assert msa.msa_check_device_status(dp.ws) == msa.MSA_OK   # the check clears the word
+
+
+def test_bad_seq_len_is_reported_not_faulted(torch_cuda):
+    import sparse_attention_decode_msa_gb300 as msa
+
+    pb = synth.make_problem(name="badlen", contexts=[700, 900], q_per_req=1, num_kv_heads=1,
+                            topk=4, seed=27)
+    pb.seq_lens[1] = pb.max_blocks * 128 + 1   # more blocks than the table holds
+    dp = device_problem(pb)
+    dp.decode_step()
+    assert msa.msa_check_device_status(dp.ws) == msa.MSA_ERR_DEVICE_CHECK
