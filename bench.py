@@ -1,0 +1,516 @@
+"""Benchmark of the fused block-sparse decode step (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config IDX] [--impl ours|reference]
+
+A step is one msa_decode_step over the whole batch of the workload (index
+score + block max, top-k select, sparse GQA decode + merge).  Timing:
+
+* value / ms_per_step: K back-to-back replays of a CUDA graph of the step,
+  bracketed by CUDA events on the launching stream.  The workload's KV and
+  index-K pools (and the step inputs) exist in several device copies that the
+  steps cycle through, sized so that at least 4x the 129 MB L2 of other data
+  is touched between two uses of the same copy: every step reads its inputs
+  from HBM.
+* stage times: the same protocol per stage (score, select, decode + merge),
+  used for the roofline of the dominant kernel.
+* e2e: the public C-ABI call with host inputs: per step a copy of the step's
+  inputs (q, q_idx, block table, seq_lens) from pinned host memory, the call,
+  and a copy of out + lse back to pinned host memory, all on one stream.
+  The KV and index-K pools are cache state and stay resident.
+* cpu_baseline / --impl reference: the CPU oracle on the host cores over a
+  bounded sample of the same workload's tokens.
+
+Multi-GPU (torchrun): every rank runs an independent replica of the
+workload (the path has no exchange step); barrier + max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+L2_BYTES = 129 * 1000 * 1000
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# helpers shared with the multi-rank tests
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reduce_max(value: float, world: int) -> float:
+    """Max of a float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(units_per_rank: int, world: int, max_seconds: float) -> float:
+    """Weak-scaling job throughput: units all ranks processed / slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+def hbm_peak():
+    try:
+        with open(PEAKS_PATH) as f:
+            v = json.load(f).get("hbm_gbs")
+        if v:
+            return float(v), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key: str, workload: str, src_files):
+    """DRAM bytes per launch of a kernel from a committed ncu summary, or None
+    if there is none for this workload or the kernel source changed since."""
+    try:
+        with open(TRAFFIC_PATH) as f:
+            rec = json.load(f).get(f"{kernel_key}:{workload}")
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("source_digest") != source_digest(src_files):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples in a background thread."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.marks = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == 7:
+                self.samples.append((time.time(), parts))
+
+    def window(self, t0, t1):
+        return [p for (t, p) in self.samples if t0 <= t <= t1]
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    @staticmethod
+    def summarize(samples, label):
+        if not samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": label}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(s[0]) for s in samples if num(s[0]) is not None]
+        mx = [num(s[1]) for s in samples if num(s[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in samples for i in range(4) if s[3 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(samples), "window": label}
+
+
+# ---------------------------------------------------------------------------
+# workload accounting
+
+
+def algorithmic_bytes(pb, selected: np.ndarray) -> dict:
+    """Bytes the method must move for one step (see the design notes).
+
+    index: the index key of every cached token once per request;
+    kv: per (request, KV head) the union over the request's query tokens of
+        the selected pages (K page + V page of that head);
+    small: q, q_idx, out, lse, the block-table rows used, seq_lens."""
+    ctx = pb.contexts
+    per_tok = 256 if pb.index_dtype == "bf16" else 64 + 8
+    index = int(ctx.sum()) * per_tok
+    page_head = 2 * 128 * 128 * (2 if pb.kv_dtype == "bf16" else 1)
+    union_pages = 0
+    for r in range(pb.num_requests):
+        rows = selected[r * pb.q_per_req:(r + 1) * pb.q_per_req].ravel()
+        union_pages += len(np.unique(rows[rows >= 0]))
+    kv = union_pages * pb.num_kv_heads * page_head
+    T, Hq = pb.num_tokens, pb.num_q_heads
+    nb = pb.blocks_per_request()
+    small = T * Hq * 128 * 2 * 2 + T * 128 * 2 + T * Hq * 4 + int(nb.sum()) * 4 + pb.num_requests * 4
+    scores_io = int(nb.sum()) * pb.q_per_req * 4  # block scores written once
+    return {"index": index, "kv": kv, "small": small, "scores_io": scores_io,
+            "total": index + kv + small, "union_pages": union_pages,
+            "sum_selected_pages": int((selected >= 0).sum())}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    import sparse_attention_decode_msa_gb300 as msa
+    from sparse_attention_decode_msa_gb300 import build as libbuild
+    from sparse_attention_decode_msa_gb300 import synth
+    from sparse_attention_decode_msa_gb300.runner import DeviceProblem
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    libbuild.build()
+    msa.load()
+
+    idx = args.config
+    pb = synth.make_workload(idx, seed=idx + 1000 * rank)
+    base = DeviceProblem(pb, device=f"cuda:{local}")
+    base.decode_step()
+    torch.cuda.synchronize()
+    status = msa.msa_check_device_status(base.ws)
+    if status != msa.MSA_OK:
+        raise RuntimeError(f"device check failed: {msa.status_string(status)}")
+    sel = base.selected[:, 0].cpu().numpy()
+    nbytes = algorithmic_bytes(pb, sel)
+
+    # device copies so that no step finds its inputs in L2
+    nrep = max(2, math.ceil(4 * L2_BYTES / max(1, nbytes["total"])) + 1)
+    reps = [base] + [base.replicate() for _ in range(nrep - 1)]
+    stream = torch.cuda.Stream()
+
+    def capture(fn):
+        graphs = []
+        for dp in reps:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                fn(dp, stream)  # warm (attribute setup) outside capture
+                stream.synchronize()
+                with torch.cuda.graph(g, stream=stream):
+                    fn(dp, stream)
+            graphs.append(g)
+        torch.cuda.synchronize()
+        return graphs
+
+    def step_fn(dp, s):
+        dp.decode_step(keep_intermediates=False, stream=s.cuda_stream)
+
+    step_graphs = capture(step_fn)
+    stage_graphs = {
+        "index_score": capture(lambda dp, s: dp.index_score(stream=s.cuda_stream)),
+        "select_topk": capture(lambda dp, s: dp.select(stream=s.cuda_stream)),
+        "sparse_decode": capture(lambda dp, s: dp.sparse_decode(stream=s.cuda_stream)),
+    }
+
+    def timed_replays(graphs, k):
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for i in range(k):
+                graphs[i % len(graphs)].replay()
+            ev1.record(stream)
+        ev1.synchronize()
+        return ev0.elapsed_time(ev1) / k  # ms per replay
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+
+    for i in range(args.warmup):
+        step_graphs[i % nrep].replay()
+    torch.cuda.synchronize()
+
+    # ---- the timed region: exactly K steps ----
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_start = time.time()
+    ms_step = timed_replays(step_graphs, args.steps)
+    torch.cuda.synchronize()
+    t_end = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    ms_step_max = reduce_max(ms_step, world)
+
+    # ---- clock soak: the same replays for >= 1.5 s if the timed region was short ----
+    soak_label = "timed region"
+    if t_end - t_start < 1.5:
+        n = max(1, int(1.5e3 / max(ms_step, 1e-3)))
+        ts0 = time.time()
+        timed_replays(step_graphs, n)
+        t_end2 = time.time()
+        soak_label = f"timed region + {t_end2 - ts0:.1f} s of the same replays right after it"
+        t_end = t_end2
+
+    # ---- per-stage times (same protocol) ----
+    k_stage = max(args.steps, 50)
+    stage_ms = {}
+    for name, graphs in stage_graphs.items():
+        for i in range(5):
+            graphs[i % nrep].replay()
+        stage_ms[name] = timed_replays(graphs, k_stage)
+
+    # ---- e2e through the public C ABI with pinned host buffers ----
+    host = []
+    for dp in reps:
+        host.append({
+            "q": dp.q.cpu().pin_memory(), "q_idx": dp.q_idx.cpu().pin_memory(),
+            "bt": dp.block_table.cpu().pin_memory(), "sl": dp.seq_lens.cpu().pin_memory(),
+            "out": torch.empty(dp.out.shape, dtype=dp.out.dtype).pin_memory(),
+            "lse": torch.empty(dp.lse.shape, dtype=dp.lse.dtype).pin_memory(),
+        })
+    h2d = sum(int(host[0][k].numel() * host[0][k].element_size()) for k in ("q", "q_idx", "bt", "sl"))
+    d2h = sum(int(host[0][k].numel() * host[0][k].element_size()) for k in ("out", "lse"))
+
+    def e2e_step(i):
+        dp, h = reps[i % nrep], host[i % nrep]
+        dp.q.copy_(h["q"], non_blocking=True)
+        dp.q_idx.copy_(h["q_idx"], non_blocking=True)
+        dp.block_table.copy_(h["bt"], non_blocking=True)
+        dp.seq_lens.copy_(h["sl"], non_blocking=True)
+        dp.decode_step(keep_intermediates=False, stream=stream.cuda_stream)
+        h["out"].copy_(dp.out, non_blocking=True)
+        h["lse"].copy_(dp.lse, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            e2e_step(i)
+        stream.synchronize()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for i in range(args.steps):
+            e2e_step(i)
+        ev1.record(stream)
+    ev1.synchronize()
+    e2e_ms = reduce_max(ev0.elapsed_time(ev1) / args.steps, world)
+    sampler.stop()
+    clocks = ClockSampler.summarize(sampler.window(t_start - 0.05, t_end + 0.05), soak_label)
+
+    T = pb.num_tokens
+    value = aggregate_throughput(T, world, ms_step_max / 1e3)
+    e2e_value = aggregate_throughput(T, world, e2e_ms / 1e3)
+
+    # roofline of the dominant kernel
+    peak, peak_src = hbm_peak()
+    dominant = max(("index_score", "sparse_decode"), key=lambda k: stage_ms[k])
+    if dominant == "sparse_decode":
+        dom_bytes = nbytes["kv"] + nbytes["small"]
+        src = ["sparse_attention_decode_msa_gb300/csrc/msa_decode.cu",
+               "sparse_attention_decode_msa_gb300/csrc/msa_internal.cuh"]
+        kernel_key = "sparse_decode_kernel"
+    else:
+        dom_bytes = nbytes["index"] + nbytes["scores_io"] + T * 256
+        src = ["sparse_attention_decode_msa_gb300/csrc/msa_score.cu",
+               "sparse_attention_decode_msa_gb300/csrc/msa_internal.cuh"]
+        kernel_key = "index_score_kernel"
+    achieved = dom_bytes / (stage_ms[dominant] / 1e3) / 1e9
+
+    result = {
+        "metric": "decode query-tokens/s",
+        "value": round(value, 1),
+        "unit": "query-tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step_max, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp8-e4m3 KV / bf16 Q" if pb.kv_dtype == "fp8" else "bf16",
+        "data": "synthetic (seeded; see config.recipe)",
+        "config": {
+            "workload": f"{pb.name} (workload {idx})",
+            "recipe": pb.recipe,
+            "requests": pb.num_requests, "q_per_req": pb.q_per_req, "tokens": T,
+            "kv_heads": pb.num_kv_heads, "q_heads": pb.num_q_heads, "topk": pb.topk,
+            "kv_dtype": pb.kv_dtype, "index_dtype": pb.index_dtype,
+            "l2": (f"inputs larger than L2: {nrep} device copies of the pools cycled, "
+                   f"{(nrep - 1) * nbytes['total'] / 1e6:.0f} MB touched between reuses of a copy"),
+            "timing": "CUDA-graph replays of msa_decode_step, CUDA events on the launch stream",
+        },
+        "fused_step_us": round(ms_step_max * 1e3, 2),
+        "algorithmic_bytes": nbytes,
+        "achieved_gbps": round(nbytes["total"] / (ms_step_max / 1e3) / 1e9, 1),
+        "frac_of_8tbs": round(nbytes["total"] / (ms_step_max / 1e3) / 8e12, 4),
+        "stages_us": {k: round(v * 1e3, 2) for k, v in stage_ms.items()},
+        "roofline": {
+            "kernel": kernel_key + (" (+ merge kernel)" if dominant == "sparse_decode" else ""),
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_source": f"{peak_src} HBM copy GB/s",
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": ncu_traffic(kernel_key, pb.name, src),
+            "algorithmic_bytes_per_launch": dom_bytes,
+        },
+        "e2e": {"value": round(e2e_value, 1), "unit": "query-tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 5)},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(pb, budget_s=args.cpu_seconds)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle
+
+
+def oracle_tokens_per_second(pb, budget_s: float, threads: int, sample_tokens=None):
+    import oracle
+
+    T = pb.num_tokens
+    if sample_tokens is None:
+        sample_tokens = min(T, threads)
+    rng = np.random.default_rng(0)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        toks = rng.choice(T, size=sample_tokens, replace=False).astype(np.int32)
+        oracle.decode_step(pb, tokens=toks, threads=threads)
+        done += sample_tokens
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            return done / el, done, el
+
+
+def cpu_baseline(pb, budget_s=15.0):
+    import oracle
+
+    threads = max(1, os.cpu_count() or 1)
+    oracle.build()
+    v, n, el = oracle_tokens_per_second(pb, budget_s, threads)
+    return {"value": round(v, 2), "unit": "query-tokens/s", "cores": threads, "kind": "oracle",
+            "sample": (f"{n} query tokens of the same workload drawn at random (whole fused step "
+                       f"per token: index score of every cached token, select, attention) in "
+                       f"{el:.1f} s, OpenMP over tokens")}
+
+
+def run_reference(args, rank, world, local):
+    """The oracle as the reference arm: K steps, each a bounded token sample."""
+    if rank != 0:
+        return
+    import oracle
+    from sparse_attention_decode_msa_gb300 import synth
+
+    oracle.build()
+    idx = args.config
+    pb = synth.make_workload(idx)
+    threads = max(1, os.cpu_count() or 1)
+    rng = np.random.default_rng(0)
+    # size the per-step sample so the whole run stays within ~3 minutes
+    probe_t0 = time.perf_counter()
+    oracle.decode_step(pb, tokens=np.array([0], dtype=np.int32), threads=1)
+    per_token = max(1e-4, time.perf_counter() - probe_t0)
+    budget = 180.0 / max(1, args.steps + args.warmup)
+    per_step = max(1, min(pb.num_tokens, threads, int(budget * threads / per_token)))
+    for _ in range(args.warmup):
+        oracle.decode_step(pb, tokens=rng.choice(pb.num_tokens, per_step, replace=False).astype(np.int32),
+                           threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.decode_step(pb, tokens=rng.choice(pb.num_tokens, per_step, replace=False).astype(np.int32),
+                           threads=threads)
+    el = time.perf_counter() - t0
+    value = per_step * args.steps / el
+    sample = (f"{per_step} random query tokens of the workload per step (whole fused step per "
+              f"token), {args.steps} steps in {el:.1f} s, OpenMP over tokens")
+    print(json.dumps({
+        "impl": "reference", "metric": "decode query-tokens/s", "value": round(value, 3),
+        "unit": "query-tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{pb.name} (workload {idx})", "recipe": pb.recipe},
+        "cpu_baseline": {"value": round(value, 3), "unit": "query-tokens/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "query-tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=1, help="workload 0..4 (default 1: spec-verify)")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world, local)
+    else:
+        run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -267,8 +267,6 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             comb_l[warp * kGroup + g8] = l_run[0];
             comb_l[warp * kGroup + g8 + 8] = l_run[1];
         }
-        for (int e = threadIdx.x; e < kGroup * kDim; e += kDecThreads)
-            comb_o[e] = 0.f;
         __syncthreads();
         float fac[2];
 #pragma unroll
@@ -280,16 +278,24 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 M = fmaxf(M, comb_m[w * kGroup + row]);
             fac[h] = (M == -INFINITY) ? 0.f : ex2(m_run[h] - M);
         }
+        // fixed order (warp 0, 1, 2, 3), no atomics: bitwise reproducible
+        for (int w = 0; w < 4; ++w) {
+            if (warp == w) {
 #pragma unroll
-        for (int n = 0; n < 16; ++n) {
+                for (int n = 0; n < 16; ++n) {
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                const int d = o_dim<FP8>(n, 2 * q4 + cc);
-                atomicAdd(&comb_o[g8 * kDim + d], o[n][cc] * fac[0]);
-                atomicAdd(&comb_o[(g8 + 8) * kDim + d], o[n][2 + cc] * fac[1]);
+                    for (int cc = 0; cc < 2; ++cc) {
+                        const int d = o_dim<FP8>(n, 2 * q4 + cc);
+                        float *a = &comb_o[g8 * kDim + d];
+                        float *b = &comb_o[(g8 + 8) * kDim + d];
+                        const float va = o[n][cc] * fac[0], vb = o[n][2 + cc] * fac[1];
+                        *a = w == 0 ? va : *a + va;
+                        *b = w == 0 ? vb : *b + vb;
+                    }
+                }
             }
+            __syncthreads();
         }
-        __syncthreads();
         // unit bookkeeping
         const long long Pt = qt[p.T];
         const long long u_first = (long long)tk.g * Pt + qt[tk.t];
@@ -575,11 +581,17 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
     const float *base = p.partial + (size_t)(c_first + u) * kPartialFloats;
 
     const int row = threadIdx.x >> 4, d0 = (threadIdx.x & 15) * 8;
+    // With more CTAs than tasks some CTAs inside [c_first, c_last] own no task
+    // and write no slot: skip them.
+    auto empty = [&](int cc) { return (long long)cc * P / G == (long long)(cc + 1) * P / G; };
     float M = -INFINITY;
     for (int s = 0; s < nslots; ++s)
-        M = fmaxf(M, base[(size_t)s * kPartialFloats + kGroup * kDim + row]);
+        if (!empty(c_first + s))
+            M = fmaxf(M, base[(size_t)s * kPartialFloats + kGroup * kDim + row]);
     float L = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int s = 0; s < nslots; ++s) {
+        if (empty(c_first + s))
+            continue;
         const float *sl = base + (size_t)s * kPartialFloats;
         const float ms = sl[kGroup * kDim + row];
         const float w = (M == -INFINITY) ? 0.f : ex2(ms - M);

@@ -52,6 +52,22 @@ class DeviceProblem:
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
         msa_workspace_init(self.ws, self.ws_bytes)
 
+    def replicate(self) -> "DeviceProblem":
+        """A copy of every buffer at new device addresses (same bytes)."""
+        import copy
+
+        import torch
+
+        dp = copy.copy(self)
+        for name in ("q_idx", "idxk", "idxk_scales", "q", "kv", "block_table", "seq_lens",
+                     "block_scores", "selected", "out", "lse"):
+            t = getattr(self, name)
+            setattr(dp, name, None if t is None else t.clone())
+        dp.shape = type(self.shape).from_buffer_copy(self.shape)
+        dp.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
+        msa_workspace_init(dp.ws, dp.ws_bytes)
+        return dp
+
     def set_decode_ctas(self, n: int):
         import torch
 

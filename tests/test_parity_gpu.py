@@ -47,12 +47,27 @@ def assert_scores_equal(pb, gpu_bs, ref_bs, tokens):
         assert np.array_equal(got, want), (t, np.flatnonzero(got != want)[:8])
 
 
-def assert_attention_close(gpu_out, gpu_lse, ref_out, ref_lse, tokens):
+def half_ulp_bf16(x):
+    """Half a bf16 ulp at |x|: the most that rounding the output to bf16 can add."""
+    _, e = np.frexp(np.abs(x))
+    return np.where(x == 0, 0.0, np.ldexp(1.0, e - 9))
+
+
+def assert_attention_close(gpu_out, gpu_lse, ref_out, ref_lse, tokens, strict=True):
+    """strict: |dO| <= 4e-3 everywhere (holds when |O| < 2, as in every
+    workload).  Otherwise 4e-3 of accumulation error plus the bf16 rounding
+    of the stored output, which alone reaches 7.8e-3 once |O| >= 2 (a
+    softmax over one or two N(0,1) values)."""
     out = gpu_out[tokens]
     lse = gpu_lse[tokens]
     assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
-    err = np.abs(out - ref_out).max()
-    assert err <= OUT_ATOL, f"max |dO| = {err}"
+    diff = np.abs(out - ref_out)
+    if strict:
+        err = diff.max()
+        assert err <= OUT_ATOL, f"max |dO| = {err}"
+    else:
+        excess = (diff - OUT_ATOL - half_ulp_bf16(ref_out)).max()
+        assert excess <= 0, f"max |dO| beyond 4e-3 + half bf16 ulp: {excess}"
     lerr = (np.abs(lse - ref_lse) / np.maximum(np.abs(ref_lse), 1.0)).max()
     assert lerr <= LSE_RTOL, f"max rel |dLSE| = {lerr}"
 
@@ -202,7 +217,8 @@ def test_short_contexts_pad_with_minus_one_and_single_position(torch_cuda):
     res = dp.results()
     assert res["selected"][0].tolist() == [0] + [-1] * 7
     assert np.array_equal(res["selected"], ref["selected"])
-    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens))
+    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens),
+                           strict=False)
 
 
 def test_page_aligned_contexts_and_dense_coverage(torch_cuda):
@@ -214,7 +230,8 @@ def test_page_aligned_contexts_and_dense_coverage(torch_cuda):
     dp.decode_step()
     res = dp.results()
     assert np.array_equal(res["selected"], ref["selected"])
-    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens))
+    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens),
+                           strict=False)
 
 
 def test_all_zero_index_keys_tie_everywhere(torch_cuda):
@@ -227,7 +244,8 @@ def test_all_zero_index_keys_tie_everywhere(torch_cuda):
     res = dp.results()
     assert np.all(res["selected"] == np.arange(16))
     assert np.array_equal(res["selected"], ref["selected"])
-    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens))
+    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens),
+                           strict=False)
 
 
 def test_max_topk_and_wide_block_table(torch_cuda):
@@ -238,7 +256,8 @@ def test_max_topk_and_wide_block_table(torch_cuda):
     dp.decode_step()
     res = dp.results()
     assert np.array_equal(res["selected"], ref["selected"])
-    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens))
+    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens),
+                           strict=False)
 
 
 def test_large_speculative_step(torch_cuda):
@@ -250,7 +269,8 @@ def test_large_speculative_step(torch_cuda):
     res = dp.results()
     assert_scores_equal(pb, res["block_scores"], ref["block_scores"], range(pb.num_tokens))
     assert np.array_equal(res["selected"], ref["selected"])
-    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens))
+    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens),
+                           strict=False)
 
 
 def test_bad_page_id_is_reported_not_faulted(torch_cuda):
