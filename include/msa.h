@@ -177,6 +177,34 @@ msa_status msa_decode_step(const msa_shape *shape, const void *q_idx, const void
                            float *block_scores, int32_t *selected, void *out, float *lse,
                            void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* Size of the fixed device scratch used by msa_sparse_decode_noalloc. */
+#define MSA_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* The paper has no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory: a plugin handed only its input and
+ * output tensors by a runtime that owns every device allocation, or code on
+ * a path where the allocator may not be called.  It computes exactly what
+ * msa_sparse_decode computes, with the same kernels, but keeps the scratch
+ * (split partials and the error word) in a fixed array of
+ * MSA_NOALLOC_SCRATCH_BYTES compiled into the library, which every GPU that
+ * loads the library holds until the process exits.  It allocates nothing.
+ *   - The first call on each device looks up that device's copy of the array
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - All calls share the one array: calls whose work overlaps on the GPU
+ *     (different streams, or different host threads) race and give wrong
+ *     results.  Each call clears the error word it needs; the partial slots
+ *     are always written before they are read.
+ *   - Device-side bounds failures are not reported (there is no workspace to
+ *     read them from); use msa_sparse_decode for that.
+ *   - Returns MSA_ERR_UNSUPPORTED when (decode CTAs + num_requests *
+ *     q_per_req * num_kv_heads) partial slots of 8320 bytes, plus 256, exceed
+ *     MSA_NOALLOC_SCRATCH_BYTES (with the default CTA count on a 152-SM GPU:
+ *     at most 856 (token, KV head) pairs). */
+msa_status msa_sparse_decode_noalloc(const msa_shape *shape, const void *q, const void *kv_pool,
+                                     const int32_t *block_table, const int32_t *seq_lens,
+                                     const int32_t *selected, void *out, float *lse,
+                                     cudaStream_t stream);
+
 /* Synchronise `stream`, read the workspace's error word and clear it.
  * Returns MSA_OK, MSA_ERR_DEVICE_CHECK, MSA_ERR_TIMEOUT or MSA_ERR_CUDA. */
 msa_status msa_check_device_status(void *workspace, cudaStream_t stream);
