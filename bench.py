@@ -232,6 +232,8 @@ def run_ours(args, rank, world, local):
 
     # device copies so that no step finds its inputs in L2
     nrep = max(2, math.ceil(4 * L2_BYTES / max(1, nbytes["total"])) + 1)
+    if args.replicas:
+        nrep = args.replicas  # profiling runs: fewer device copies (ncu flushes caches itself)
     reps = [base] + [base.replicate() for _ in range(nrep - 1)]
     stream = torch.cuda.Stream()
 
@@ -502,6 +504,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--replicas", type=int, default=0,
+                    help="device copies of the pools (default: enough that inputs exceed L2); "
+                         "small values are for ncu captures only")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

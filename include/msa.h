@@ -133,8 +133,9 @@ typedef struct msa_shape {
  * shape is invalid or unsupported).  Pure host function. */
 size_t msa_workspace_bytes(const msa_shape *shape);
 
-/* Zero the workspace's error word.  Call once after allocating it (any
- * later call leaves it clear unless a kernel reports an error). */
+/* Zero the workspace (error word and the decode's split-arrival counters).
+ * Call once after allocating it, and again after a call reported
+ * MSA_ERR_TIMEOUT; every other call leaves the counters at zero. */
 msa_status msa_workspace_init(void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Stage (a): block_scores[t][0][b] = max over the visible positions of
@@ -196,10 +197,11 @@ msa_status msa_decode_step(const msa_shape *shape, const void *q_idx, const void
  *     are always written before they are read.
  *   - Device-side bounds failures are not reported (there is no workspace to
  *     read them from); use msa_sparse_decode for that.
- *   - Returns MSA_ERR_UNSUPPORTED when (decode CTAs + num_requests *
- *     q_per_req * num_kv_heads) partial slots of 8320 bytes, plus 256, exceed
- *     MSA_NOALLOC_SCRATCH_BYTES (with the default CTA count on a 152-SM GPU:
- *     at most 856 (token, KV head) pairs). */
+ *   - Returns MSA_ERR_UNSUPPORTED when the scratch it needs exceeds
+ *     MSA_NOALLOC_SCRATCH_BYTES: 256 bytes of error word, a 4-byte counter per
+ *     (token, KV head) pair rounded up to 256 bytes, and (decode CTAs + pairs)
+ *     partial slots of 8320 bytes (with the default CTA count on a 152-SM
+ *     GPU: at most 855 (token, KV head) pairs). */
 msa_status msa_sparse_decode_noalloc(const msa_shape *shape, const void *q, const void *kv_pool,
                                      const int32_t *block_table, const int32_t *seq_lens,
                                      const int32_t *selected, void *out, float *lse,

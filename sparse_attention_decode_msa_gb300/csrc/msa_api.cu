@@ -65,6 +65,8 @@ WorkspaceLayout layout_of(const msa_shape *s)
     const size_t T = (size_t)tokens_of(s);
     WorkspaceLayout w;
     size_t off = kAlign; // error word
+    w.counters_off = off;
+    off = align_up(off + T * s->num_kv_heads * sizeof(int32_t));
     w.scores_off = off;
     off = align_up(off + T * s->max_blocks_per_seq * sizeof(float));
     w.selected_off = off;
@@ -131,7 +133,7 @@ msa_status score_impl(const msa_shape *s, const void *q_idx, const void *idxk_po
 }
 
 msa_status select_impl(const msa_shape *s, const float *block_scores, const int32_t *seq_lens,
-                       int32_t *selected, void *ws, cudaStream_t stream)
+                       int32_t *selected, void *ws, cudaStream_t stream, bool pdl)
 {
     SelectParams p;
     p.block_scores = block_scores;
@@ -142,13 +144,13 @@ msa_status select_impl(const msa_shape *s, const float *block_scores, const int3
     p.nq = s->q_per_req;
     p.maxB = s->max_blocks_per_seq;
     p.k = s->topk;
-    return cuda_status(launch_select(p, stream));
+    return cuda_status(launch_select(p, stream, pdl));
 }
 
 msa_status decode_impl(const msa_shape *s, const void *q, const void *kv_pool,
                        const int32_t *block_table, const int32_t *seq_lens,
                        const int32_t *selected, void *out, float *lse, void *ws,
-                       cudaStream_t stream)
+                       cudaStream_t stream, bool pdl)
 {
     const WorkspaceLayout w = layout_of(s);
     DecodeParams p;
@@ -159,6 +161,7 @@ msa_status decode_impl(const msa_shape *s, const void *q, const void *kv_pool,
     p.out = static_cast<uint16_t *>(out);
     p.lse = lse;
     p.partial = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + w.partial_off);
+    p.counters = reinterpret_cast<int *>(static_cast<uint8_t *>(ws) + w.counters_off);
     p.err = static_cast<uint32_t *>(ws);
     p.R = s->num_requests;
     p.nq = s->q_per_req;
@@ -180,7 +183,7 @@ msa_status decode_impl(const msa_shape *s, const void *q, const void *kv_pool,
         if (ctas > max_tasks)
             ctas = (int)max_tasks;
     }
-    return cuda_status(launch_sparse_decode(p, kv_pool, s->kv_dtype, ctas, stream));
+    return cuda_status(launch_sparse_decode(p, kv_pool, s->kv_dtype, ctas, stream, pdl));
 }
 
 } // namespace
@@ -201,7 +204,7 @@ msa_status msa_workspace_init(void *workspace, size_t workspace_bytes, cudaStrea
 {
     if (!workspace || !aligned16(workspace) || workspace_bytes < kAlign)
         return MSA_ERR_INVALID_ARGUMENT;
-    return cuda_status(cudaMemsetAsync(workspace, 0, kAlign, stream));
+    return cuda_status(cudaMemsetAsync(workspace, 0, workspace_bytes, stream));
 }
 
 msa_status msa_index_score(const msa_shape *shape, const void *q_idx, const void *idxk_pool,
@@ -242,7 +245,7 @@ msa_status msa_select_topk(const msa_shape *shape, const float *block_scores,
         return MSA_ERR_INVALID_ARGUMENT;
     if (tokens_of(shape) == 0)
         return MSA_OK;
-    return select_impl(shape, block_scores, seq_lens, selected, workspace, stream);
+    return select_impl(shape, block_scores, seq_lens, selected, workspace, stream, false);
 }
 
 msa_status msa_sparse_decode(const msa_shape *shape, const void *q, const void *kv_pool,
@@ -263,7 +266,7 @@ msa_status msa_sparse_decode(const msa_shape *shape, const void *q, const void *
     if (tokens_of(shape) == 0)
         return MSA_OK;
     return decode_impl(shape, q, kv_pool, block_table, seq_lens, selected, out, lse, workspace,
-                       stream);
+                       stream, false);
 }
 
 msa_status msa_decode_step(const msa_shape *shape, const void *q_idx, const void *idxk_pool,
@@ -297,10 +300,11 @@ msa_status msa_decode_step(const msa_shape *shape, const void *q_idx, const void
     if ((st = score_impl(shape, q_idx, idxk_pool, idxk_scales, block_table, seq_lens,
                          block_scores, workspace, stream)) != MSA_OK)
         return st;
-    if ((st = select_impl(shape, block_scores, seq_lens, selected, workspace, stream)) != MSA_OK)
+    // the select and the decode are programmatic dependents of the kernel before them
+    if ((st = select_impl(shape, block_scores, seq_lens, selected, workspace, stream, true)) != MSA_OK)
         return st;
     return decode_impl(shape, q, kv_pool, block_table, seq_lens, selected, out, lse, workspace,
-                       stream);
+                       stream, true);
 }
 
 msa_status msa_check_device_status(void *workspace, cudaStream_t stream)

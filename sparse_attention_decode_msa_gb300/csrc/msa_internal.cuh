@@ -7,6 +7,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -38,6 +39,7 @@ constexpr size_t kPartialFloats = size_t(kGroup) * kDim + 2 * kGroup;
 constexpr size_t kPartialBytes = kPartialFloats * sizeof(float);
 
 struct WorkspaceLayout {
+    size_t counters_off; // int32 [T * Hkv]: split-arrival counters of the decode (kept at 0)
     size_t scores_off;   // fp32 [T][maxB] (decode_step when block_scores == NULL)
     size_t selected_off; // int32 [T][k]   (decode_step when selected == NULL)
     size_t partial_off;  // decode partial slots
@@ -72,18 +74,41 @@ struct DecodeParams {
     uint16_t *out;           // bf16 bits [T][Hq][D]
     float *lse;              // [T][Hq]
     float *partial;          // slots of kPartialFloats
+    int *counters;           // [T * Hkv], zero between calls
     uint32_t *err;
     int R, nq, T, Hkv, maxB, k, num_pages;
     float scale_log2; // softmax_scale * log2(e) (* k_scale for FP8 keys)
     float v_scale;    // 1 for bf16 values
 };
 
-// Host launchers (return the first CUDA error of the launch sequence).
+// Host launchers (return the first CUDA error of the launch sequence).  With
+// `pdl` the kernel is launched as a programmatic dependent of the previous
+// kernel in the stream (it runs its prologue early and waits on the grid
+// dependency before reading that kernel's outputs); only kernels of the same
+// call are chained this way.
 cudaError_t launch_index_score(const ScoreParams &p, int index_dtype, int num_sms,
                                cudaStream_t stream);
-cudaError_t launch_select(const SelectParams &p, cudaStream_t stream);
+cudaError_t launch_select(const SelectParams &p, cudaStream_t stream, bool pdl);
 cudaError_t launch_sparse_decode(const DecodeParams &p, const void *kv_pool, int kv_dtype,
-                                 int ctas, cudaStream_t stream);
+                                 int ctas, cudaStream_t stream, bool pdl);
+
+// cudaLaunchKernelEx with an optional programmatic-stream-serialization attribute.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, bool pdl, Args &&...args)
+{
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = pdl ? attr : nullptr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---------------------------------------------------------------------------
 // device helpers
@@ -150,7 +175,32 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
     return true;
 }
 
+// ---- programmatic dependent launch ----------------------------------------
+
+// Block until the kernels this grid depends on have completed and their
+// writes are visible (a no-op without a programmatic dependency).
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next kernel in the stream to be scheduled now.
+__device__ __forceinline__ void launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- TMA ------------------------------------------------------------------
+
+// 1-D bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
                                             uint32_t bar)

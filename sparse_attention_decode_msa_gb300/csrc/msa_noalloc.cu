@@ -6,7 +6,7 @@
 // all device memory, code whose allocator may not be called on the path
 // that issues the decode, or a deployment that forbids run-time cudaMalloc
 // altogether.  For them this entry point keeps the decode's scratch (the
-// split partials and the device error word) in a fixed array compiled into
+// split partials, their arrival counters and the device error word) in a fixed array compiled into
 // the library.  The array lives in every GPU's memory from the moment the
 // library is loaded on it until the process exits.  Nothing here calls
 // cudaMalloc, cudaFree or any allocating routine.
@@ -20,7 +20,8 @@
 namespace msa {
 namespace {
 
-// Device scratch: [0, 256) error word, then the decode's partial slots.
+// Device scratch: [0, 256) error word, then one arrival counter per
+// (token, KV head) unit, then the decode's partial slots.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[MSA_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
@@ -93,16 +94,20 @@ extern "C" msa_status msa_sparse_decode_noalloc(const msa_shape *shape, const vo
         if (ctas > max_tasks)
             ctas = (int)max_tasks;
     }
-    // scratch needed: error word + one partial slot per (CTA + unit)
-    const long long slots = (long long)ctas + (long long)T * shape->num_kv_heads;
-    if (256 + slots * (long long)kPartialBytes > (long long)MSA_NOALLOC_SCRATCH_BYTES)
+    // scratch needed: error word, one arrival counter per unit (rounded up to
+    // 256 bytes), one partial slot per (CTA + unit)
+    const long long units = (long long)T * shape->num_kv_heads;
+    const long long head = 256 + (units * 4 + 255) / 256 * 256;
+    const long long slots = (long long)ctas + units;
+    if (head + slots * (long long)kPartialBytes > (long long)MSA_NOALLOC_SCRATCH_BYTES)
         return MSA_ERR_UNSUPPORTED; // too big for the fixed scratch: use msa_sparse_decode
 
     unsigned char *scratch = static_cast<unsigned char *>(scratch_address(dev));
     if (!scratch)
         return MSA_ERR_CUDA;
-    // the error word must start at zero; the partial slots are written before read
-    if (cudaMemsetAsync(scratch, 0, 256, stream) != cudaSuccess)
+    // the error word and the arrival counters must start at zero; the partial
+    // slots are written before they are read
+    if (cudaMemsetAsync(scratch, 0, (size_t)head, stream) != cudaSuccess)
         return MSA_ERR_CUDA;
 
     DecodeParams p;
@@ -112,7 +117,8 @@ extern "C" msa_status msa_sparse_decode_noalloc(const msa_shape *shape, const vo
     p.selected = selected;
     p.out = static_cast<uint16_t *>(out);
     p.lse = lse;
-    p.partial = reinterpret_cast<float *>(scratch + 256);
+    p.partial = reinterpret_cast<float *>(scratch + head);
+    p.counters = reinterpret_cast<int *>(scratch + 256);
     p.err = reinterpret_cast<uint32_t *>(scratch);
     p.R = shape->num_requests;
     p.nq = shape->q_per_req;
@@ -124,7 +130,7 @@ extern "C" msa_status msa_sparse_decode_noalloc(const msa_shape *shape, const vo
     const bool fp8 = shape->kv_dtype == MSA_FP8_E4M3;
     p.scale_log2 = shape->softmax_scale * 1.4426950408889634f * (fp8 ? shape->k_scale : 1.f);
     p.v_scale = fp8 ? shape->v_scale : 1.f;
-    return launch_sparse_decode(p, kv_pool, shape->kv_dtype, ctas, stream) == cudaSuccess
+    return launch_sparse_decode(p, kv_pool, shape->kv_dtype, ctas, stream, false) == cudaSuccess
                ? MSA_OK
                : MSA_ERR_CUDA;
 }

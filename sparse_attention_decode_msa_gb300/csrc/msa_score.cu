@@ -74,6 +74,7 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(const ScoreP
     extern __shared__ int item_prefix[]; // [R + 1]
     __shared__ float red[4][PPI][NT * 8];
 
+    launch_dependents(); // the select may start its prologue while pages are scored
     build_item_prefix<PPI>(p, item_prefix);
     const int total = item_prefix[p.R];
 

@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(const SelectPa
     __shared__ uint32_t s_prefix;
     __shared__ int s_need;
 
+    launch_dependents(); // the decode may start its prologue while tokens are selected
     const int t = blockIdx.x;
     const int r = t / p.nq, j = t - r * p.nq;
     int32_t *out = p.selected + (size_t)t * p.k;
@@ -84,6 +85,8 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(const SelectPa
         return;
     }
 
+    // block_scores come from the previous kernel of the step
+    grid_dependency_wait();
     const float *row = p.block_scores + (size_t)t * p.maxB;
     for (int b = threadIdx.x; b < n; b += kSelThreads)
         keys[b] = order_key(row[b]);
@@ -178,7 +181,7 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(const SelectPa
 
 } // namespace
 
-cudaError_t launch_select(const SelectParams &p, cudaStream_t stream)
+cudaError_t launch_select(const SelectParams &p, cudaStream_t stream, bool pdl)
 {
     const size_t smem = sizeof(uint32_t) * (size_t)p.maxB;
     if (smem > 48 * 1024) {
@@ -188,7 +191,9 @@ cudaError_t launch_select(const SelectParams &p, cudaStream_t stream)
             return e;
     }
     const int T = p.R * p.nq;
-    select_topk_kernel<<<T, kSelThreads, smem, stream>>>(p);
+    cudaError_t e = launch_kernel(select_topk_kernel, dim3(T), dim3(kSelThreads), smem, stream, pdl, p);
+    if (e != cudaSuccess)
+        return e;
     return cudaGetLastError();
 }
 
