@@ -18,21 +18,25 @@
 //   to its slot and bumps the unit's arrival counter; the CTA that arrives
 //   last combines the slots in slot order (so the result does not depend on
 //   which CTA is last), writes O and LSE, and resets the counter to zero.
-// * Data movement.  Each CTA first gathers its task table (block id and page
-//   of every task, through `selected` and the block table) into shared memory
-//   with all threads at once, so no page lookup sits on the copy path.  Per
-//   task the K and the V tile of KV head g (32 KiB each in bf16, 16 KiB in
-//   FP8) are fetched by TMA (cp.async.bulk.tensor, 128-byte swizzle) into a
-//   ring of shared-memory stages guarded by mbarriers; one thread keeps
-//   kAhead tasks in flight.  The 16 query rows of each unit (4 KiB) arrive by
-//   a 1-D bulk copy ahead of the unit.  Page offsets are 64-bit.
-// * Math.  Each of the 4 warps owns 32 of the page's 128 tokens and keeps its
-//   own online-softmax state for the 16 query heads; S = Q K^T and O += P V
-//   are mma.sync m16n8k16 tiles fed by ldmatrix from the swizzled stages
-//   (bf16), or by ldmatrix plus in-register E4M3 -> f16 converts (FP8: keys and
-//   values are exact in f16; k_scale is folded into the logit scale and
-//   v_scale into the output).  Logits are kept in base 2.  The 4 warps' states
-//   are combined in a fixed order.
+// * Data movement.  One producer warp gathers the CTA's task table (block id
+//   and page of every task, through `selected` and the block table) into
+//   shared memory ahead of use, and issues the copies: per task the K and the
+//   V tile of KV head g (32 KiB each in bf16, 16 KiB in FP8) by TMA
+//   (cp.async.bulk.tensor, 128-byte swizzle) into a ring of shared-memory
+//   stages, each guarded by a "full" mbarrier (bytes landed) and an "empty"
+//   mbarrier (all consumer warps done), and the 16 query rows of each unit
+//   (4 KiB) by a 1-D bulk copy.  Consumers hand a K stage back as soon as
+//   Q K^T has read it.  Page offsets are 64-bit.
+// * Math.  Each of the 8 consumer warps owns 16 of the page's 128 tokens and
+//   keeps its own online-softmax state for the 16 query heads; S = Q K^T and
+//   O += P V are mma.sync m16n8k16 tiles fed by ldmatrix from the swizzled
+//   stages (bf16), or by ldmatrix plus in-register E4M3 -> f16 converts (FP8:
+//   keys and values are exact in f16; k_scale is folded into the logit scale
+//   and v_scale into the output).  Logits are kept in base 2.  The warps'
+//   states are combined in a fixed order.
+// * Every wait is bounded; a timeout sets MSA_ERR_TIMEOUT, raises a CTA abort
+//   flag that ends every other wait, and the producer waits (bounded) for its
+//   copies in flight before the CTA exits.
 #include <cmath>
 
 #include "msa_internal.cuh"
@@ -40,20 +44,62 @@
 namespace msa {
 namespace {
 
-constexpr int kDecThreads = 128;
-constexpr int kQBufs = 4;     // query-row buffers (>= tasks in flight)
-constexpr int kWin = 256;     // task-table window (two windows resident)
+constexpr int kConsumerWarps = 8;              // each owns kTPW tokens of every page
+constexpr int kConsumers = 32 * kConsumerWarps;
+constexpr int kTPW = kPage / kConsumerWarps;   // tokens per consumer warp
+constexpr int kNT = kTPW / 8;                  // S n-tiles (8 tokens) per warp
+constexpr int kKK = kTPW / 16;                 // P.V k-steps (16 tokens) per warp
+constexpr int kVPR = 64 / kConsumerWarps;      // accumulator values per lane per combine round
+static_assert(kTPW % 16 == 0, "a warp's tokens must fill whole m16n8k16 k-steps");
+constexpr int kDecThreads = kConsumers + 32; // + one producer warp
+constexpr int kQBufs = 2;                    // query-row buffers
+constexpr int kWin = 128;                    // task-table window (two windows resident)
 constexpr int kQBytes = kGroup * kDim * 2;
+constexpr int kMaxSmem = 232448;             // dynamic shared memory limit per CTA
 
-template <bool FP8>
+template <bool FP8, int STAGES>
 struct Cfg {
     static constexpr int kTileBytes = FP8 ? 16384 : 32768;
-    static constexpr int kStages = FP8 ? 8 : 4; // two stages (K, V) per task
-    static constexpr int kAhead = kStages / 2;  // tasks in flight
-    static constexpr int kRingBytes = kTileBytes * kStages;
-    static_assert(kAhead <= kQBufs, "a unit's query buffer must outlive the tasks in flight");
-    static_assert(kAhead < kWin, "the task table must hold the tasks in flight");
+    static constexpr int kAhead = STAGES / 2;  // tasks the producer may run ahead
+    static constexpr int kRingBytes = kTileBytes * STAGES;
+    static_assert(STAGES % 2 == 0, "K and V of a task take two stages");
+    static_assert(kAhead < kWin, "the task table must cover the tasks in flight");
 };
+
+// Shared-memory layout of the decode CTA (offsets from a 1024-byte aligned
+// base); the host sizes the allocation with the same function.
+struct SmemLayout {
+    size_t ring, qbuf, bars, table, cbuf, comb, flags, qt, total;
+};
+
+__host__ __device__ constexpr size_t align_to(size_t v, size_t a)
+{
+    return (v + a - 1) / a * a;
+}
+
+__host__ __device__ inline SmemLayout decode_layout(int T, int stages, int tile_bytes)
+{
+    SmemLayout L{};
+    size_t off = 0;
+    L.ring = off;                                   // 1024-aligned: 128-byte swizzle atoms
+    off += (size_t)stages * tile_bytes;
+    L.qbuf = off = align_to(off, 128);             // bulk-copy destinations: 16-byte aligned
+    off += (size_t)kQBufs * kQBytes;
+    L.bars = off = align_to(off, 8);               // full[S], empty[S], qfull, qempty, consumer barrier
+    off += (size_t)(2 * stages + 2 * kQBufs + 1) * 8;
+    L.table = off = align_to(off, 16);             // int4 entries
+    off += (size_t)2 * kWin * 16;
+    L.cbuf = off = align_to(off, 16);              // [warps][kVPR][32] floats (8 KiB)
+    off += (size_t)kConsumerWarps * kVPR * 32 * 4;
+    L.comb = off = align_to(off, 16);              // comb_m[4][16], comb_l[4][16]
+    off += (size_t)2 * kConsumerWarps * kGroup * 4;
+    L.flags = off = align_to(off, 16);             // 4 ints
+    off += 16;
+    L.qt = off = align_to(off, 16);                // [T + 1] ints
+    off += (size_t)(T + 1) * 4;
+    L.total = align_to(off, 16) + 1024;            // + slack to align the base
+    return L;
+}
 
 struct Task {
     int t, g, i;
@@ -153,35 +199,46 @@ __device__ __forceinline__ int o_dim(int nt, int col)
     return FP8 ? (nt >> 1) * 16 + 2 * col + (nt & 1) : nt * 8 + col;
 }
 
-template <bool FP8>
+template <bool FP8, int STAGES>
 __global__ void __launch_bounds__(kDecThreads, 1)
     sparse_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p)
 {
-    using C = Cfg<FP8>;
+    using C = Cfg<FP8, STAGES>;
     extern __shared__ uint8_t smem_raw[];
-    // ring at a 1024-byte boundary (128-byte swizzle atoms)
-    uint8_t *ring = reinterpret_cast<uint8_t *>(
+    uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *qbuf = ring + C::kRingBytes;                                  // [kQBufs][16][128] bf16
-    uint64_t *bars = reinterpret_cast<uint64_t *>(qbuf + kQBufs * kQBytes); // [kStages]
-    uint64_t *qbars = bars + C::kStages;                                   // [kQBufs]
-    int4 *table = reinterpret_cast<int4 *>(qbars + kQBufs);               // [2][kWin]
-    float *comb_o = reinterpret_cast<float *>(table + 2 * kWin);          // [16][128]
-    float *comb_m = comb_o + kGroup * kDim;                               // [4][16]
-    float *comb_l = comb_m + 4 * kGroup;                                  // [4][16]
-    int *s_flag = reinterpret_cast<int *>(comb_l + 4 * kGroup);           // [4]
-    int *qt = s_flag + 4;                                                  // [T + 1]
+    const SmemLayout lay = decode_layout(p.T, STAGES, C::kTileBytes);
+    uint8_t *ring = base + lay.ring;                                    // [S] tiles
+    uint8_t *qbuf = base + lay.qbuf;                                    // [kQBufs][16][128] bf16
+    uint64_t *full = reinterpret_cast<uint64_t *>(base + lay.bars);    // [S] tile landed
+    uint64_t *empty = full + STAGES;                                    // [S] tile consumed
+    uint64_t *qfull = empty + STAGES;                                   // [kQBufs]
+    uint64_t *qempty = qfull + kQBufs;                                  // [kQBufs]
+    uint64_t *csync_bar = qempty + kQBufs;                              // consumer barrier
+    int4 *table = reinterpret_cast<int4 *>(base + lay.table);          // [2][kWin]
+    float *cbuf = reinterpret_cast<float *>(base + lay.cbuf);          // [warps][kVPR][32]
+    float *comb_m = reinterpret_cast<float *>(base + lay.comb);        // [warps][16]
+    float *comb_l = comb_m + kConsumerWarps * kGroup;                   // [warps][16]
+    int *s_flag = reinterpret_cast<int *>(base + lay.flags);           // [0] last, [1] abort
+    int *qt = reinterpret_cast<int *>(base + lay.qt);                  // [T + 1]
+    volatile int *abort_flag = s_flag + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g8 = lane >> 2, q4 = lane & 3;
 
     // ---- prologue: everything that does not read the previous kernel's output ----
     if (threadIdx.x == 0) {
         prefetch_tensormap(&kv_map);
-        for (int s = 0; s < C::kStages; ++s)
-            mbar_init(smem_u32(&bars[s]), 1);
-        for (int s = 0; s < kQBufs; ++s)
-            mbar_init(smem_u32(&qbars[s]), 1);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), kConsumerWarps);
+        }
+        for (int s = 0; s < kQBufs; ++s) {
+            mbar_init(smem_u32(&qfull[s]), 1);
+            mbar_init(smem_u32(&qempty[s]), kConsumerWarps);
+        }
+        mbar_init(smem_u32(csync_bar), kConsumers);
+        s_flag[0] = 0;
+        s_flag[1] = 0;
         fence_mbar_init();
     }
     build_token_prefix(p, qt);
@@ -197,68 +254,110 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     if (ntasks == 0)
         return;
 
-    auto fill_window = [&](int w) {
-        const int l0 = w * kWin;
-        int4 *dst = table + (w & 1) * kWin;
-        for (int i = threadIdx.x; i < kWin && l0 + i < ntasks; i += kDecThreads)
-            dst[i] = make_entry(p, x_begin + l0 + i, qt);
-    };
-    fill_window(0);
-    if (ntasks > kWin)
-        fill_window(1);
-    __syncthreads();
-
     auto entry = [&](int l) -> int4 { return table[((l / kWin) & 1) * kWin + (l % kWin)]; };
 
-    // ---- producer (thread 0): K and V tiles of task l into stages 2l, 2l+1 mod S,
-    // and the query rows of every new unit into qbuf[unit index mod kQBufs] ----
-    int issued_tiles = 0;   // thread 0 only
-    int prod_units = 0;     // thread 0 only
-    int prod_last = -1;     // thread 0 only: unit of the last issued task
-    auto issue = [&](int l) {
-        const int4 e = entry(l);
-        const int u = e.w * p.T + e.z;
-        if (u != prod_last) {
-            prod_last = u;
-            const int qb = prod_units % kQBufs;
-            ++prod_units;
-            const uint32_t qbar = smem_u32(&qbars[qb]);
-            mbar_arrive_expect_tx(qbar, kQBytes);
-            bulk_load(smem_u32(qbuf + qb * kQBytes),
-                      p.q + ((size_t)e.z * p.Hkv * kGroup + (size_t)e.w * kGroup) * kDim, kQBytes,
-                      qbar);
-        }
-        issued_tiles = 2 * l + 2;
-        for (int kv = 0; kv < 2; ++kv) {
-            const int z = 2 * l + kv;
-            const uint32_t bar = smem_u32(&bars[z % C::kStages]);
-            const uint32_t dst = smem_u32(ring + (size_t)(z % C::kStages) * C::kTileBytes);
-            if (e.x < 0) {
-                mbar_arrive(bar); // completes the phase with no data; consumers skip the task
-                continue;
+    if (warp == kConsumerWarps) {
+        // =================== producer warp ===================
+        auto fill_window = [&](int w) {
+            const int l0 = w * kWin;
+            int4 *dst = table + (w & 1) * kWin;
+            for (int i = lane; i < kWin && l0 + i < ntasks; i += 32)
+                dst[i] = make_entry(p, x_begin + l0 + i, qt);
+            __syncwarp();
+        };
+        fill_window(0);
+        if (ntasks > kWin)
+            fill_window(1);
+        int issued = 0;        // tiles issued (lane 0)
+        int q_issued = 0;      // query-row copies issued (lane 0)
+        int prod_units = 0, prod_last = -1;
+        bool ok = true;
+        for (int l = 0; l < ntasks && ok; ++l) {
+            // K stage of task l: wait until the consumers released its previous tile
+            const int zk = 2 * l;
+            if (lane == 0 && zk >= STAGES)
+                ok = mbar_wait_or_abort(smem_u32(&empty[zk % STAGES]), ((zk / STAGES) - 1) & 1,
+                                        abort_flag);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok)
+                break;
+            // the consumers have read every entry up to task l - S/2: the window
+            // before this one can be replaced by the one after it
+            if (l % kWin == C::kAhead && l >= kWin && (l / kWin + 1) * kWin < ntasks)
+                fill_window(l / kWin + 1);
+            if (lane == 0) {
+                const int4 e = entry(l);
+                const int u = e.w * p.T + e.z;
+                if (u != prod_last) {
+                    prod_last = u;
+                    const int qb = prod_units % kQBufs;
+                    if (prod_units >= kQBufs)
+                        ok = mbar_wait_or_abort(smem_u32(&qempty[qb]),
+                                                ((prod_units / kQBufs) - 1) & 1, abort_flag);
+                    if (ok) {
+                        const uint32_t qbar = smem_u32(&qfull[qb]);
+                        mbar_arrive_expect_tx(qbar, kQBytes);
+                        bulk_load(smem_u32(qbuf + qb * kQBytes),
+                                  p.q + ((size_t)e.z * p.Hkv * kGroup + (size_t)e.w * kGroup) * kDim,
+                                  kQBytes, qbar);
+                        q_issued = prod_units + 1;
+                    }
+                    ++prod_units;
+                }
+                for (int kv = 0; kv < 2 && ok; ++kv) {
+                    const int z = zk + kv;
+                    const int st = z % STAGES;
+                    if (kv == 1 && z >= STAGES)
+                        ok = mbar_wait_or_abort(smem_u32(&empty[st]), ((z / STAGES) - 1) & 1,
+                                                abort_flag);
+                    if (!ok)
+                        break;
+                    const uint32_t bar = smem_u32(&full[st]);
+                    issued = z + 1;
+                    if (e.x < 0) {
+                        mbar_arrive(bar); // completes the phase with no data; consumers skip the task
+                        continue;
+                    }
+                    const uint32_t dst = smem_u32(ring + (size_t)st * C::kTileBytes);
+                    const int row = e.x + kv * p.Hkv * kPage;
+                    mbar_arrive_expect_tx(bar, C::kTileBytes);
+                    tma_load_2d(dst, &kv_map, 0, row, bar);
+                    if (!FP8)
+                        tma_load_2d(dst + 16384, &kv_map, 64, row, bar);
+                }
             }
-            const int row = e.x + kv * p.Hkv * kPage;
-            mbar_arrive_expect_tx(bar, C::kTileBytes);
-            tma_load_2d(dst, &kv_map, 0, row, bar);
-            if (!FP8)
-                tma_load_2d(dst + 16384, &kv_map, 64, row, bar);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
         }
-    };
-    if (threadIdx.x == 0) {
-        const int pre = ntasks < C::kAhead ? ntasks : C::kAhead;
-        for (int l = 0; l < pre; ++l)
-            issue(l);
+        if (!ok && lane == 0) {
+            set_error(p.err, kErrTimeout);
+            *abort_flag = 1;
+            // Wait (bounded) for every copy this warp issued, so none lands in
+            // shared memory after the CTA has exited.
+            for (int z = issued - STAGES < 0 ? 0 : issued - STAGES; z < issued; ++z)
+                (void)mbar_wait_bounded(smem_u32(&full[z % STAGES]), (z / STAGES) & 1);
+            for (int u = q_issued - kQBufs < 0 ? 0 : q_issued - kQBufs; u < q_issued; ++u)
+                (void)mbar_wait_bounded(smem_u32(&qfull[u % kQBufs]), (u / kQBufs) & 1);
+        }
+        return;
     }
 
-    // ---- consumer state (every warp) ----
+    // =================== consumer warps 0..3 ===================
+    const int g8 = lane >> 2, q4 = lane & 3;
     float o[16][4];
     float m_run[2], l_run[2];
     uint32_t qa[8][4];
-    int cur_unit = -1, cons_units = 0;
-    int cur_t = 0, cur_g = 0;
-    bool abort = false;
-    int abort_task = 0;
-    const int tb = warp * 32; // this warp's tokens within a page
+    int cur_unit = -1, cons_units = 0, cur_t = 0, cur_g = 0;
+    int sync_phase = 0;
+    bool ok = true;
+    const int tb = warp * kTPW; // this warp's tokens within a page
+
+    // bounded barrier of the 128 consumer threads
+    auto csync = [&]() {
+        mbar_arrive(smem_u32(csync_bar));
+        if (!mbar_wait_or_abort(smem_u32(csync_bar), sync_phase & 1, abort_flag))
+            ok = false;
+        ++sync_phase;
+    };
 
     auto reset_state = [&]() {
 #pragma unroll
@@ -293,21 +392,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         }
     };
 
-    // O and LSE rows of unit (t, g) from a combined (o, M, L): o is unnormalised.
-    auto store_final = [&](int t, int g, int row, int d0, const float (&v)[8], float M, float L) {
-        const float inv = L > 0.f ? 1.f / L : 0.f; // one reciprocal per row
-        uint4 packed;
-        packed.x = pack_bf16(v[0] * inv, v[1] * inv);
-        packed.y = pack_bf16(v[2] * inv, v[3] * inv);
-        packed.z = pack_bf16(v[4] * inv, v[5] * inv);
-        packed.w = pack_bf16(v[6] * inv, v[7] * inv);
-        const size_t h = (size_t)t * p.Hkv * kGroup + (size_t)g * kGroup + row;
-        *reinterpret_cast<uint4 *>(p.out + h * kDim + d0) = packed;
-        if (d0 == 0)
-            p.lse[h] = (M == -INFINITY) ? -INFINITY : (M + log2f(L)) * 0.69314718055994531f;
-    };
-
-    // Combine the 4 warps' states of unit (t, g); write its output, or its
+    // Combine the warps' states of unit (t, g); write its output, or its
     // partial and, if this CTA is the last of the unit to arrive, the merge.
     auto finalize = [&](int t, int g) {
 #pragma unroll
@@ -321,34 +406,22 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             comb_l[warp * kGroup + g8] = l_run[0];
             comb_l[warp * kGroup + g8 + 8] = l_run[1];
         }
-        __syncthreads();
-        float fac[2];
+        csync();
+        // per row (g8, g8 + 8): combined max M, denominator L, this warp's factor
+        float M[2], L[2], fac[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int row = g8 + 8 * h;
-            float M = -INFINITY;
+            M[h] = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < 4; ++w)
-                M = fmaxf(M, comb_m[w * kGroup + row]);
-            fac[h] = (M == -INFINITY) ? 0.f : ex2(m_run[h] - M);
-        }
-        // fixed order (warp 0, 1, 2, 3): bitwise reproducible
-        for (int w = 0; w < 4; ++w) {
-            if (warp == w) {
+            for (int w = 0; w < kConsumerWarps; ++w)
+                M[h] = fmaxf(M[h], comb_m[w * kGroup + row]);
+            L[h] = 0.f;
 #pragma unroll
-                for (int n = 0; n < 16; ++n) {
-#pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        const int d = o_dim<FP8>(n, 2 * q4 + cc);
-                        float *a = &comb_o[g8 * kDim + d];
-                        float *b = &comb_o[(g8 + 8) * kDim + d];
-                        const float va = o[n][cc] * fac[0], vb = o[n][2 + cc] * fac[1];
-                        *a = w == 0 ? va : *a + va;
-                        *b = w == 0 ? vb : *b + vb;
-                    }
-                }
-            }
-            __syncthreads();
+            for (int w = 0; w < kConsumerWarps; ++w)
+                L[h] += (M[h] == -INFINITY) ? 0.f
+                                            : comb_l[w * kGroup + row] * ex2(comb_m[w * kGroup + row] - M[h]);
+            fac[h] = (M[h] == -INFINITY) ? 0.f : ex2(m_run[h] - M[h]);
         }
         const long long Pt = qt[p.T];
         const long long u_first = (long long)g * Pt + qt[t];
@@ -358,112 +431,167 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const int u = g * p.T + t;
         const bool whole = c_first == c_last;
         float *slot = p.partial + (size_t)(c + u) * kPartialFloats;
-        for (int e = threadIdx.x; e < kGroup * kDim / 8; e += kDecThreads) {
-            const int row = e >> 4, d0 = (e & 15) * 8;
-            float M = -INFINITY;
+        const size_t hbase = (size_t)t * p.Hkv * kGroup + (size_t)g * kGroup;
+        // Sum the warps' accumulators in kConsumerWarps rounds of kVPR values per
+        // lane through an 8 KiB buffer laid out [warp][value][lane] (conflict-free);
+        // warp rr sums round rr in warp order (fixed, so bitwise reproducible)
+        // and writes those dimensions.
 #pragma unroll
-            for (int w = 0; w < 4; ++w)
-                M = fmaxf(M, comb_m[w * kGroup + row]);
-            float L = 0.f;
+        for (int rr = 0; rr < kConsumerWarps; ++rr) {
 #pragma unroll
-            for (int w = 0; w < 4; ++w)
-                L += (M == -INFINITY) ? 0.f : comb_l[w * kGroup + row] * ex2(comb_m[w * kGroup + row] - M);
-            float v[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                v[i] = comb_o[row * kDim + d0 + i] * p.v_scale;
-            if (whole) {
-                store_final(t, g, row, d0, v, M, L);
-            } else {
-                float4 *dst = reinterpret_cast<float4 *>(slot + row * kDim + d0);
-                dst[0] = make_float4(v[0], v[1], v[2], v[3]);
-                dst[1] = make_float4(v[4], v[5], v[6], v[7]);
-                if (d0 == 0) {
-                    slot[kGroup * kDim + row] = M;
-                    slot[kGroup * kDim + kGroup + row] = L;
-                }
+            for (int i = 0; i < kVPR; ++i) {
+                const int n = rr * (kVPR / 4) + (i >> 2), e = i & 3;
+                cbuf[(warp * kVPR + i) * 32 + lane] = o[n][e] * fac[e >> 1];
             }
-        }
-        if (!whole) {
-            __threadfence(); // publish this CTA's slot before counting in
-            __syncthreads();
-            if (threadIdx.x == 0) {
-                int arrivals = 0;
-                for (int cc = c_first; cc <= c_last; ++cc)
-                    arrivals += !range_empty(cc, P, G);
-                const int before = atomicAdd(&p.counters[u], 1);
-                s_flag[0] = before == arrivals - 1;
-            }
-            __syncthreads();
-            if (s_flag[0]) {
-                __threadfence();
-                // merge every slot of the unit, in slot order
-                const float *base = p.partial + (size_t)(c_first + u) * kPartialFloats;
-                const int nslots = c_last - c_first + 1;
-                for (int e = threadIdx.x; e < kGroup * kDim / 8; e += kDecThreads) {
-                    const int row = e >> 4, d0 = (e & 15) * 8;
-                    float M = -INFINITY;
-                    for (int s = 0; s < nslots; ++s)
-                        if (!range_empty(c_first + s, P, G))
-                            M = fmaxf(M, __ldcg(base + (size_t)s * kPartialFloats + kGroup * kDim + row));
-                    float L = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                    for (int s = 0; s < nslots; ++s) {
-                        if (range_empty(c_first + s, P, G))
-                            continue;
-                        const float *sl = base + (size_t)s * kPartialFloats;
-                        const float ms = __ldcg(sl + kGroup * kDim + row);
-                        const float wgt = (M == -INFINITY) ? 0.f : ex2(ms - M);
-                        L += wgt * __ldcg(sl + kGroup * kDim + kGroup + row);
-                        const float4 a = __ldcg(reinterpret_cast<const float4 *>(sl + row * kDim + d0));
-                        const float4 b = __ldcg(reinterpret_cast<const float4 *>(sl + row * kDim + d0 + 4));
-                        acc[0] += wgt * a.x; acc[1] += wgt * a.y; acc[2] += wgt * a.z; acc[3] += wgt * a.w;
-                        acc[4] += wgt * b.x; acc[5] += wgt * b.y; acc[6] += wgt * b.z; acc[7] += wgt * b.w;
+            csync();
+            if (warp == rr) {
+#pragma unroll
+                for (int i = 0; i < kVPR; i += 2) {
+                    const int n = rr * (kVPR / 4) + (i >> 2), e = i & 3; // e in {0, 2}: cols 2q4, 2q4+1 of row e/2
+                    float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kConsumerWarps; ++w) {
+                        v0 += cbuf[(w * kVPR + i) * 32 + lane];
+                        v1 += cbuf[(w * kVPR + i + 1) * 32 + lane];
                     }
-                    store_final(t, g, row, d0, acc, M, L);
+                    const int h = e >> 1, row = g8 + 8 * h;
+                    v0 *= p.v_scale;
+                    v1 *= p.v_scale;
+                    const int d0 = o_dim<FP8>(n, 2 * q4), d1 = o_dim<FP8>(n, 2 * q4 + 1);
+                    if (whole) {
+                        const float inv = L[h] > 0.f ? 1.f / L[h] : 0.f;
+                        const uint32_t pk = pack_bf16(v0 * inv, v1 * inv);
+                        uint16_t *orow = p.out + (hbase + row) * kDim;
+                        if (!FP8) {
+                            *reinterpret_cast<uint32_t *>(orow + d0) = pk; // d1 == d0 + 1
+                        } else {
+                            orow[d0] = (uint16_t)(pk & 0xFFFFu);
+                            orow[d1] = (uint16_t)(pk >> 16);
+                        }
+                    } else {
+                        float *srow = slot + row * kDim;
+                        if (!FP8) {
+                            *reinterpret_cast<float2 *>(srow + d0) = make_float2(v0, v1);
+                        } else {
+                            srow[d0] = v0;
+                            srow[d1] = v1;
+                        }
+                    }
                 }
-                if (threadIdx.x == 0)
-                    p.counters[u] = 0; // ready for the next call
+            }
+            csync();
+        }
+        if (warp == 0 && q4 == 0) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int row = g8 + 8 * h;
+                if (whole) {
+                    p.lse[hbase + row] =
+                        (M[h] == -INFINITY) ? -INFINITY : (M[h] + log2f(L[h])) * 0.69314718055994531f;
+                } else {
+                    slot[kGroup * kDim + row] = M[h];
+                    slot[kGroup * kDim + kGroup + row] = L[h];
+                }
             }
         }
-        __syncthreads();
+        if (whole)
+            return;
+        __threadfence(); // publish this CTA's slot before counting in
+        csync();
+        if (threadIdx.x == 0) {
+            int arrivals = 0;
+            for (int cc = c_first; cc <= c_last; ++cc)
+                arrivals += !range_empty(cc, P, G);
+            const int before = atomicAdd(&p.counters[u], 1);
+            s_flag[0] = before == arrivals - 1;
+        }
+        csync();
+        if (s_flag[0]) {
+            __threadfence();
+            // merge every slot of the unit, in slot order; one reciprocal per row
+            const float *base = p.partial + (size_t)(c_first + u) * kPartialFloats;
+            const int nslots = c_last - c_first + 1;
+            for (int e = threadIdx.x; e < kGroup * kDim / 8; e += kConsumers) {
+                const int row = e >> 4, d0 = (e & 15) * 8;
+                float Mx = -INFINITY;
+                for (int s = 0; s < nslots; ++s)
+                    if (!range_empty(c_first + s, P, G))
+                        Mx = fmaxf(Mx, __ldcg(base + (size_t)s * kPartialFloats + kGroup * kDim + row));
+                float Lx = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                for (int s = 0; s < nslots; ++s) {
+                    if (range_empty(c_first + s, P, G))
+                        continue;
+                    const float *sl = base + (size_t)s * kPartialFloats;
+                    const float ms = __ldcg(sl + kGroup * kDim + row);
+                    const float wgt = (Mx == -INFINITY) ? 0.f : ex2(ms - Mx);
+                    Lx += wgt * __ldcg(sl + kGroup * kDim + kGroup + row);
+                    const float4 a = __ldcg(reinterpret_cast<const float4 *>(sl + row * kDim + d0));
+                    const float4 b = __ldcg(reinterpret_cast<const float4 *>(sl + row * kDim + d0 + 4));
+                    acc[0] += wgt * a.x; acc[1] += wgt * a.y; acc[2] += wgt * a.z; acc[3] += wgt * a.w;
+                    acc[4] += wgt * b.x; acc[5] += wgt * b.y; acc[6] += wgt * b.z; acc[7] += wgt * b.w;
+                }
+                const float inv = Lx > 0.f ? 1.f / Lx : 0.f;
+                uint4 packed;
+                packed.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+                packed.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+                packed.z = pack_bf16(acc[4] * inv, acc[5] * inv);
+                packed.w = pack_bf16(acc[6] * inv, acc[7] * inv);
+                *reinterpret_cast<uint4 *>(p.out + (hbase + row) * kDim + d0) = packed;
+                if (d0 == 0)
+                    p.lse[hbase + row] =
+                        (Mx == -INFINITY) ? -INFINITY : (Mx + log2f(Lx)) * 0.69314718055994531f;
+            }
+            if (threadIdx.x == 0)
+                p.counters[u] = 0; // ready for the next call
+        }
+        csync(); // s_flag and cbuf are reused by the next unit
     };
 
-    for (int l = 0; l < ntasks; ++l) {
-        const int4 e = entry(l);
+    for (int l = 0; l < ntasks && ok; ++l) {
+        const int zk = 2 * l, zv = 2 * l + 1;
+        const int sk = zk % STAGES, sv = zv % STAGES;
+        if (!mbar_wait_or_abort(smem_u32(&full[sk]), (zk / STAGES) & 1, abort_flag)) {
+            ok = false;
+            break;
+        }
+        const int4 e = entry(l); // written before the producer armed full[sk]
         const int u = e.w * p.T + e.z;
         if (u != cur_unit) {
-            if (cur_unit >= 0)
+            if (cur_unit >= 0) {
                 finalize(cur_t, cur_g);
+                if (!ok)
+                    break;
+            }
             cur_unit = u;
             cur_t = e.z;
             cur_g = e.w;
             reset_state();
             const int qb = cons_units % kQBufs;
-            if (!mbar_wait_bounded(smem_u32(&qbars[qb]), (cons_units / kQBufs) & 1))
-                abort = true;
-            ++cons_units;
+            if (!mbar_wait_or_abort(smem_u32(&qfull[qb]), (cons_units / kQBufs) & 1, abort_flag)) {
+                ok = false;
+                break;
+            }
             load_q(qb);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_u32(&qempty[qb]));
+            ++cons_units;
         }
         const int r = e.z / p.nq, j = e.z - r * p.nq;
-        const int L = p.seq_lens[r] + j;
-        const int zk = 2 * l, zv = 2 * l + 1;
-        const uint32_t tileK = smem_u32(ring + (size_t)(zk % C::kStages) * C::kTileBytes);
-        const uint32_t tileV = smem_u32(ring + (size_t)(zv % C::kStages) * C::kTileBytes);
+        const int Lvis = p.seq_lens[r] + j;
+        const uint32_t tileK = smem_u32(ring + (size_t)sk * C::kTileBytes);
+        const uint32_t tileV = smem_u32(ring + (size_t)sv * C::kTileBytes);
+        const bool live = e.x >= 0;
 
-        bool ok = mbar_wait_bounded(smem_u32(&bars[zk % C::kStages]), (zk / C::kStages) & 1);
-        ok = mbar_wait_bounded(smem_u32(&bars[zv % C::kStages]), (zv / C::kStages) & 1) && ok;
-        if (!ok)
-            abort = true;
-
-        if (e.x >= 0 && !abort) {
-            // ---- S = Q K^T over this warp's 32 tokens: 4 n-tiles of 8 tokens ----
-            float s[4][4];
+        // ---- S = Q K^T over this warp's kTPW tokens: kNT n-tiles of 8 tokens ----
+        float s[kNT][4];
 #pragma unroll
-            for (int n = 0; n < 4; ++n)
-                s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+        for (int n = 0; n < kNT; ++n)
+            s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+        if (live) {
             if (!FP8) {
 #pragma unroll
-                for (int n2 = 0; n2 < 2; ++n2) {
+                for (int n2 = 0; n2 < kNT / 2; ++n2) {
                     const int mi = lane >> 3;
                     const int tok = tb + 16 * n2 + ((mi >> 1) << 3) + (lane & 7);
 #pragma unroll
@@ -479,7 +607,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 }
             } else {
 #pragma unroll
-                for (int n2 = 0; n2 < 2; ++n2) {
+                for (int n2 = 0; n2 < kNT / 2; ++n2) {
                     const int mi = lane >> 3;
                     const int tok = tb + 16 * n2 + ((mi & 1) << 3) + (lane & 7);
 #pragma unroll
@@ -500,17 +628,24 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                     }
                 }
             }
+        }
+        // the K tile is no longer read: hand its stage back to the producer
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_u32(&empty[sk]));
 
+        uint32_t pa[kKK][4];
+        if (live) {
             // ---- scale, causal mask, online softmax (base 2) ----
             const int pos0 = e.y * kPage + tb; // position of this warp's token 0
-            const bool need_mask = pos0 + 32 > L;
+            const bool need_mask = pos0 + kTPW > Lvis;
             float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-            for (int n = 0; n < 4; ++n) {
+            for (int n = 0; n < kNT; ++n) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     float v = s[n][k] * p.scale_log2;
-                    if (need_mask && pos0 + 8 * n + 2 * q4 + (k & 1) >= L)
+                    if (need_mask && pos0 + 8 * n + 2 * q4 + (k & 1) >= Lvis)
                         v = -INFINITY;
                     s[n][k] = v;
                     mx[k >> 1] = fmaxf(mx[k >> 1], v);
@@ -534,9 +669,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 o[n][2] *= alpha[1];
                 o[n][3] *= alpha[1];
             }
-            uint32_t pa[2][4];
 #pragma unroll
-            for (int n = 0; n < 4; ++n) {
+            for (int n = 0; n < kNT; ++n) {
                 const float p0 = ex2(s[n][0] - ref[0]), p1 = ex2(s[n][1] - ref[0]);
                 const float p2 = ex2(s[n][2] - ref[1]), p3 = ex2(s[n][3] - ref[1]);
                 l_run[0] += p0 + p1;
@@ -546,11 +680,17 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 pa[kk][hi + 0] = FP8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
                 pa[kk][hi + 1] = FP8 ? pack_f16(p2, p3) : pack_bf16(p2, p3);
             }
+        }
 
-            // ---- O += P V over this warp's 32 tokens ----
+        if (!mbar_wait_or_abort(smem_u32(&full[sv]), (zv / STAGES) & 1, abort_flag)) {
+            ok = false;
+            break;
+        }
+        if (live) {
+            // ---- O += P V over this warp's kTPW tokens ----
             if (!FP8) {
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
+                for (int kk = 0; kk < kKK; ++kk) {
                     const int mi = lane >> 3;
                     const int tok = tb + 16 * kk + ((mi & 1) << 3) + (lane & 7);
 #pragma unroll
@@ -566,7 +706,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 }
             } else {
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
+                for (int kk = 0; kk < kKK; ++kk) {
                     const int mi = lane >> 3;
                     const int tok = tb + 16 * kk + ((mi & 1) << 3) + (lane & 7);
 #pragma unroll
@@ -589,35 +729,607 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 }
             }
         }
-
-        // every warp is done with both stages of task l
-        abort = __syncthreads_or(abort);
-        if (abort) {
-            abort_task = l;
-            break;
-        }
-        // refill the table window that task l closed
-        if ((l + 1) % kWin == 0 && l + 1 + kWin < ntasks) {
-            fill_window((l + 1) / kWin + 1);
-            __syncthreads();
-        }
-        if (threadIdx.x == 0 && l + C::kAhead < ntasks)
-            issue(l + C::kAhead);
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_u32(&empty[sv]));
     }
+    if (ok && cur_unit >= 0)
+        finalize(cur_t, cur_g);
+    if (!ok) {
+        set_error(p.err, kErrTimeout);
+        *abort_flag = 1;
+    }
+}
 
-    if (abort) {
-        if (threadIdx.x == 0) {
+// ===========================================================================
+// bf16 KV: tcgen05 UMMA with TMEM accumulators
+// ===========================================================================
+//
+// Per page (task) of unit (t, g):
+//   S^T[128 tok][16 heads] = K[128 tok][128 dim] . Q^T          (M=128, N=16, K=128)
+//   O^T[128 dim][16 heads] = V^T[128 dim][128 tok] . P^T        (M=128, N=16, K=128)
+// both issued by one thread as tcgen05.mma.kind::f16 (8 instructions of K=16
+// each), fp32 accumulators in TMEM (double-buffered: S at columns 0/16, O at
+// 32/48).  Operands: K tile and the unit's Q rows are K-major with the TMA's
+// 128-byte swizzle; the V tile, as loaded, is the MN-major form of V^T; P^T is
+// written by the softmax warps in the K-major 128-byte-swizzled form.
+// Warps: 0 = TMA producer + task table, 1 = MMA issuer + TMEM owner,
+// 2..5 = softmax (thread = one TMEM lane: a token for S^T, a dimension for
+// O^T).  The softmax warps exchange per-head page maxima through shared memory,
+// keep the running max / denominator per head, and fold each page's O^T into
+// 16 registers (one per head) once the next page's P^T is written.
+
+constexpr int kUWarps = 6;                 // producer, MMA, 4 softmax
+constexpr int kUThreads = 32 * kUWarps;
+constexpr int kUSoftmax = 128;             // softmax threads
+constexpr int kUTmemCols = 64;             // S[2] + O[2], 16 columns each
+constexpr int kUTile = 32768;              // bf16 K or V tile of one (page, KV head)
+constexpr int kUQTile = 4096;              // 16 query rows of one unit, two 64-dim boxes
+constexpr int kUPTile = 4096;              // P^T of one page: [16 heads][128 tokens] bf16
+
+struct USmem {
+    size_t ring, qbuf, pbuf, bars, table, xbuf, lbuf, misc, qt, total;
+};
+
+__host__ __device__ inline USmem umma_layout(int T, int stages)
+{
+    USmem L{};
+    size_t off = 0;
+    L.ring = off;                          // 1024-aligned tiles
+    off += (size_t)stages * kUTile;
+    L.qbuf = off = align_to(off, 1024);    // [2] query tiles (swizzle atoms: 1024-aligned)
+    off += 2 * kUQTile;
+    L.pbuf = off = align_to(off, 1024);    // [2] P^T tiles
+    off += 2 * kUPTile;
+    // full[S], empty[S], qfull[2], qempty[2], s_full[2], s_free[2], p_full[2],
+    // p_free[2], o_full[2], o_free[2], softmax sync, done
+    L.bars = off = align_to(off, 8);
+    off += (size_t)(2 * stages + 16 + 2) * 8;
+    L.table = off = align_to(off, 16);     // [2][kWin] int4
+    off += (size_t)2 * kWin * 16;
+    L.xbuf = off = align_to(off, 16);      // [2][4 quarters][16] page maxima
+    off += 2 * 4 * 16 * 4;
+    L.lbuf = off = align_to(off, 16);      // [4 quarters][16] denominators
+    off += 4 * 16 * 4;
+    L.misc = off = align_to(off, 16);      // tmem base, flags
+    off += 16;
+    L.qt = off = align_to(off, 16);        // [T + 1]
+    off += (size_t)(T + 1) * 4;
+    L.total = align_to(off, 16) + 1024;
+    return L;
+}
+
+template <int STAGES>
+__global__ void __launch_bounds__(kUThreads, 1)
+    sparse_decode_umma_kernel(const __grid_constant__ CUtensorMap kv_map,
+                              const __grid_constant__ CUtensorMap q_map, const DecodeParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const USmem lay = umma_layout(p.T, STAGES);
+    uint8_t *ring = base + lay.ring;
+    uint8_t *qbuf = base + lay.qbuf;
+    uint8_t *pbuf = base + lay.pbuf;
+    uint64_t *full = reinterpret_cast<uint64_t *>(base + lay.bars);
+    uint64_t *empty = full + STAGES;
+    uint64_t *qfull = empty + STAGES;
+    uint64_t *qempty = qfull + 2;
+    uint64_t *s_full = qempty + 2;
+    uint64_t *s_free = s_full + 2;
+    uint64_t *p_full = s_free + 2;
+    uint64_t *p_free = p_full + 2;
+    uint64_t *o_full = p_free + 2;
+    uint64_t *o_free = o_full + 2;
+    uint64_t *smx_bar = o_free + 2;    // softmax-warps barrier (128 arrivals)
+    uint64_t *done_bar = smx_bar + 1;  // softmax warps finished with TMEM (4 arrivals)
+    int4 *table = reinterpret_cast<int4 *>(base + lay.table);
+    float *xbuf = reinterpret_cast<float *>(base + lay.xbuf);
+    float *lbuf = reinterpret_cast<float *>(base + lay.lbuf);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + lay.misc);
+    int *s_flag = reinterpret_cast<int *>(base + lay.misc) + 1; // [0] last arrival, [1] abort
+    int *qt = reinterpret_cast<int *>(base + lay.qt);
+    volatile int *abort_flag = s_flag + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&kv_map);
+        prefetch_tensormap(&q_map);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&qfull[b]), 1);
+            mbar_init(smem_u32(&qempty[b]), 1);
+            mbar_init(smem_u32(&s_full[b]), 1);
+            mbar_init(smem_u32(&s_free[b]), 4);
+            mbar_init(smem_u32(&p_full[b]), 4);
+            mbar_init(smem_u32(&p_free[b]), 1);
+            mbar_init(smem_u32(&o_full[b]), 1);
+            mbar_init(smem_u32(&o_free[b]), 4);
+        }
+        mbar_init(smem_u32(smx_bar), kUSoftmax);
+        mbar_init(smem_u32(done_bar), 4);
+        s_flag[0] = 0;
+        s_flag[1] = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1)
+        tmem_alloc(smem_u32(tmem_slot), kUTmemCols);
+    build_token_prefix(p, qt);
+    tcgen05_before_sync();
+    __syncthreads();
+    tcgen05_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    const long long P = (long long)p.Hkv * qt[p.T];
+    const int G = gridDim.x, c = blockIdx.x;
+    const long long x_begin = (long long)c * P / G, x_end = (long long)(c + 1) * P / G;
+    const int ntasks = (int)(x_end - x_begin);
+
+    grid_dependency_wait(); // `selected` comes from the previous kernel of the step
+
+    auto entry = [&](int l) -> int4 { return table[((l / kWin) & 1) * kWin + (l % kWin)]; };
+    auto unit_of = [&](const int4 &e) { return e.w * p.T + e.z; };
+    auto fill_window = [&](int w) { // producer warp
+        const int l0 = w * kWin;
+        int4 *dst = table + (w & 1) * kWin;
+        for (int i = lane; i < kWin && l0 + i < ntasks; i += 32)
+            dst[i] = make_entry(p, x_begin + l0 + i, qt);
+        __syncwarp();
+    };
+    // the first two table windows, visible to every warp before anything starts
+    if (warp == 0) {
+        if (ntasks > 0)
+            fill_window(0);
+        if (ntasks > kWin)
+            fill_window(1);
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        // =================== producer ===================
+        constexpr int kAhead = STAGES / 2;
+        int issued = 0, q_issued = 0, prod_units = 0, prod_last = -1;
+        bool ok = true;
+        for (int l = 0; l < ntasks && ok; ++l) {
+            const int zk = 2 * l;
+            if (lane == 0 && zk >= STAGES)
+                ok = mbar_wait_or_abort(smem_u32(&empty[zk % STAGES]), ((zk / STAGES) - 1) & 1,
+                                        abort_flag);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok)
+                break;
+            // The softmax warps trail the MMA warp by up to two tasks and the MMA
+            // warp trails this one by up to kAhead: only kAhead + 2 tasks into
+            // a window has every reader left the window before it.
+            if (l % kWin == kAhead + 2 && l >= kWin && (l / kWin + 1) * kWin < ntasks)
+                fill_window(l / kWin + 1);
+            if (lane == 0) {
+                const int4 e = entry(l);
+                const int u = unit_of(e);
+                if (u != prod_last) {
+                    prod_last = u;
+                    const int qb = prod_units & 1;
+                    if (prod_units >= 2)
+                        ok = mbar_wait_or_abort(smem_u32(&qempty[qb]), ((prod_units >> 1) - 1) & 1,
+                                                abort_flag);
+                    if (ok) {
+                        const uint32_t qbar = smem_u32(&qfull[qb]);
+                        const uint32_t dst = smem_u32(qbuf + qb * kUQTile);
+                        const int row = (e.z * p.Hkv + e.w) * kGroup;
+                        mbar_arrive_expect_tx(qbar, kUQTile);
+                        tma_load_2d(dst, &q_map, 0, row, qbar);
+                        tma_load_2d(dst + kUQTile / 2, &q_map, 64, row, qbar);
+                        q_issued = prod_units + 1;
+                    }
+                    ++prod_units;
+                }
+                for (int kv = 0; kv < 2 && ok; ++kv) {
+                    const int z = zk + kv;
+                    const int st = z % STAGES;
+                    if (kv == 1 && z >= STAGES)
+                        ok = mbar_wait_or_abort(smem_u32(&empty[st]), ((z / STAGES) - 1) & 1,
+                                                abort_flag);
+                    if (!ok)
+                        break;
+                    const uint32_t bar = smem_u32(&full[st]);
+                    issued = z + 1;
+                    if (e.x < 0) {
+                        mbar_arrive(bar); // no data: consumers skip the task
+                        continue;
+                    }
+                    const uint32_t dst = smem_u32(ring + (size_t)st * kUTile);
+                    const int row = e.x + kv * p.Hkv * kPage;
+                    mbar_arrive_expect_tx(bar, kUTile);
+                    tma_load_2d(dst, &kv_map, 0, row, bar);
+                    tma_load_2d(dst + kUTile / 2, &kv_map, 64, row, bar);
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+        }
+        if (!ok && lane == 0) {
             set_error(p.err, kErrTimeout);
-            // Wait (bounded) for every copy issued and not yet consumed, so none
-            // lands in shared memory after the CTA has exited.
-            for (int z = 2 * abort_task; z < issued_tiles; ++z)
-                (void)mbar_wait_bounded(smem_u32(&bars[z % C::kStages]), (z / C::kStages) & 1);
-            for (int u = cons_units; u < prod_units; ++u)
-                (void)mbar_wait_bounded(smem_u32(&qbars[u % kQBufs]), (u / kQBufs) & 1);
+            *abort_flag = 1;
+            for (int z = issued - STAGES < 0 ? 0 : issued - STAGES; z < issued; ++z)
+                (void)mbar_wait_bounded(smem_u32(&full[z % STAGES]), (z / STAGES) & 1);
+            for (int u = q_issued - 2 < 0 ? 0 : q_issued - 2; u < q_issued; ++u)
+                (void)mbar_wait_bounded(smem_u32(&qfull[u & 1]), (u >> 1) & 1);
         }
         return;
     }
-    finalize(cur_t, cur_g);
+
+    if (warp == 1) {
+        // =================== MMA issuer (lane 0) ===================
+        constexpr uint32_t kIdescS = umma_idesc_bf16(128, 16, 0, 0); // K and Q^T both K-major
+        constexpr uint32_t kIdescO = umma_idesc_bf16(128, 16, 1, 0); // V^T MN-major, P^T K-major
+        bool ok = true;
+        if (lane == 0) {
+            int cons_units = 0, cur_unit = -1;
+            for (int l = 0; l < ntasks && ok; ++l) {
+                const int zk = 2 * l, zv = zk + 1, b = l & 1;
+                ok = mbar_wait_or_abort(smem_u32(&full[zk % STAGES]), (zk / STAGES) & 1, abort_flag);
+                if (!ok)
+                    break;
+                const int4 e = entry(l);
+                const int u = unit_of(e);
+                const int qb = (u != cur_unit ? cons_units : cons_units - 1) & 1;
+                if (u != cur_unit) {
+                    ok = mbar_wait_or_abort(smem_u32(&qfull[qb]), (cons_units >> 1) & 1, abort_flag);
+                    cur_unit = u;
+                    ++cons_units;
+                }
+                if (ok && l >= 2)
+                    ok = mbar_wait_or_abort(smem_u32(&s_free[b]), ((l >> 1) - 1) & 1, abort_flag);
+                if (!ok)
+                    break;
+                tcgen05_after_sync();
+                const bool live = e.x >= 0;
+                const uint32_t tileK = smem_u32(ring + (size_t)(zk % STAGES) * kUTile);
+                const uint32_t tileV = smem_u32(ring + (size_t)(zv % STAGES) * kUTile);
+                const uint32_t qtile = smem_u32(qbuf + qb * kUQTile);
+                const uint32_t ptile = smem_u32(pbuf + b * kUPTile);
+                if (live) {
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint64_t a = umma_desc_sw128(tileK + (ks >> 2) * (kUTile / 2) + (ks & 3) * 32, 16, 1024);
+                        const uint64_t bq = umma_desc_sw128(qtile + (ks >> 2) * (kUQTile / 2) + (ks & 3) * 32, 16, 1024);
+                        umma_bf16(tmem + 16 * b, a, bq, kIdescS, ks > 0);
+                    }
+                }
+                umma_commit(smem_u32(&s_full[b]));
+                umma_commit(smem_u32(&empty[zk % STAGES])); // K tile read
+                // last task of its unit: the query tile can be replaced
+                const bool unit_ends = (l + 1 == ntasks) || unit_of(entry(l + 1)) != u;
+                if (unit_ends)
+                    umma_commit(smem_u32(&qempty[qb]));
+                ok = mbar_wait_or_abort(smem_u32(&full[zv % STAGES]), (zv / STAGES) & 1, abort_flag);
+                if (ok)
+                    ok = mbar_wait_or_abort(smem_u32(&p_full[b]), (l >> 1) & 1, abort_flag);
+                if (ok && l >= 2)
+                    ok = mbar_wait_or_abort(smem_u32(&o_free[b]), ((l >> 1) - 1) & 1, abort_flag);
+                if (!ok)
+                    break;
+                tcgen05_after_sync();
+                if (live) {
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        // V^T, MN-major: 16 tokens per k-step = 16 rows of 128 bytes;
+                        // the two 64-dim halves of a row are 16 KiB apart (LBO)
+                        const uint64_t a = umma_desc_sw128(tileV + ks * 2048, kUTile / 2, 1024);
+                        const uint64_t bp = umma_desc_sw128(ptile + (ks >> 2) * (kUPTile / 2) + (ks & 3) * 32, 16, 1024);
+                        umma_bf16(tmem + 32 + 16 * b, a, bp, kIdescO, ks > 0);
+                    }
+                }
+                umma_commit(smem_u32(&o_full[b]));
+                umma_commit(smem_u32(&p_free[b]));
+                umma_commit(smem_u32(&empty[zv % STAGES])); // V tile read
+            }
+            if (!ok) {
+                set_error(p.err, kErrTimeout);
+                *abort_flag = 1;
+            }
+        }
+        __syncwarp();
+        // free TMEM once the softmax warps are done with it (they always arrive,
+        // also after an abort; the wait is bounded)
+        if (lane == 0)
+            (void)mbar_wait_bounded(smem_u32(done_bar), 0);
+        __syncwarp();
+        tcgen05_after_sync();
+        tmem_dealloc(tmem, kUTmemCols);
+        return;
+    }
+
+    // =================== softmax warps 2..5 ===================
+    const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
+    const int idx = 32 * quarter + lane;   // token of S^T / dimension of O^T
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16);
+    int sync_phase = 0;
+    bool ok = true;
+    auto ssync = [&]() {
+        mbar_arrive(smem_u32(smx_bar));
+        if (!mbar_wait_or_abort(smem_u32(smx_bar), sync_phase & 1, abort_flag))
+            ok = false;
+        ++sync_phase;
+    };
+
+    float o[16], lsum[16], m_run[16], alpha_prev[16];
+    bool pending = false; // a page's O^T waits to be folded in
+    int pending_b = 0;
+    int cur_unit = -1, cur_t = 0, cur_g = 0;
+
+    auto reset = [&]() {
+#pragma unroll
+        for (int h = 0; h < 16; ++h) {
+            o[h] = 0.f;
+            lsum[h] = 0.f;
+            m_run[h] = -INFINITY;
+            alpha_prev[h] = 1.f;
+        }
+    };
+
+    // fold the pending page's O^T (thread = dimension) into o[]
+    auto fold = [&](int l_prev) {
+        const int b = l_prev & 1;
+        if (!mbar_wait_or_abort(smem_u32(&o_full[b]), (l_prev >> 1) & 1, abort_flag)) {
+            ok = false;
+            return;
+        }
+        tcgen05_after_sync();
+        if (pending) {
+            float v[16];
+            tmem_ld16(lane_base + 32 + 16 * b, v);
+#pragma unroll
+            for (int h = 0; h < 16; ++h)
+                o[h] = o[h] * alpha_prev[h] + v[h];
+        }
+        tcgen05_before_sync();
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_u32(&o_free[b]));
+        pending = false;
+    };
+
+    auto finalize = [&](int t, int g) {
+        // denominators: reduce lsum over the 128 token lanes
+        float lr[16];
+#pragma unroll
+        for (int h = 0; h < 16; ++h) {
+            float v = lsum[h];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                v += __shfl_xor_sync(0xffffffffu, v, off);
+            lr[h] = v;
+        }
+        if (lane == 0) {
+#pragma unroll
+            for (int h = 0; h < 16; ++h)
+                lbuf[quarter * 16 + h] = lr[h];
+        }
+        ssync();
+        float L[16];
+#pragma unroll
+        for (int h = 0; h < 16; ++h)
+            L[h] = lbuf[h] + lbuf[16 + h] + lbuf[32 + h] + lbuf[48 + h];
+        ssync(); // lbuf is reused by the next unit
+        const long long Pt = qt[p.T];
+        const long long u_first = (long long)g * Pt + qt[t];
+        const int n_u = qt[t + 1] - qt[t];
+        const int c_first = owner_of(u_first, P, G);
+        const int c_last = owner_of(u_first + n_u - 1, P, G);
+        const int u = g * p.T + t;
+        const bool whole = c_first == c_last;
+        const size_t hbase = (size_t)t * p.Hkv * kGroup + (size_t)g * kGroup;
+        float *slot = p.partial + (size_t)(c + u) * kPartialFloats;
+        if (whole) {
+#pragma unroll
+            for (int h = 0; h < 16; ++h) {
+                const float inv = L[h] > 0.f ? 1.f / L[h] : 0.f;
+                p.out[(hbase + h) * kDim + idx] = (uint16_t)(pack_bf16(o[h] * inv, 0.f) & 0xFFFFu);
+            }
+            if (idx < 16) {
+                float Mh = -INFINITY, Lh = 0.f;
+#pragma unroll
+                for (int h = 0; h < 16; ++h)
+                    if (h == idx) {
+                        Mh = m_run[h];
+                        Lh = L[h];
+                    }
+                p.lse[hbase + idx] = (Mh == -INFINITY) ? -INFINITY : (Mh + log2f(Lh)) * 0.69314718055994531f;
+            }
+            return;
+        }
+#pragma unroll
+        for (int h = 0; h < 16; ++h)
+            slot[h * kDim + idx] = o[h];
+        if (idx < 16) {
+            float Mh = -INFINITY, Lh = 0.f;
+#pragma unroll
+            for (int h = 0; h < 16; ++h)
+                if (h == idx) {
+                    Mh = m_run[h];
+                    Lh = L[h];
+                }
+            slot[kGroup * kDim + idx] = Mh;
+            slot[kGroup * kDim + kGroup + idx] = Lh;
+        }
+        __threadfence(); // publish this CTA's slot before counting in
+        ssync();
+        if (threadIdx.x == 64) {
+            int arrivals = 0;
+            for (int cc = c_first; cc <= c_last; ++cc)
+                arrivals += !range_empty(cc, P, G);
+            const int before = atomicAdd(&p.counters[u], 1);
+            s_flag[0] = before == arrivals - 1;
+        }
+        ssync();
+        if (s_flag[0]) {
+            __threadfence();
+            const float *sbase = p.partial + (size_t)(c_first + u) * kPartialFloats;
+            const int nslots = c_last - c_first + 1;
+            const int sidx = threadIdx.x - 64; // 0..127
+            for (int e = sidx; e < kGroup * kDim / 8; e += kUSoftmax) {
+                const int row = e >> 4, d0 = (e & 15) * 8;
+                float Mx = -INFINITY;
+                for (int s = 0; s < nslots; ++s)
+                    if (!range_empty(c_first + s, P, G))
+                        Mx = fmaxf(Mx, __ldcg(sbase + (size_t)s * kPartialFloats + kGroup * kDim + row));
+                float Lx = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                for (int s = 0; s < nslots; ++s) {
+                    if (range_empty(c_first + s, P, G))
+                        continue;
+                    const float *sl = sbase + (size_t)s * kPartialFloats;
+                    const float ms = __ldcg(sl + kGroup * kDim + row);
+                    const float wgt = (Mx == -INFINITY) ? 0.f : ex2(ms - Mx);
+                    Lx += wgt * __ldcg(sl + kGroup * kDim + kGroup + row);
+                    const float4 a = __ldcg(reinterpret_cast<const float4 *>(sl + row * kDim + d0));
+                    const float4 bb = __ldcg(reinterpret_cast<const float4 *>(sl + row * kDim + d0 + 4));
+                    acc[0] += wgt * a.x; acc[1] += wgt * a.y; acc[2] += wgt * a.z; acc[3] += wgt * a.w;
+                    acc[4] += wgt * bb.x; acc[5] += wgt * bb.y; acc[6] += wgt * bb.z; acc[7] += wgt * bb.w;
+                }
+                const float inv = Lx > 0.f ? 1.f / Lx : 0.f;
+                uint4 packed;
+                packed.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+                packed.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+                packed.z = pack_bf16(acc[4] * inv, acc[5] * inv);
+                packed.w = pack_bf16(acc[6] * inv, acc[7] * inv);
+                *reinterpret_cast<uint4 *>(p.out + (hbase + row) * kDim + d0) = packed;
+                if (d0 == 0)
+                    p.lse[hbase + row] = (Mx == -INFINITY) ? -INFINITY : (Mx + log2f(Lx)) * 0.69314718055994531f;
+            }
+            if (threadIdx.x == 64)
+                p.counters[u] = 0; // ready for the next call
+        }
+        ssync(); // s_flag is reused by the next unit
+    };
+
+    int l_last = -1;
+    for (int l = 0; l < ntasks && ok; ++l) {
+        const int b = l & 1;
+        if (!mbar_wait_or_abort(smem_u32(&s_full[b]), (l >> 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+        }
+        tcgen05_after_sync();
+        const int4 e = entry(l);
+        const int u = unit_of(e);
+        const bool live = e.x >= 0;
+        float sv[16];
+        if (live)
+            tmem_ld16(lane_base + 16 * b, sv);
+        tcgen05_before_sync();
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_u32(&s_free[b]));
+
+        if (u != cur_unit) {
+            if (cur_unit >= 0) {
+                if (l_last >= 0)
+                    fold(l_last);
+                if (!ok)
+                    break;
+                finalize(cur_t, cur_g);
+                if (!ok)
+                    break;
+            }
+            cur_unit = u;
+            cur_t = e.z;
+            cur_g = e.w;
+            reset();
+            l_last = -1;
+        }
+
+        // page maxima per head (log2 domain), across the 128 tokens
+        const int r = e.z / p.nq, j = e.z - r * p.nq;
+        const int Lvis = p.seq_lens[r] + j;
+        const bool visible = live && e.y * kPage + idx < Lvis;
+        float wmax[16];
+#pragma unroll
+        for (int h = 0; h < 16; ++h) {
+            sv[h] = visible ? sv[h] * p.scale_log2 : -INFINITY;
+            wmax[h] = warp_max_f32(sv[h]);
+        }
+        if (lane == 0) {
+            float4 *xw = reinterpret_cast<float4 *>(xbuf + (b * 4 + quarter) * 16);
+            xw[0] = make_float4(wmax[0], wmax[1], wmax[2], wmax[3]);
+            xw[1] = make_float4(wmax[4], wmax[5], wmax[6], wmax[7]);
+            xw[2] = make_float4(wmax[8], wmax[9], wmax[10], wmax[11]);
+            xw[3] = make_float4(wmax[12], wmax[13], wmax[14], wmax[15]);
+        }
+        ssync();
+        float alpha[16], pv[16];
+#pragma unroll
+        for (int h4 = 0; h4 < 4; ++h4) {
+            const float4 a0 = reinterpret_cast<const float4 *>(xbuf + (b * 4 + 0) * 16)[h4];
+            const float4 a1 = reinterpret_cast<const float4 *>(xbuf + (b * 4 + 1) * 16)[h4];
+            const float4 a2 = reinterpret_cast<const float4 *>(xbuf + (b * 4 + 2) * 16)[h4];
+            const float4 a3 = reinterpret_cast<const float4 *>(xbuf + (b * 4 + 3) * 16)[h4];
+            const float pm[4] = {fmaxf(fmaxf(a0.x, a1.x), fmaxf(a2.x, a3.x)),
+                                 fmaxf(fmaxf(a0.y, a1.y), fmaxf(a2.y, a3.y)),
+                                 fmaxf(fmaxf(a0.z, a1.z), fmaxf(a2.z, a3.z)),
+                                 fmaxf(fmaxf(a0.w, a1.w), fmaxf(a2.w, a3.w))};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int h = 4 * h4 + k;
+                const float m_new = fmaxf(m_run[h], pm[k]);
+                const float ref = (m_new == -INFINITY) ? 0.f : m_new;
+                alpha[h] = ex2(m_run[h] - ref); // 0 when m_run is -inf
+                m_run[h] = m_new;
+                pv[h] = ex2(sv[h] - ref);
+                lsum[h] = lsum[h] * alpha[h] + pv[h];
+            }
+        }
+        // P^T[h][token idx] into the K-major, 128-byte-swizzled B tile
+        if (l >= 2 && !mbar_wait_or_abort(smem_u32(&p_free[b]), ((l >> 1) - 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+        }
+        if (live) {
+            uint8_t *pt = pbuf + b * kUPTile + (idx >> 6) * (kUPTile / 2);
+            const int col = idx & 63;
+#pragma unroll
+            for (int h = 0; h < 16; ++h) {
+                const uint32_t off = h * 128 + ((((col >> 3) ^ (h & 7))) << 4) + (col & 7) * 2;
+                *reinterpret_cast<uint16_t *>(pt + off) = (uint16_t)(pack_bf16(pv[h], 0.f) & 0xFFFFu);
+            }
+            fence_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_u32(&p_full[b]));
+
+        // fold the previous page of this unit, then this page becomes pending
+        if (l_last >= 0) {
+            fold(l_last);
+            if (!ok)
+                break;
+        }
+#pragma unroll
+        for (int h = 0; h < 16; ++h)
+            alpha_prev[h] = live ? alpha[h] : 1.f;
+        pending = live;
+        pending_b = b;
+        l_last = l;
+        // a skipped page (no data) contributes p = 0 and alpha = 1
+    }
+    (void)pending_b;
+    if (ok && cur_unit >= 0) {
+        if (l_last >= 0)
+            fold(l_last);
+        if (ok)
+            finalize(cur_t, cur_g);
+    }
+    if (!ok) {
+        set_error(p.err, kErrTimeout);
+        *abort_flag = 1;
+    }
+    tcgen05_before_sync();
+    __syncwarp();
+    if (lane == 0)
+        mbar_arrive(smem_u32(done_bar));
 }
 
 // ---- tensor map of the KV pool: rows of 128 elements, [pages*2*Hkv*128] rows ----
@@ -662,26 +1374,65 @@ bool encode_kv_map(CUtensorMap *map, const void *kv_pool, int kv_dtype, int num_
     return r == CUDA_SUCCESS;
 }
 
-template <bool FP8>
+template <bool FP8, int STAGES>
 size_t decode_smem_bytes(int T)
 {
-    using C = Cfg<FP8>;
-    return 1024 + C::kRingBytes + kQBufs * kQBytes + (C::kStages + kQBufs) * sizeof(uint64_t) +
-           2 * kWin * sizeof(int4) + sizeof(float) * (kGroup * kDim + 8 * kGroup) +
-           sizeof(int) * (size_t)(4 + T + 1);
+    return decode_layout(T, STAGES, Cfg<FP8, STAGES>::kTileBytes).total;
 }
 
-template <bool FP8>
+template <bool FP8, int STAGES>
 cudaError_t launch_decode_t(const DecodeParams &p, const CUtensorMap &map, int ctas,
                             cudaStream_t stream, bool pdl)
 {
-    const size_t smem = decode_smem_bytes<FP8>(p.T);
-    cudaError_t e = cudaFuncSetAttribute(sparse_decode_kernel<FP8>,
+    const size_t smem = decode_smem_bytes<FP8, STAGES>(p.T);
+    cudaError_t e = cudaFuncSetAttribute(sparse_decode_kernel<FP8, STAGES>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
-    e = launch_kernel(sparse_decode_kernel<FP8>, dim3(ctas), dim3(kDecThreads), smem, stream, pdl,
-                      map, p);
+    e = launch_kernel(sparse_decode_kernel<FP8, STAGES>, dim3(ctas), dim3(kDecThreads), smem,
+                      stream, pdl, map, p);
+    if (e != cudaSuccess)
+        return e;
+    return cudaGetLastError();
+}
+
+// The deepest ring that fits next to the token prefix (T + 1 ints).
+template <bool FP8>
+cudaError_t launch_decode_fit(const DecodeParams &p, const CUtensorMap &map, int ctas,
+                              cudaStream_t stream, bool pdl)
+{
+    constexpr int kDeep = FP8 ? 12 : 6, kShallow = FP8 ? 8 : 4;
+    if (decode_smem_bytes<FP8, kDeep>(p.T) <= (size_t)kMaxSmem)
+        return launch_decode_t<FP8, kDeep>(p, map, ctas, stream, pdl);
+    return launch_decode_t<FP8, kShallow>(p, map, ctas, stream, pdl);
+}
+
+// Query rows [T * Hq][128] bf16, boxes of 64 dims x 16 rows, 128-byte swizzle.
+bool encode_q_map(CUtensorMap *map, const void *q, int T, int Hkv)
+{
+    EncodeFn enc = get_encode();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)kDim, (cuuint64_t)T * Hkv * kGroup};
+    const cuuint64_t strides[1] = {(cuuint64_t)kDim * 2};
+    const cuuint32_t box[2] = {64u, (cuuint32_t)kGroup};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(q), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int STAGES>
+cudaError_t launch_umma_t(const DecodeParams &p, const CUtensorMap &kv, const CUtensorMap &qm,
+                          int ctas, cudaStream_t stream, bool pdl)
+{
+    const size_t smem = umma_layout(p.T, STAGES).total;
+    cudaError_t e = cudaFuncSetAttribute(sparse_decode_umma_kernel<STAGES>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    e = launch_kernel(sparse_decode_umma_kernel<STAGES>, dim3(ctas), dim3(kUThreads), smem, stream,
+                      pdl, kv, qm, p);
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();
@@ -696,8 +1447,13 @@ cudaError_t launch_sparse_decode(const DecodeParams &p, const void *kv_pool, int
     if (!encode_kv_map(&map, kv_pool, kv_dtype, p.num_pages, p.Hkv))
         return cudaErrorInvalidValue;
     if (kv_dtype == MSA_FP8_E4M3)
-        return launch_decode_t<true>(p, map, ctas, stream, pdl);
-    return launch_decode_t<false>(p, map, ctas, stream, pdl);
+        return launch_decode_fit<true>(p, map, ctas, stream, pdl);
+    CUtensorMap qmap;
+    if (!encode_q_map(&qmap, p.q, p.T, p.Hkv))
+        return cudaErrorInvalidValue;
+    if (umma_layout(p.T, 6).total <= (size_t)kMaxSmem)
+        return launch_umma_t<6>(p, map, qmap, ctas, stream, pdl);
+    return launch_umma_t<4>(p, map, qmap, ctas, stream, pdl);
 }
 
 } // namespace msa
