@@ -170,7 +170,8 @@ __device__ __forceinline__ bool range_empty(int c, long long P, int G)
     return (long long)c * P / G == (long long)(c + 1) * P / G;
 }
 
-// Table entry of task x: {K-tile row in the KV tensor map or -1, block id, t, g}.
+// Table entry of task x: {K-tile row in the KV tensor map or -1, visible
+// tokens of the page (1..128: the causal limit cuts the last block), t, g}.
 __device__ int4 make_entry(const DecodeParams &p, long long x, const int *qt)
 {
     const Task tk = task_of(x, qt, p.T);
@@ -187,7 +188,8 @@ __device__ int4 make_entry(const DecodeParams &p, long long x, const int *qt)
         else
             row = (int)(((page * 2) * p.Hkv + tk.g) * kPage);
     }
-    return make_int4(row, b, tk.t, tk.g);
+    const int nvis = min(kPage, p.seq_lens[r] + j - b * kPage);
+    return make_int4(row, nvis, tk.t, tk.g);
 }
 
 // Output dimension of accumulator column `col` (0..7) of n-tile nt.
@@ -577,8 +579,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 mbar_arrive(smem_u32(&qempty[qb]));
             ++cons_units;
         }
-        const int r = e.z / p.nq, j = e.z - r * p.nq;
-        const int Lvis = p.seq_lens[r] + j;
+        const int nvis = e.y; // visible tokens of this page
         const uint32_t tileK = smem_u32(ring + (size_t)sk * C::kTileBytes);
         const uint32_t tileV = smem_u32(ring + (size_t)sv * C::kTileBytes);
         const bool live = e.x >= 0;
@@ -637,15 +638,14 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         uint32_t pa[kKK][4];
         if (live) {
             // ---- scale, causal mask, online softmax (base 2) ----
-            const int pos0 = e.y * kPage + tb; // position of this warp's token 0
-            const bool need_mask = pos0 + kTPW > Lvis;
+            const bool need_mask = tb + kTPW > nvis;
             float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
             for (int n = 0; n < kNT; ++n) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     float v = s[n][k] * p.scale_log2;
-                    if (need_mask && pos0 + 8 * n + 2 * q4 + (k & 1) >= Lvis)
+                    if (need_mask && tb + 8 * n + 2 * q4 + (k & 1) >= nvis)
                         v = -INFINITY;
                     s[n][k] = v;
                     mx[k >> 1] = fmaxf(mx[k >> 1], v);
@@ -759,9 +759,11 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 // keep the running max / denominator per head, and fold each page's O^T into
 // 16 registers (one per head) once the next page's P^T is written.
 
-constexpr int kUWarps = 6;                 // producer, MMA, 4 softmax
+constexpr int kUSmxWarps = 8;              // softmax warps: two per TMEM lane quarter
+constexpr int kUWarps = 2 + kUSmxWarps;    // producer, MMA, softmax
 constexpr int kUThreads = 32 * kUWarps;
-constexpr int kUSoftmax = 128;             // softmax threads
+constexpr int kUSoftmax = 32 * kUSmxWarps; // softmax threads
+constexpr int kUHeads = 8;                 // heads per softmax thread (half of the group)
 constexpr int kUTmemCols = 64;             // S[2] + O[2], 16 columns each
 constexpr int kUTile = 32768;              // bf16 K or V tile of one (page, KV head)
 constexpr int kUQTile = 4096;              // 16 query rows of one unit, two 64-dim boxes
@@ -799,6 +801,20 @@ __host__ __device__ inline USmem umma_layout(int T, int stages)
     return L;
 }
 
+// 8 consecutive 32-bit TMEM columns of this thread's lane (warp-wide).
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8])
+{
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        v[i] = __uint_as_float(r[i]);
+}
+
 template <int STAGES>
 __global__ void __launch_bounds__(kUThreads, 1)
     sparse_decode_umma_kernel(const __grid_constant__ CUtensorMap kv_map,
@@ -821,8 +837,8 @@ __global__ void __launch_bounds__(kUThreads, 1)
     uint64_t *p_free = p_full + 2;
     uint64_t *o_full = p_free + 2;
     uint64_t *o_free = o_full + 2;
-    uint64_t *smx_bar = o_free + 2;    // softmax-warps barrier (128 arrivals)
-    uint64_t *done_bar = smx_bar + 1;  // softmax warps finished with TMEM (4 arrivals)
+    uint64_t *smx_bar = o_free + 2;    // softmax-warps barrier (kUSoftmax arrivals)
+    uint64_t *done_bar = smx_bar + 1;  // softmax warps finished with TMEM (kUSmxWarps arrivals)
     int4 *table = reinterpret_cast<int4 *>(base + lay.table);
     float *xbuf = reinterpret_cast<float *>(base + lay.xbuf);
     float *lbuf = reinterpret_cast<float *>(base + lay.lbuf);
@@ -844,14 +860,14 @@ __global__ void __launch_bounds__(kUThreads, 1)
             mbar_init(smem_u32(&qfull[b]), 1);
             mbar_init(smem_u32(&qempty[b]), 1);
             mbar_init(smem_u32(&s_full[b]), 1);
-            mbar_init(smem_u32(&s_free[b]), 4);
-            mbar_init(smem_u32(&p_full[b]), 4);
+            mbar_init(smem_u32(&s_free[b]), kUSmxWarps);
+            mbar_init(smem_u32(&p_full[b]), kUSmxWarps);
             mbar_init(smem_u32(&p_free[b]), 1);
             mbar_init(smem_u32(&o_full[b]), 1);
-            mbar_init(smem_u32(&o_free[b]), 4);
+            mbar_init(smem_u32(&o_free[b]), kUSmxWarps);
         }
         mbar_init(smem_u32(smx_bar), kUSoftmax);
-        mbar_init(smem_u32(done_bar), 4);
+        mbar_init(smem_u32(done_bar), kUSmxWarps);
         s_flag[0] = 0;
         s_flag[1] = 0;
         fence_mbar_init();
@@ -903,9 +919,9 @@ __global__ void __launch_bounds__(kUThreads, 1)
             if (!ok)
                 break;
             // The softmax warps trail the MMA warp by up to two tasks and the MMA
-            // warp trails this one by up to kAhead: only kAhead + 2 tasks into
+            // warp trails this one by up to kAhead: only kAhead + 3 tasks into
             // a window has every reader left the window before it.
-            if (l % kWin == kAhead + 2 && l >= kWin && (l / kWin + 1) * kWin < ntasks)
+            if (l % kWin == kAhead + 3 && l >= kWin && (l / kWin + 1) * kWin < ntasks)
                 fill_window(l / kWin + 1);
             if (lane == 0) {
                 const int4 e = entry(l);
@@ -963,35 +979,32 @@ __global__ void __launch_bounds__(kUThreads, 1)
 
     if (warp == 1) {
         // =================== MMA issuer (lane 0) ===================
+        // S^T(l + 1) is issued before P^T(l) is awaited, so the tensor core
+        // works on the next page while the softmax warps work on this one.
         constexpr uint32_t kIdescS = umma_idesc_bf16(128, 16, 0, 0); // K and Q^T both K-major
         constexpr uint32_t kIdescO = umma_idesc_bf16(128, 16, 1, 0); // V^T MN-major, P^T K-major
         bool ok = true;
         if (lane == 0) {
-            int cons_units = 0, cur_unit = -1;
-            for (int l = 0; l < ntasks && ok; ++l) {
-                const int zk = 2 * l, zv = zk + 1, b = l & 1;
-                ok = mbar_wait_or_abort(smem_u32(&full[zk % STAGES]), (zk / STAGES) & 1, abort_flag);
-                if (!ok)
-                    break;
+            int s_units = 0, s_unit = -1;
+            auto issue_s = [&](int l) -> bool {
+                const int zk = 2 * l, b = l & 1;
+                if (!mbar_wait_or_abort(smem_u32(&full[zk % STAGES]), (zk / STAGES) & 1, abort_flag))
+                    return false;
                 const int4 e = entry(l);
                 const int u = unit_of(e);
-                const int qb = (u != cur_unit ? cons_units : cons_units - 1) & 1;
-                if (u != cur_unit) {
-                    ok = mbar_wait_or_abort(smem_u32(&qfull[qb]), (cons_units >> 1) & 1, abort_flag);
-                    cur_unit = u;
-                    ++cons_units;
+                if (u != s_unit) {
+                    if (!mbar_wait_or_abort(smem_u32(&qfull[s_units & 1]), (s_units >> 1) & 1, abort_flag))
+                        return false;
+                    s_unit = u;
+                    ++s_units;
                 }
-                if (ok && l >= 2)
-                    ok = mbar_wait_or_abort(smem_u32(&s_free[b]), ((l >> 1) - 1) & 1, abort_flag);
-                if (!ok)
-                    break;
+                const int qb = (s_units - 1) & 1;
+                if (l >= 2 && !mbar_wait_or_abort(smem_u32(&s_free[b]), ((l >> 1) - 1) & 1, abort_flag))
+                    return false;
                 tcgen05_after_sync();
-                const bool live = e.x >= 0;
-                const uint32_t tileK = smem_u32(ring + (size_t)(zk % STAGES) * kUTile);
-                const uint32_t tileV = smem_u32(ring + (size_t)(zv % STAGES) * kUTile);
-                const uint32_t qtile = smem_u32(qbuf + qb * kUQTile);
-                const uint32_t ptile = smem_u32(pbuf + b * kUPTile);
-                if (live) {
+                if (e.x >= 0) {
+                    const uint32_t tileK = smem_u32(ring + (size_t)(zk % STAGES) * kUTile);
+                    const uint32_t qtile = smem_u32(qbuf + qb * kUQTile);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
                         const uint64_t a = umma_desc_sw128(tileK + (ks >> 2) * (kUTile / 2) + (ks & 3) * 32, 16, 1024);
@@ -1002,18 +1015,22 @@ __global__ void __launch_bounds__(kUThreads, 1)
                 umma_commit(smem_u32(&s_full[b]));
                 umma_commit(smem_u32(&empty[zk % STAGES])); // K tile read
                 // last task of its unit: the query tile can be replaced
-                const bool unit_ends = (l + 1 == ntasks) || unit_of(entry(l + 1)) != u;
-                if (unit_ends)
+                if (l + 1 == ntasks || unit_of(entry(l + 1)) != u)
                     umma_commit(smem_u32(&qempty[qb]));
-                ok = mbar_wait_or_abort(smem_u32(&full[zv % STAGES]), (zv / STAGES) & 1, abort_flag);
-                if (ok)
-                    ok = mbar_wait_or_abort(smem_u32(&p_full[b]), (l >> 1) & 1, abort_flag);
-                if (ok && l >= 2)
-                    ok = mbar_wait_or_abort(smem_u32(&o_free[b]), ((l >> 1) - 1) & 1, abort_flag);
-                if (!ok)
-                    break;
+                return true;
+            };
+            auto issue_pv = [&](int l) -> bool {
+                const int zv = 2 * l + 1, b = l & 1;
+                if (!mbar_wait_or_abort(smem_u32(&full[zv % STAGES]), (zv / STAGES) & 1, abort_flag))
+                    return false;
+                if (!mbar_wait_or_abort(smem_u32(&p_full[b]), (l >> 1) & 1, abort_flag))
+                    return false;
+                if (l >= 2 && !mbar_wait_or_abort(smem_u32(&o_free[b]), ((l >> 1) - 1) & 1, abort_flag))
+                    return false;
                 tcgen05_after_sync();
-                if (live) {
+                if (entry(l).x >= 0) {
+                    const uint32_t tileV = smem_u32(ring + (size_t)(zv % STAGES) * kUTile);
+                    const uint32_t ptile = smem_u32(pbuf + b * kUPTile);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
                         // V^T, MN-major: 16 tokens per k-step = 16 rows of 128 bytes;
@@ -1026,6 +1043,15 @@ __global__ void __launch_bounds__(kUThreads, 1)
                 umma_commit(smem_u32(&o_full[b]));
                 umma_commit(smem_u32(&p_free[b]));
                 umma_commit(smem_u32(&empty[zv % STAGES])); // V tile read
+                return true;
+            };
+            if (ntasks > 0)
+                ok = issue_s(0);
+            for (int l = 0; l < ntasks && ok; ++l) {
+                if (l + 1 < ntasks)
+                    ok = issue_s(l + 1);
+                if (ok)
+                    ok = issue_pv(l);
             }
             if (!ok) {
                 set_error(p.err, kErrTimeout);
@@ -1043,10 +1069,16 @@ __global__ void __launch_bounds__(kUThreads, 1)
         return;
     }
 
-    // =================== softmax warps 2..5 ===================
-    const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
+    // =================== softmax warps 2..9 ===================
+    // Warps w and w + 4 share TMEM lanes 32*(w & 3) .. +31 and split the 16
+    // heads into halves: each thread holds one token (of S^T) or one dimension
+    // (of O^T) for kUHeads heads.
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;      // heads 8*half .. 8*half + 7
+    const int h0 = kUHeads * half;
     const int idx = 32 * quarter + lane;   // token of S^T / dimension of O^T
-    const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16);
+    const int sidx = threadIdx.x - 64;     // 0 .. kUSoftmax - 1
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16) + h0;
     int sync_phase = 0;
     bool ok = true;
     auto ssync = [&]() {
@@ -1056,14 +1088,13 @@ __global__ void __launch_bounds__(kUThreads, 1)
         ++sync_phase;
     };
 
-    float o[16], lsum[16], m_run[16], alpha_prev[16];
+    float o[kUHeads], lsum[kUHeads], m_run[kUHeads], alpha_prev[kUHeads];
     bool pending = false; // a page's O^T waits to be folded in
-    int pending_b = 0;
     int cur_unit = -1, cur_t = 0, cur_g = 0;
 
     auto reset = [&]() {
 #pragma unroll
-        for (int h = 0; h < 16; ++h) {
+        for (int h = 0; h < kUHeads; ++h) {
             o[h] = 0.f;
             lsum[h] = 0.f;
             m_run[h] = -INFINITY;
@@ -1071,7 +1102,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
         }
     };
 
-    // fold the pending page's O^T (thread = dimension) into o[]
+    // fold the previous page's O^T (thread = dimension) into o[]
     auto fold = [&](int l_prev) {
         const int b = l_prev & 1;
         if (!mbar_wait_or_abort(smem_u32(&o_full[b]), (l_prev >> 1) & 1, abort_flag)) {
@@ -1080,10 +1111,10 @@ __global__ void __launch_bounds__(kUThreads, 1)
         }
         tcgen05_after_sync();
         if (pending) {
-            float v[16];
-            tmem_ld16(lane_base + 32 + 16 * b, v);
+            float v[kUHeads];
+            tmem_ld8(lane_base + 32 + 16 * b, v);
 #pragma unroll
-            for (int h = 0; h < 16; ++h)
+            for (int h = 0; h < kUHeads; ++h)
                 o[h] = o[h] * alpha_prev[h] + v[h];
         }
         tcgen05_before_sync();
@@ -1095,25 +1126,20 @@ __global__ void __launch_bounds__(kUThreads, 1)
 
     auto finalize = [&](int t, int g) {
         // denominators: reduce lsum over the 128 token lanes
-        float lr[16];
 #pragma unroll
-        for (int h = 0; h < 16; ++h) {
+        for (int h = 0; h < kUHeads; ++h) {
             float v = lsum[h];
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1)
                 v += __shfl_xor_sync(0xffffffffu, v, off);
-            lr[h] = v;
-        }
-        if (lane == 0) {
-#pragma unroll
-            for (int h = 0; h < 16; ++h)
-                lbuf[quarter * 16 + h] = lr[h];
+            if (lane == 0)
+                lbuf[quarter * 16 + h0 + h] = v;
         }
         ssync();
-        float L[16];
+        float L[kUHeads];
 #pragma unroll
-        for (int h = 0; h < 16; ++h)
-            L[h] = lbuf[h] + lbuf[16 + h] + lbuf[32 + h] + lbuf[48 + h];
+        for (int h = 0; h < kUHeads; ++h)
+            L[h] = lbuf[h0 + h] + lbuf[16 + h0 + h] + lbuf[32 + h0 + h] + lbuf[48 + h0 + h];
         ssync(); // lbuf is reused by the next unit
         const long long Pt = qt[p.T];
         const long long u_first = (long long)g * Pt + qt[t];
@@ -1122,43 +1148,35 @@ __global__ void __launch_bounds__(kUThreads, 1)
         const int c_last = owner_of(u_first + n_u - 1, P, G);
         const int u = g * p.T + t;
         const bool whole = c_first == c_last;
-        const size_t hbase = (size_t)t * p.Hkv * kGroup + (size_t)g * kGroup;
+        const size_t hbase = (size_t)t * p.Hkv * kGroup + (size_t)g * kGroup + h0;
         float *slot = p.partial + (size_t)(c + u) * kPartialFloats;
+        float Mi = -INFINITY, Li = 0.f; // head h0 + idx (idx < kUHeads)
+#pragma unroll
+        for (int h = 0; h < kUHeads; ++h)
+            if (h == idx) {
+                Mi = m_run[h];
+                Li = L[h];
+            }
         if (whole) {
 #pragma unroll
-            for (int h = 0; h < 16; ++h) {
+            for (int h = 0; h < kUHeads; ++h) {
                 const float inv = L[h] > 0.f ? 1.f / L[h] : 0.f;
                 p.out[(hbase + h) * kDim + idx] = (uint16_t)(pack_bf16(o[h] * inv, 0.f) & 0xFFFFu);
             }
-            if (idx < 16) {
-                float Mh = -INFINITY, Lh = 0.f;
-#pragma unroll
-                for (int h = 0; h < 16; ++h)
-                    if (h == idx) {
-                        Mh = m_run[h];
-                        Lh = L[h];
-                    }
-                p.lse[hbase + idx] = (Mh == -INFINITY) ? -INFINITY : (Mh + log2f(Lh)) * 0.69314718055994531f;
-            }
+            if (idx < kUHeads)
+                p.lse[hbase + idx] = (Mi == -INFINITY) ? -INFINITY : (Mi + log2f(Li)) * 0.69314718055994531f;
             return;
         }
 #pragma unroll
-        for (int h = 0; h < 16; ++h)
-            slot[h * kDim + idx] = o[h];
-        if (idx < 16) {
-            float Mh = -INFINITY, Lh = 0.f;
-#pragma unroll
-            for (int h = 0; h < 16; ++h)
-                if (h == idx) {
-                    Mh = m_run[h];
-                    Lh = L[h];
-                }
-            slot[kGroup * kDim + idx] = Mh;
-            slot[kGroup * kDim + kGroup + idx] = Lh;
+        for (int h = 0; h < kUHeads; ++h)
+            slot[(h0 + h) * kDim + idx] = o[h];
+        if (idx < kUHeads) {
+            slot[kGroup * kDim + h0 + idx] = Mi;
+            slot[kGroup * kDim + kGroup + h0 + idx] = Li;
         }
         __threadfence(); // publish this CTA's slot before counting in
         ssync();
-        if (threadIdx.x == 64) {
+        if (sidx == 0) {
             int arrivals = 0;
             for (int cc = c_first; cc <= c_last; ++cc)
                 arrivals += !range_empty(cc, P, G);
@@ -1170,7 +1188,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
             __threadfence();
             const float *sbase = p.partial + (size_t)(c_first + u) * kPartialFloats;
             const int nslots = c_last - c_first + 1;
-            const int sidx = threadIdx.x - 64; // 0..127
+            const size_t obase = (size_t)t * p.Hkv * kGroup + (size_t)g * kGroup;
             for (int e = sidx; e < kGroup * kDim / 8; e += kUSoftmax) {
                 const int row = e >> 4, d0 = (e & 15) * 8;
                 float Mx = -INFINITY;
@@ -1196,11 +1214,11 @@ __global__ void __launch_bounds__(kUThreads, 1)
                 packed.y = pack_bf16(acc[2] * inv, acc[3] * inv);
                 packed.z = pack_bf16(acc[4] * inv, acc[5] * inv);
                 packed.w = pack_bf16(acc[6] * inv, acc[7] * inv);
-                *reinterpret_cast<uint4 *>(p.out + (hbase + row) * kDim + d0) = packed;
+                *reinterpret_cast<uint4 *>(p.out + (obase + row) * kDim + d0) = packed;
                 if (d0 == 0)
-                    p.lse[hbase + row] = (Mx == -INFINITY) ? -INFINITY : (Mx + log2f(Lx)) * 0.69314718055994531f;
+                    p.lse[obase + row] = (Mx == -INFINITY) ? -INFINITY : (Mx + log2f(Lx)) * 0.69314718055994531f;
             }
-            if (threadIdx.x == 64)
+            if (sidx == 0)
                 p.counters[u] = 0; // ready for the next call
         }
         ssync(); // s_flag is reused by the next unit
@@ -1217,9 +1235,9 @@ __global__ void __launch_bounds__(kUThreads, 1)
         const int4 e = entry(l);
         const int u = unit_of(e);
         const bool live = e.x >= 0;
-        float sv[16];
+        float sv[kUHeads];
         if (live)
-            tmem_ld16(lane_base + 16 * b, sv);
+            tmem_ld8(lane_base + 16 * b, sv);
         tcgen05_before_sync();
         __syncwarp();
         if (lane == 0)
@@ -1242,35 +1260,31 @@ __global__ void __launch_bounds__(kUThreads, 1)
             l_last = -1;
         }
 
-        // page maxima per head (log2 domain), across the 128 tokens
-        const int r = e.z / p.nq, j = e.z - r * p.nq;
-        const int Lvis = p.seq_lens[r] + j;
-        const bool visible = live && e.y * kPage + idx < Lvis;
-        float wmax[16];
+        // page maxima per head (log2 domain) across the 128 tokens
+        const bool visible = live && idx < e.y;
+        float wmax[kUHeads];
 #pragma unroll
-        for (int h = 0; h < 16; ++h) {
+        for (int h = 0; h < kUHeads; ++h) {
             sv[h] = visible ? sv[h] * p.scale_log2 : -INFINITY;
             wmax[h] = warp_max_f32(sv[h]);
         }
         if (lane == 0) {
-            float4 *xw = reinterpret_cast<float4 *>(xbuf + (b * 4 + quarter) * 16);
+            float4 *xw = reinterpret_cast<float4 *>(xbuf + (b * 4 + quarter) * 16 + h0);
             xw[0] = make_float4(wmax[0], wmax[1], wmax[2], wmax[3]);
             xw[1] = make_float4(wmax[4], wmax[5], wmax[6], wmax[7]);
-            xw[2] = make_float4(wmax[8], wmax[9], wmax[10], wmax[11]);
-            xw[3] = make_float4(wmax[12], wmax[13], wmax[14], wmax[15]);
         }
         ssync();
-        float alpha[16], pv[16];
+        float alpha[kUHeads], pv[kUHeads];
 #pragma unroll
-        for (int h4 = 0; h4 < 4; ++h4) {
-            const float4 a0 = reinterpret_cast<const float4 *>(xbuf + (b * 4 + 0) * 16)[h4];
-            const float4 a1 = reinterpret_cast<const float4 *>(xbuf + (b * 4 + 1) * 16)[h4];
-            const float4 a2 = reinterpret_cast<const float4 *>(xbuf + (b * 4 + 2) * 16)[h4];
-            const float4 a3 = reinterpret_cast<const float4 *>(xbuf + (b * 4 + 3) * 16)[h4];
-            const float pm[4] = {fmaxf(fmaxf(a0.x, a1.x), fmaxf(a2.x, a3.x)),
-                                 fmaxf(fmaxf(a0.y, a1.y), fmaxf(a2.y, a3.y)),
-                                 fmaxf(fmaxf(a0.z, a1.z), fmaxf(a2.z, a3.z)),
-                                 fmaxf(fmaxf(a0.w, a1.w), fmaxf(a2.w, a3.w))};
+        for (int h4 = 0; h4 < kUHeads / 4; ++h4) {
+            float4 a[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                a[q] = reinterpret_cast<const float4 *>(xbuf + (b * 4 + q) * 16 + h0)[h4];
+            const float pm[4] = {fmaxf(fmaxf(a[0].x, a[1].x), fmaxf(a[2].x, a[3].x)),
+                                 fmaxf(fmaxf(a[0].y, a[1].y), fmaxf(a[2].y, a[3].y)),
+                                 fmaxf(fmaxf(a[0].z, a[1].z), fmaxf(a[2].z, a[3].z)),
+                                 fmaxf(fmaxf(a[0].w, a[1].w), fmaxf(a[2].w, a[3].w))};
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int h = 4 * h4 + k;
@@ -1291,8 +1305,9 @@ __global__ void __launch_bounds__(kUThreads, 1)
             uint8_t *pt = pbuf + b * kUPTile + (idx >> 6) * (kUPTile / 2);
             const int col = idx & 63;
 #pragma unroll
-            for (int h = 0; h < 16; ++h) {
-                const uint32_t off = h * 128 + ((((col >> 3) ^ (h & 7))) << 4) + (col & 7) * 2;
+            for (int h = 0; h < kUHeads; ++h) {
+                const int hh = h0 + h;
+                const uint32_t off = hh * 128 + ((((col >> 3) ^ (hh & 7))) << 4) + (col & 7) * 2;
                 *reinterpret_cast<uint16_t *>(pt + off) = (uint16_t)(pack_bf16(pv[h], 0.f) & 0xFFFFu);
             }
             fence_async_smem();
@@ -1307,15 +1322,13 @@ __global__ void __launch_bounds__(kUThreads, 1)
             if (!ok)
                 break;
         }
+        // a page with no data contributes p = 0 and leaves the state unchanged
 #pragma unroll
-        for (int h = 0; h < 16; ++h)
+        for (int h = 0; h < kUHeads; ++h)
             alpha_prev[h] = live ? alpha[h] : 1.f;
         pending = live;
-        pending_b = b;
         l_last = l;
-        // a skipped page (no data) contributes p = 0 and alpha = 1
     }
-    (void)pending_b;
     if (ok && cur_unit >= 0) {
         if (l_last >= 0)
             fold(l_last);
