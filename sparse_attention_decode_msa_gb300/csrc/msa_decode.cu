@@ -760,9 +760,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 // 16 registers (one per head) once the next page's P^T is written.
 
 constexpr int kUSmxWarps = 8;              // softmax warps: two per TMEM lane quarter
-constexpr int kUWarps = 2 + kUSmxWarps;    // producer, MMA, softmax
-constexpr int kUThreads = 32 * kUWarps;
+constexpr int kUCvtWarps = 4;              // FP8 only: E4M3 -> f16 converter warps
 constexpr int kUSoftmax = 32 * kUSmxWarps; // softmax threads
+template <bool FP8>
+constexpr int kUThreadsT = 32 * (2 + kUSmxWarps + (FP8 ? kUCvtWarps : 0)); // producer, MMA, softmax[, converters]
 constexpr int kUHeads = 8;                 // heads per softmax thread (half of the group)
 constexpr int kUTmemCols = 64;             // S[2] + O[2], 16 columns each
 constexpr int kUTile = 32768;              // bf16 K or V tile of one (page, KV head)
@@ -770,23 +771,28 @@ constexpr int kUQTile = 4096;              // 16 query rows of one unit, two 64-
 constexpr int kUPTile = 4096;              // P^T of one page: [16 heads][128 tokens] bf16
 
 struct USmem {
-    size_t ring, qbuf, pbuf, bars, table, xbuf, lbuf, misc, qt, total;
+    size_t ring, stage, qbuf, pbuf, bars, table, xbuf, lbuf, misc, qt, total;
 };
 
-__host__ __device__ inline USmem umma_layout(int T, int stages)
+// bf16: the ring holds the MMA operands.  FP8: the ring holds E4M3 tiles
+// (16 KiB) and one f16 staging tile each for K and V feeds the MMA.
+__host__ __device__ inline USmem umma_layout(int T, int stages, bool fp8)
 {
     USmem L{};
     size_t off = 0;
     L.ring = off;                          // 1024-aligned tiles
-    off += (size_t)stages * kUTile;
+    off += (size_t)stages * (fp8 ? kUTile / 2 : kUTile);
+    L.stage = off = align_to(off, 1024);   // FP8: K and V f16 tiles
+    off += fp8 ? 2 * kUTile : 0;
     L.qbuf = off = align_to(off, 1024);    // [2] query tiles (swizzle atoms: 1024-aligned)
     off += 2 * kUQTile;
     L.pbuf = off = align_to(off, 1024);    // [2] P^T tiles
     off += 2 * kUPTile;
     // full[S], empty[S], qfull[2], qempty[2], s_full[2], s_free[2], p_full[2],
-    // p_free[2], o_full[2], o_free[2], softmax sync, done
+    // p_free[2], o_full[2], o_free[2], softmax sync, done, then FP8 only:
+    // kst_full, kst_empty, vst_full, vst_empty, qconv[2]
     L.bars = off = align_to(off, 8);
-    off += (size_t)(2 * stages + 16 + 2) * 8;
+    off += (size_t)(2 * stages + 16 + 2 + 6) * 8;
     L.table = off = align_to(off, 16);     // [2][kWin] int4
     off += (size_t)2 * kWin * 16;
     L.xbuf = off = align_to(off, 16);      // [2][4 quarters][16] page maxima
@@ -815,16 +821,19 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8])
         v[i] = __uint_as_float(r[i]);
 }
 
-template <int STAGES>
-__global__ void __launch_bounds__(kUThreads, 1)
+template <bool FP8, int STAGES>
+__global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
     sparse_decode_umma_kernel(const __grid_constant__ CUtensorMap kv_map,
                               const __grid_constant__ CUtensorMap q_map, const DecodeParams p)
 {
+    constexpr int kRaw = FP8 ? kUTile / 2 : kUTile; // bytes of one ring tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const USmem lay = umma_layout(p.T, STAGES);
+    const USmem lay = umma_layout(p.T, STAGES, FP8);
     uint8_t *ring = base + lay.ring;
+    uint8_t *kst = base + lay.stage;        // FP8: f16 K tile
+    uint8_t *vst = kst + kUTile;            // FP8: f16 V tile
     uint8_t *qbuf = base + lay.qbuf;
     uint8_t *pbuf = base + lay.pbuf;
     uint64_t *full = reinterpret_cast<uint64_t *>(base + lay.bars);
@@ -839,6 +848,11 @@ __global__ void __launch_bounds__(kUThreads, 1)
     uint64_t *o_free = o_full + 2;
     uint64_t *smx_bar = o_free + 2;    // softmax-warps barrier (kUSoftmax arrivals)
     uint64_t *done_bar = smx_bar + 1;  // softmax warps finished with TMEM (kUSmxWarps arrivals)
+    uint64_t *kst_full = done_bar + 1; // FP8: staging K converted (kUCvtWarps)
+    uint64_t *kst_empty = kst_full + 1; // FP8: staging K read by the MMA (commit)
+    uint64_t *vst_full = kst_empty + 1;
+    uint64_t *vst_empty = vst_full + 1;
+    uint64_t *qconv = vst_empty + 1;   // FP8: [2] query tile widened to f16 (kUCvtWarps)
     int4 *table = reinterpret_cast<int4 *>(base + lay.table);
     float *xbuf = reinterpret_cast<float *>(base + lay.xbuf);
     float *lbuf = reinterpret_cast<float *>(base + lay.lbuf);
@@ -854,9 +868,14 @@ __global__ void __launch_bounds__(kUThreads, 1)
         prefetch_tensormap(&q_map);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&empty[s]), 1);
+            mbar_init(smem_u32(&empty[s]), FP8 ? kUCvtWarps : 1);
         }
+        mbar_init(smem_u32(kst_full), kUCvtWarps);
+        mbar_init(smem_u32(kst_empty), 1);
+        mbar_init(smem_u32(vst_full), kUCvtWarps);
+        mbar_init(smem_u32(vst_empty), 1);
         for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&qconv[b]), kUCvtWarps);
             mbar_init(smem_u32(&qfull[b]), 1);
             mbar_init(smem_u32(&qempty[b]), 1);
             mbar_init(smem_u32(&s_full[b]), 1);
@@ -919,9 +938,10 @@ __global__ void __launch_bounds__(kUThreads, 1)
             if (!ok)
                 break;
             // The softmax warps trail the MMA warp by up to two tasks and the MMA
-            // warp trails this one by up to kAhead: only kAhead + 3 tasks into
-            // a window has every reader left the window before it.
-            if (l % kWin == kAhead + 3 && l >= kWin && (l / kWin + 1) * kWin < ntasks)
+            // warp trails this one by up to kAhead (kAhead + 1 with the FP8
+            // converters between them): only kAhead + 3 (+ 1) tasks into a
+            // window has every reader left the window before it.
+            if (l % kWin == kAhead + 3 + (FP8 ? 1 : 0) && l >= kWin && (l / kWin + 1) * kWin < ntasks)
                 fill_window(l / kWin + 1);
             if (lane == 0) {
                 const int4 e = entry(l);
@@ -957,11 +977,12 @@ __global__ void __launch_bounds__(kUThreads, 1)
                         mbar_arrive(bar); // no data: consumers skip the task
                         continue;
                     }
-                    const uint32_t dst = smem_u32(ring + (size_t)st * kUTile);
+                    const uint32_t dst = smem_u32(ring + (size_t)st * kRaw);
                     const int row = e.x + kv * p.Hkv * kPage;
-                    mbar_arrive_expect_tx(bar, kUTile);
+                    mbar_arrive_expect_tx(bar, kRaw);
                     tma_load_2d(dst, &kv_map, 0, row, bar);
-                    tma_load_2d(dst + kUTile / 2, &kv_map, 64, row, bar);
+                    if (!FP8)
+                        tma_load_2d(dst + kUTile / 2, &kv_map, 64, row, bar);
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -981,19 +1002,24 @@ __global__ void __launch_bounds__(kUThreads, 1)
         // =================== MMA issuer (lane 0) ===================
         // S^T(l + 1) is issued before P^T(l) is awaited, so the tensor core
         // works on the next page while the softmax warps work on this one.
-        constexpr uint32_t kIdescS = umma_idesc_bf16(128, 16, 0, 0); // K and Q^T both K-major
-        constexpr uint32_t kIdescO = umma_idesc_bf16(128, 16, 1, 0); // V^T MN-major, P^T K-major
+        // bf16 operands, or f16 for FP8 KV (widened E4M3, f16 Q and P)
+        constexpr uint32_t kF16 = FP8 ? ~((7u << 7) | (7u << 10)) : ~0u;
+        constexpr uint32_t kIdescS = umma_idesc_bf16(128, 16, 0, 0) & kF16; // K and Q^T both K-major
+        constexpr uint32_t kIdescO = umma_idesc_bf16(128, 16, 1, 0) & kF16; // V^T MN-major, P^T K-major
         bool ok = true;
         if (lane == 0) {
             int s_units = 0, s_unit = -1;
             auto issue_s = [&](int l) -> bool {
                 const int zk = 2 * l, b = l & 1;
-                if (!mbar_wait_or_abort(smem_u32(&full[zk % STAGES]), (zk / STAGES) & 1, abort_flag))
+                if (!FP8 && !mbar_wait_or_abort(smem_u32(&full[zk % STAGES]), (zk / STAGES) & 1, abort_flag))
+                    return false;
+                if (FP8 && !mbar_wait_or_abort(smem_u32(kst_full), l & 1, abort_flag))
                     return false;
                 const int4 e = entry(l);
                 const int u = unit_of(e);
                 if (u != s_unit) {
-                    if (!mbar_wait_or_abort(smem_u32(&qfull[s_units & 1]), (s_units >> 1) & 1, abort_flag))
+                    uint64_t *qb_bar = FP8 ? qconv : qfull;
+                    if (!mbar_wait_or_abort(smem_u32(&qb_bar[s_units & 1]), (s_units >> 1) & 1, abort_flag))
                         return false;
                     s_unit = u;
                     ++s_units;
@@ -1003,7 +1029,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
                     return false;
                 tcgen05_after_sync();
                 if (e.x >= 0) {
-                    const uint32_t tileK = smem_u32(ring + (size_t)(zk % STAGES) * kUTile);
+                    const uint32_t tileK = FP8 ? smem_u32(kst) : smem_u32(ring + (size_t)(zk % STAGES) * kRaw);
                     const uint32_t qtile = smem_u32(qbuf + qb * kUQTile);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
@@ -1013,7 +1039,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
                     }
                 }
                 umma_commit(smem_u32(&s_full[b]));
-                umma_commit(smem_u32(&empty[zk % STAGES])); // K tile read
+                umma_commit(FP8 ? smem_u32(kst_empty) : smem_u32(&empty[zk % STAGES])); // K tile read
                 // last task of its unit: the query tile can be replaced
                 if (l + 1 == ntasks || unit_of(entry(l + 1)) != u)
                     umma_commit(smem_u32(&qempty[qb]));
@@ -1021,7 +1047,9 @@ __global__ void __launch_bounds__(kUThreads, 1)
             };
             auto issue_pv = [&](int l) -> bool {
                 const int zv = 2 * l + 1, b = l & 1;
-                if (!mbar_wait_or_abort(smem_u32(&full[zv % STAGES]), (zv / STAGES) & 1, abort_flag))
+                if (!FP8 && !mbar_wait_or_abort(smem_u32(&full[zv % STAGES]), (zv / STAGES) & 1, abort_flag))
+                    return false;
+                if (FP8 && !mbar_wait_or_abort(smem_u32(vst_full), l & 1, abort_flag))
                     return false;
                 if (!mbar_wait_or_abort(smem_u32(&p_full[b]), (l >> 1) & 1, abort_flag))
                     return false;
@@ -1029,7 +1057,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
                     return false;
                 tcgen05_after_sync();
                 if (entry(l).x >= 0) {
-                    const uint32_t tileV = smem_u32(ring + (size_t)(zv % STAGES) * kUTile);
+                    const uint32_t tileV = FP8 ? smem_u32(vst) : smem_u32(ring + (size_t)(zv % STAGES) * kRaw);
                     const uint32_t ptile = smem_u32(pbuf + b * kUPTile);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
@@ -1042,7 +1070,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
                 }
                 umma_commit(smem_u32(&o_full[b]));
                 umma_commit(smem_u32(&p_free[b]));
-                umma_commit(smem_u32(&empty[zv % STAGES])); // V tile read
+                umma_commit(FP8 ? smem_u32(vst_empty) : smem_u32(&empty[zv % STAGES])); // V tile read
                 return true;
             };
             if (ntasks > 0)
@@ -1066,6 +1094,94 @@ __global__ void __launch_bounds__(kUThreads, 1)
         __syncwarp();
         tcgen05_after_sync();
         tmem_dealloc(tmem, kUTmemCols);
+        return;
+    }
+
+    if (FP8 && warp >= 2 + kUSmxWarps) {
+        // =================== converter warps (FP8) ===================
+        // E4M3 K / V tiles from the ring into the f16 staging tiles, in the
+        // two-64-dim-box, 128-byte-swizzled layout the MMA descriptors read;
+        // the query tile of each new unit is widened from bf16 to f16 in place.
+        const int ct = threadIdx.x - 32 * (2 + kUSmxWarps); // 0..127
+        bool ok = true;
+        int units = 0, cur = -1;
+        auto convert = [&](const uint8_t *raw, uint8_t *dst) {
+#pragma unroll 2
+            for (int item = ct; item < kPage * 8; item += 32 * kUCvtWarps) {
+                const int r = item >> 3, c = item & 7; // row, 16-byte chunk of 16 E4M3 dims
+                const uint4 w = *reinterpret_cast<const uint4 *>(raw + r * 128 + ((c ^ (r & 7)) << 4));
+                uint4 lo, hi;
+                lo.x = e4m3x2_to_f16x2(w.x & 0xFFFFu);
+                lo.y = e4m3x2_to_f16x2(w.x >> 16);
+                lo.z = e4m3x2_to_f16x2(w.y & 0xFFFFu);
+                lo.w = e4m3x2_to_f16x2(w.y >> 16);
+                hi.x = e4m3x2_to_f16x2(w.z & 0xFFFFu);
+                hi.y = e4m3x2_to_f16x2(w.z >> 16);
+                hi.z = e4m3x2_to_f16x2(w.w & 0xFFFFu);
+                hi.w = e4m3x2_to_f16x2(w.w >> 16);
+                const int h = c >> 2, c0 = 2 * (c & 3);  // box (64 dims), first 8-dim chunk
+                uint8_t *row = dst + h * (kUTile / 2) + r * 128;
+                *reinterpret_cast<uint4 *>(row + ((c0 ^ (r & 7)) << 4)) = lo;
+                *reinterpret_cast<uint4 *>(row + (((c0 + 1) ^ (r & 7)) << 4)) = hi;
+            }
+            fence_async_smem();
+        };
+        for (int l = 0; l < ntasks && ok; ++l) {
+            const int zk = 2 * l, zv = zk + 1;
+            ok = mbar_wait_or_abort(smem_u32(&full[zk % STAGES]), (zk / STAGES) & 1, abort_flag);
+            if (!ok)
+                break;
+            const int4 e = entry(l);
+            const int u = unit_of(e);
+            if (u != cur) {
+                const int qb = units & 1;
+                ok = mbar_wait_or_abort(smem_u32(&qfull[qb]), (units >> 1) & 1, abort_flag);
+                if (!ok)
+                    break;
+                uint8_t *q = qbuf + qb * kUQTile;
+                for (int i = ct; i < kUQTile / 16; i += 32 * kUCvtWarps) {
+                    uint4 v = reinterpret_cast<uint4 *>(q)[i];
+                    v.x = bf16x2_to_f16x2(v.x);
+                    v.y = bf16x2_to_f16x2(v.y);
+                    v.z = bf16x2_to_f16x2(v.z);
+                    v.w = bf16x2_to_f16x2(v.w);
+                    reinterpret_cast<uint4 *>(q)[i] = v;
+                }
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_u32(&qconv[qb]));
+                cur = u;
+                ++units;
+            }
+            if (l >= 1)
+                ok = mbar_wait_or_abort(smem_u32(kst_empty), (l - 1) & 1, abort_flag);
+            if (!ok)
+                break;
+            if (e.x >= 0)
+                convert(ring + (size_t)(zk % STAGES) * kRaw, kst);
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(smem_u32(kst_full));
+                mbar_arrive(smem_u32(&empty[zk % STAGES]));
+            }
+            ok = mbar_wait_or_abort(smem_u32(&full[zv % STAGES]), (zv / STAGES) & 1, abort_flag);
+            if (ok && l >= 1)
+                ok = mbar_wait_or_abort(smem_u32(vst_empty), (l - 1) & 1, abort_flag);
+            if (!ok)
+                break;
+            if (e.x >= 0)
+                convert(ring + (size_t)(zv % STAGES) * kRaw, vst);
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(smem_u32(vst_full));
+                mbar_arrive(smem_u32(&empty[zv % STAGES]));
+            }
+        }
+        if (!ok) {
+            set_error(p.err, kErrTimeout);
+            *abort_flag = 1;
+        }
         return;
     }
 
@@ -1157,6 +1273,9 @@ __global__ void __launch_bounds__(kUThreads, 1)
                 Mi = m_run[h];
                 Li = L[h];
             }
+#pragma unroll
+        for (int h = 0; h < kUHeads; ++h)
+            o[h] *= p.v_scale; // 1 for bf16 values
         if (whole) {
 #pragma unroll
             for (int h = 0; h < kUHeads; ++h) {
@@ -1308,7 +1427,8 @@ __global__ void __launch_bounds__(kUThreads, 1)
             for (int h = 0; h < kUHeads; ++h) {
                 const int hh = h0 + h;
                 const uint32_t off = hh * 128 + ((((col >> 3) ^ (hh & 7))) << 4) + (col & 7) * 2;
-                *reinterpret_cast<uint16_t *>(pt + off) = (uint16_t)(pack_bf16(pv[h], 0.f) & 0xFFFFu);
+                const uint32_t pk = FP8 ? pack_f16(pv[h], 0.f) : pack_bf16(pv[h], 0.f);
+                *reinterpret_cast<uint16_t *>(pt + off) = (uint16_t)(pk & 0xFFFFu);
             }
             fence_async_smem();
         }
@@ -1435,17 +1555,17 @@ bool encode_q_map(CUtensorMap *map, const void *q, int T, int Hkv)
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int STAGES>
+template <bool FP8, int STAGES>
 cudaError_t launch_umma_t(const DecodeParams &p, const CUtensorMap &kv, const CUtensorMap &qm,
                           int ctas, cudaStream_t stream, bool pdl)
 {
-    const size_t smem = umma_layout(p.T, STAGES).total;
-    cudaError_t e = cudaFuncSetAttribute(sparse_decode_umma_kernel<STAGES>,
+    const size_t smem = umma_layout(p.T, STAGES, FP8).total;
+    cudaError_t e = cudaFuncSetAttribute(sparse_decode_umma_kernel<FP8, STAGES>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
-    e = launch_kernel(sparse_decode_umma_kernel<STAGES>, dim3(ctas), dim3(kUThreads), smem, stream,
-                      pdl, kv, qm, p);
+    e = launch_kernel(sparse_decode_umma_kernel<FP8, STAGES>, dim3(ctas), dim3(kUThreadsT<FP8>), smem,
+                      stream, pdl, kv, qm, p);
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();
@@ -1459,14 +1579,17 @@ cudaError_t launch_sparse_decode(const DecodeParams &p, const void *kv_pool, int
     CUtensorMap map;
     if (!encode_kv_map(&map, kv_pool, kv_dtype, p.num_pages, p.Hkv))
         return cudaErrorInvalidValue;
-    if (kv_dtype == MSA_FP8_E4M3)
-        return launch_decode_fit<true>(p, map, ctas, stream, pdl);
     CUtensorMap qmap;
     if (!encode_q_map(&qmap, p.q, p.T, p.Hkv))
         return cudaErrorInvalidValue;
-    if (umma_layout(p.T, 6).total <= (size_t)kMaxSmem)
-        return launch_umma_t<6>(p, map, qmap, ctas, stream, pdl);
-    return launch_umma_t<4>(p, map, qmap, ctas, stream, pdl);
+    if (kv_dtype == MSA_FP8_E4M3) {
+        if (umma_layout(p.T, 8, true).total <= (size_t)kMaxSmem)
+            return launch_umma_t<true, 8>(p, map, qmap, ctas, stream, pdl);
+        return launch_umma_t<true, 4>(p, map, qmap, ctas, stream, pdl);
+    }
+    if (umma_layout(p.T, 6, false).total <= (size_t)kMaxSmem)
+        return launch_umma_t<false, 6>(p, map, qmap, ctas, stream, pdl);
+    return launch_umma_t<false, 4>(p, map, qmap, ctas, stream, pdl);
 }
 
 } // namespace msa

@@ -439,6 +439,8 @@ __device__ __forceinline__ float ex2(float x)
 __device__ __forceinline__ uint32_t order_key(float f)
 {
     uint32_t u = __float_as_uint(f);
+    if (u == 0x80000000u) // -0 equals +0: one key, so the tie goes by block index
+        u = 0u;
     return u ^ ((u >> 31) ? 0xFFFFFFFFu : 0x80000000u);
 }
 

@@ -6,9 +6,10 @@
 // any tie width.  Output ("Add Rubin (sm_107) MiniMax-M3.1 low-latency decode
 // targets", q8kv4 indexer commit): ascending block ids, -1 padded to k.
 //
-// One CTA per token.  Scores map to order-preserving 32-bit keys; an MSB-first
-// radix select (four 8-bit digits) finds the k-th largest key theta and how
-// many of the blocks equal to theta are still needed.  A block is selected if
+// Scores map to order-preserving 32-bit keys.  Rows of up to 2048 blocks take
+// one warp per token (below); longer rows one CTA per token, where an
+// MSB-first radix select (four 8-bit digits) finds the k-th largest key theta
+// and how many of the blocks equal to theta are still needed.  A block is selected if
 // its key is above theta, or equal to theta and among the first `need` such
 // blocks in index order.  Two CTA-wide exclusive scans over blocks in index
 // order give each tie its rank and each selected block its output slot, so
@@ -179,10 +180,104 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(const SelectPa
         out[i] = -1;
 }
 
+// ---------------------------------------------------------------------------
+// Rows of up to 2048 blocks: one warp per token, no CTA barrier.  Lane l holds
+// the keys of blocks l, l + 32, ... in registers.  theta, the k-th largest
+// key, is built bit by bit from the top: a bit is kept while at least k keys
+// are >= the candidate (a warp-wide sum per bit).  The selection pass walks
+// the blocks in index order 32 at a time; ballots give each tie its rank and
+// each selected block its output slot, so the table comes out ascending.
+constexpr int kWarpSelWarps = 4;
+constexpr int kWarpSelMaxN = 2048;
+
+template <int S> // key slots per lane: rows of up to 32 * S blocks
+__global__ void __launch_bounds__(32 * kWarpSelWarps) select_topk_warp_kernel(const SelectParams p)
+{
+    launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int T = p.R * p.nq;
+    const int t = blockIdx.x * kWarpSelWarps + (threadIdx.x >> 5);
+    if (t >= T)
+        return;
+    const int r = t / p.nq, j = t - r * p.nq;
+    int32_t *out = p.selected + (size_t)t * p.k;
+    const int seq_len = p.seq_lens[r];
+    const long long nb_req = ((long long)seq_len + p.nq - 1 + kPage - 1) / kPage;
+    if (seq_len < 1 || nb_req > p.maxB) {
+        if (lane == 0)
+            set_error(p.err, kErrSeqLen);
+        for (int i = lane; i < p.k; i += 32)
+            out[i] = -1;
+        return;
+    }
+    const int n = ceil_div(seq_len + j, kPage);
+    if (n <= p.k) {
+        for (int i = lane; i < p.k; i += 32)
+            out[i] = i < n ? i : -1;
+        return;
+    }
+    grid_dependency_wait(); // block_scores come from the previous kernel of the step
+    const float *row = p.block_scores + (size_t)t * p.maxB;
+    uint32_t key[S];
+#pragma unroll
+    for (int s = 0; s < S; ++s) {
+        const int b = lane + 32 * s;
+        // blocks past n take key 0, below every candidate tried (all >= 1)
+        key[s] = b < n ? order_key(row[b]) : 0u;
+    }
+    uint32_t theta = 0;
+#pragma unroll 1
+    for (int bit = 31; bit >= 0; --bit) {
+        const uint32_t cand = theta | (1u << bit);
+        int c0 = 0, c1 = 0;
+#pragma unroll
+        for (int s = 0; s < S; s += 2) {
+            c0 += key[s] >= cand;
+            c1 += key[s + 1] >= cand;
+        }
+        if ((int)__reduce_add_sync(0xffffffffu, (unsigned)(c0 + c1)) >= p.k)
+            theta = cand;
+    }
+    int gt = 0;
+#pragma unroll
+    for (int s = 0; s < S; ++s)
+        gt += key[s] > theta;
+    // blocks equal to theta still needed, taken in index order
+    const int need = p.k - (int)__reduce_add_sync(0xffffffffu, (unsigned)gt);
+    const uint32_t below = (1u << lane) - 1u;
+    int ties = 0, slot = 0;
+#pragma unroll
+    for (int s = 0; s < S; ++s) {
+        const bool eq = key[s] == theta;
+        const uint32_t em = __ballot_sync(0xffffffffu, eq);
+        const bool sel = key[s] > theta || (eq && ties + __popc(em & below) < need);
+        ties += __popc(em);
+        const uint32_t sm = __ballot_sync(0xffffffffu, sel);
+        if (sel)
+            out[slot + __popc(sm & below)] = lane + 32 * s;
+        slot += __popc(sm);
+    }
+}
+
 } // namespace
 
 cudaError_t launch_select(const SelectParams &p, cudaStream_t stream, bool pdl)
 {
+    if (p.maxB <= kWarpSelMaxN) {
+        const dim3 grid((p.R * p.nq + kWarpSelWarps - 1) / kWarpSelWarps), block(32 * kWarpSelWarps);
+        cudaError_t e;
+        if (p.maxB <= 256)
+            e = launch_kernel(select_topk_warp_kernel<8>, grid, block, 0, stream, pdl, p);
+        else if (p.maxB <= 512)
+            e = launch_kernel(select_topk_warp_kernel<16>, grid, block, 0, stream, pdl, p);
+        else if (p.maxB <= 1024)
+            e = launch_kernel(select_topk_warp_kernel<32>, grid, block, 0, stream, pdl, p);
+        else
+            e = launch_kernel(select_topk_warp_kernel<64>, grid, block, 0, stream, pdl, p);
+        if (e != cudaSuccess)
+            return e;
+        return cudaGetLastError();
+    }
     const size_t smem = sizeof(uint32_t) * (size_t)p.maxB;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(select_topk_kernel,

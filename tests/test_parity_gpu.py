@@ -189,9 +189,14 @@ def test_select_random_rows_with_heavy_ties(torch_cuda):
     import sparse_attention_decode_msa_gb300 as msa
 
     rng = np.random.default_rng(77)
-    for k, maxB, R in [(1, 40, 64), (16, 1024, 48), (33, 700, 20), (256, 3000, 12), (7, 9216, 4)]:
+    # one warp per token (maxB <= 2048: 8, 16, 32 or 64 keys a lane) and one
+    # CTA per token (longer rows); -0.0 and +0.0 are the same score
+    for k, maxB, R in [(1, 40, 64), (16, 256, 30), (16, 1024, 48), (32, 1024, 24), (2, 513, 20),
+                       (33, 700, 20), (200, 256, 9), (64, 2048, 10), (16, 1500, 7),
+                       (256, 3000, 12), (7, 9216, 4)]:
         seq_lens = rng.integers(1, maxB * 128 + 1, size=R).astype(np.int32)
         scores = rng.integers(-3, 4, size=(R, 1, maxB)).astype(np.float32)
+        scores[(scores == 0) & (rng.random(scores.shape) < 0.5)] = -0.0
         shape = msa.make_shape(num_requests=R, q_per_req=1, num_kv_heads=1, num_pages=1,
                                max_blocks_per_seq=maxB, topk=k)
         ws_bytes = msa.msa_workspace_bytes(shape)
