@@ -3,16 +3,18 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config IDX] [--impl ours|reference]
 
 A step is one msa_decode_step over the whole batch of the workload (index
-score + block max, top-k select, sparse GQA decode + merge).  Timing:
+score + block max, top-k select, sparse GQA decode with its split merge).
+Timing:
 
-* value / ms_per_step: K back-to-back replays of a CUDA graph of the step,
-  bracketed by CUDA events on the launching stream.  The workload's KV and
-  index-K pools (and the step inputs) exist in several device copies that the
-  steps cycle through, sized so that at least 4x the 129 MB L2 of other data
-  is touched between two uses of the same copy: every step reads its inputs
-  from HBM.
-* stage times: the same protocol per stage (score, select, decode + merge),
-  used for the roofline of the dominant kernel.
+* value / ms_per_step: exactly K steps, bracketed by CUDA events on the
+  launching stream, run as CUDA graphs that each hold one step per device
+  copy of the workload (the last graph holds the K mod copies remainder).
+  The workload's KV and index-K pools (and the step inputs) exist in several
+  device copies that the steps cycle through, sized so that at least 4x the
+  129 MB L2 of other data is touched between two uses of the same copy: every
+  step reads its inputs from HBM.
+* stage times: the same protocol per stage (score, select, decode), used for
+  the roofline of the dominant kernel.
 * e2e: the public C-ABI call with host inputs: per step a copy of the step's
   inputs (q, q_idx, block table, seq_lens) from pinned host memory, the call,
   and a copy of out + lse back to pinned host memory, all on one stream.
@@ -44,6 +46,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 L2_BYTES = 129 * 1000 * 1000
+KERNELS_PER_STEP = 3  # index score, select, sparse decode
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_PATH = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 FALLBACK_HBM_GBS = 6800.0
@@ -237,46 +240,59 @@ def run_ours(args, rank, world, local):
     reps = [base] + [base.replicate() for _ in range(nrep - 1)]
     stream = torch.cuda.Stream()
 
-    def capture(fn):
-        graphs = []
-        for dp in reps:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.stream(stream):
+    def capture(fn, count):
+        """One graph running fn on replicas 0 .. count-1 in turn (count steps)."""
+        with torch.cuda.stream(stream):
+            for dp in reps[:count]:
                 fn(dp, stream)  # warm (attribute setup) outside capture
-                stream.synchronize()
-                with torch.cuda.graph(g, stream=stream):
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for dp in reps[:count]:
                     fn(dp, stream)
-            graphs.append(g)
         torch.cuda.synchronize()
-        return graphs
+        return g
 
     def step_fn(dp, s):
         dp.decode_step(keep_intermediates=False, stream=s.cuda_stream)
 
-    step_graphs = capture(step_fn)
-    stage_graphs = {
-        "index_score": capture(lambda dp, s: dp.index_score(stream=s.cuda_stream)),
-        "select_topk": capture(lambda dp, s: dp.select(stream=s.cuda_stream)),
-        "sparse_decode": capture(lambda dp, s: dp.sparse_decode(stream=s.cuda_stream)),
+    stage_fns = {
+        "index_score": lambda dp, s: dp.index_score(stream=s.cuda_stream),
+        "select_topk": lambda dp, s: dp.select(stream=s.cuda_stream),
+        "sparse_decode": lambda dp, s: dp.sparse_decode(stream=s.cuda_stream),
     }
+    graph_cache = {}
 
-    def timed_replays(graphs, k):
+    def graphs_for(name, fn, k):
+        """Graphs whose replays run exactly k launches of fn: full rounds over
+        the nrep replicas, then the remainder."""
+        full, rem = divmod(k, nrep)
+        if (name, nrep) not in graph_cache:
+            graph_cache[(name, nrep)] = capture(fn, nrep)
+        seq = [graph_cache[(name, nrep)]] * full
+        if rem:
+            if (name, rem) not in graph_cache:
+                graph_cache[(name, rem)] = capture(fn, rem)
+            seq.append(graph_cache[(name, rem)])
+        return seq
+
+    def timed_replays(name, fn, k):
+        seq = graphs_for(name, fn, k)
         ev0 = torch.cuda.Event(enable_timing=True)
         ev1 = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
             ev0.record(stream)
-            for i in range(k):
-                graphs[i % len(graphs)].replay()
+            for g in seq:
+                g.replay()
             ev1.record(stream)
         ev1.synchronize()
-        return ev0.elapsed_time(ev1) / k  # ms per replay
+        return ev0.elapsed_time(ev1) / k  # ms per launch of fn
 
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
 
-    for i in range(args.warmup):
-        step_graphs[i % nrep].replay()
+    timed_replays("step", step_fn, max(args.warmup, 1))  # untimed warm-up steps
     torch.cuda.synchronize()
 
     # ---- the timed region: exactly K steps ----
@@ -284,7 +300,7 @@ def run_ours(args, rank, world, local):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t_start = time.time()
-    ms_step = timed_replays(step_graphs, args.steps)
+    ms_step = timed_replays("step", step_fn, args.steps)
     torch.cuda.synchronize()
     t_end = time.time()
     if world > 1:
@@ -296,7 +312,7 @@ def run_ours(args, rank, world, local):
     if t_end - t_start < 1.5:
         n = max(1, int(1.5e3 / max(ms_step, 1e-3)))
         ts0 = time.time()
-        timed_replays(step_graphs, n)
+        timed_replays("step", step_fn, n)
         t_end2 = time.time()
         soak_label = f"timed region + {t_end2 - ts0:.1f} s of the same replays right after it"
         t_end = t_end2
@@ -304,10 +320,9 @@ def run_ours(args, rank, world, local):
     # ---- per-stage times (same protocol) ----
     k_stage = max(args.steps, 50)
     stage_ms = {}
-    for name, graphs in stage_graphs.items():
-        for i in range(5):
-            graphs[i % nrep].replay()
-        stage_ms[name] = timed_replays(graphs, k_stage)
+    for name, fn in stage_fns.items():
+        timed_replays(name, fn, 5)
+        stage_ms[name] = timed_replays(name, fn, k_stage)
 
     # ---- e2e through the public C ABI with pinned host buffers ----
     host = []
@@ -386,7 +401,7 @@ def run_ours(args, rank, world, local):
             "kv_dtype": pb.kv_dtype, "index_dtype": pb.index_dtype,
             "l2": (f"inputs larger than L2: {nrep} device copies of the pools cycled, "
                    f"{(nrep - 1) * nbytes['total'] / 1e6:.0f} MB touched between reuses of a copy"),
-            "timing": "CUDA-graph replays of msa_decode_step, CUDA events on the launch stream",
+            "timing": "CUDA graphs of consecutive msa_decode_step calls, one per device copy; CUDA events on the launch stream",
         },
         "fused_step_us": round(ms_step_max * 1e3, 2),
         "algorithmic_bytes": nbytes,
@@ -407,7 +422,7 @@ def run_ours(args, rank, world, local):
         "e2e": {"value": round(e2e_value, 1), "unit": "query-tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 5)},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

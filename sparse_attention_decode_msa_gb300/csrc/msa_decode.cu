@@ -24,16 +24,14 @@
 //   V tile of KV head g (32 KiB each in bf16, 16 KiB in FP8) by TMA
 //   (cp.async.bulk.tensor, 128-byte swizzle) into a ring of shared-memory
 //   stages, each guarded by a "full" mbarrier (bytes landed) and an "empty"
-//   mbarrier (all consumer warps done), and the 16 query rows of each unit
-//   (4 KiB) by a 1-D bulk copy.  Consumers hand a K stage back as soon as
-//   Q K^T has read it.  Page offsets are 64-bit.
-// * Math.  Each of the 8 consumer warps owns 16 of the page's 128 tokens and
-//   keeps its own online-softmax state for the 16 query heads; S = Q K^T and
-//   O += P V are mma.sync m16n8k16 tiles fed by ldmatrix from the swizzled
-//   stages (bf16), or by ldmatrix plus in-register E4M3 -> f16 converts (FP8:
-//   keys and values are exact in f16; k_scale is folded into the logit scale
-//   and v_scale into the output).  Logits are kept in base 2.  The warps'
-//   states are combined in a fixed order.
+//   mbarrier (tile consumed), and the 16 query rows of each unit (4 KiB) by
+//   TMA.  A K stage goes back to the producer as soon as S has read it.
+// * Math.  On the tensor cores (tcgen05.mma, accumulators in TMEM), per page:
+//   S^T = K Q^T and O^T = V^T P^T, M = 128 (tokens, then dimensions), N = 16
+//   query heads; see the section before the kernel.  FP8 keys and values are
+//   widened to f16 in shared memory by four converter warps (exact), with
+//   k_scale folded into the logit scale and v_scale into the output.  Logits
+//   are kept in base 2.
 // * Every wait is bounded; a timeout sets MSA_ERR_TIMEOUT, raises a CTA abort
 //   flag that ends every other wait, and the producer waits (bounded) for its
 //   copies in flight before the CTA exits.
@@ -44,62 +42,8 @@
 namespace msa {
 namespace {
 
-constexpr int kConsumerWarps = 8;              // each owns kTPW tokens of every page
-constexpr int kConsumers = 32 * kConsumerWarps;
-constexpr int kTPW = kPage / kConsumerWarps;   // tokens per consumer warp
-constexpr int kNT = kTPW / 8;                  // S n-tiles (8 tokens) per warp
-constexpr int kKK = kTPW / 16;                 // P.V k-steps (16 tokens) per warp
-constexpr int kVPR = 64 / kConsumerWarps;      // accumulator values per lane per combine round
-static_assert(kTPW % 16 == 0, "a warp's tokens must fill whole m16n8k16 k-steps");
-constexpr int kDecThreads = kConsumers + 32; // + one producer warp
-constexpr int kQBufs = 2;                    // query-row buffers
 constexpr int kWin = 128;                    // task-table window (two windows resident)
-constexpr int kQBytes = kGroup * kDim * 2;
 constexpr int kMaxSmem = 232448;             // dynamic shared memory limit per CTA
-
-template <bool FP8, int STAGES>
-struct Cfg {
-    static constexpr int kTileBytes = FP8 ? 16384 : 32768;
-    static constexpr int kAhead = STAGES / 2;  // tasks the producer may run ahead
-    static constexpr int kRingBytes = kTileBytes * STAGES;
-    static_assert(STAGES % 2 == 0, "K and V of a task take two stages");
-    static_assert(kAhead < kWin, "the task table must cover the tasks in flight");
-};
-
-// Shared-memory layout of the decode CTA (offsets from a 1024-byte aligned
-// base); the host sizes the allocation with the same function.
-struct SmemLayout {
-    size_t ring, qbuf, bars, table, cbuf, comb, flags, qt, total;
-};
-
-__host__ __device__ constexpr size_t align_to(size_t v, size_t a)
-{
-    return (v + a - 1) / a * a;
-}
-
-__host__ __device__ inline SmemLayout decode_layout(int T, int stages, int tile_bytes)
-{
-    SmemLayout L{};
-    size_t off = 0;
-    L.ring = off;                                   // 1024-aligned: 128-byte swizzle atoms
-    off += (size_t)stages * tile_bytes;
-    L.qbuf = off = align_to(off, 128);             // bulk-copy destinations: 16-byte aligned
-    off += (size_t)kQBufs * kQBytes;
-    L.bars = off = align_to(off, 8);               // full[S], empty[S], qfull, qempty, consumer barrier
-    off += (size_t)(2 * stages + 2 * kQBufs + 1) * 8;
-    L.table = off = align_to(off, 16);             // int4 entries
-    off += (size_t)2 * kWin * 16;
-    L.cbuf = off = align_to(off, 16);              // [warps][kVPR][32] floats (8 KiB)
-    off += (size_t)kConsumerWarps * kVPR * 32 * 4;
-    L.comb = off = align_to(off, 16);              // comb_m[4][16], comb_l[4][16]
-    off += (size_t)2 * kConsumerWarps * kGroup * 4;
-    L.flags = off = align_to(off, 16);             // 4 ints
-    off += 16;
-    L.qt = off = align_to(off, 16);                // [T + 1] ints
-    off += (size_t)(T + 1) * 4;
-    L.total = align_to(off, 16) + 1024;            // + slack to align the base
-    return L;
-}
 
 struct Task {
     int t, g, i;
@@ -193,556 +137,8 @@ __device__ int4 make_entry(const DecodeParams &p, long long x, const int *qt)
 }
 
 // Output dimension of accumulator column `col` (0..7) of n-tile nt.
-template <bool FP8>
-__device__ __forceinline__ int o_dim(int nt, int col)
-{
-    // bf16: n-tile nt = dims 8nt..8nt+7.  FP8: virtual n-tile nt = (chunk C,
-    // parity) covers dims 16C + 2n + parity.
-    return FP8 ? (nt >> 1) * 16 + 2 * col + (nt & 1) : nt * 8 + col;
-}
-
-template <bool FP8, int STAGES>
-__global__ void __launch_bounds__(kDecThreads, 1)
-    sparse_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p)
-{
-    using C = Cfg<FP8, STAGES>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *base = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const SmemLayout lay = decode_layout(p.T, STAGES, C::kTileBytes);
-    uint8_t *ring = base + lay.ring;                                    // [S] tiles
-    uint8_t *qbuf = base + lay.qbuf;                                    // [kQBufs][16][128] bf16
-    uint64_t *full = reinterpret_cast<uint64_t *>(base + lay.bars);    // [S] tile landed
-    uint64_t *empty = full + STAGES;                                    // [S] tile consumed
-    uint64_t *qfull = empty + STAGES;                                   // [kQBufs]
-    uint64_t *qempty = qfull + kQBufs;                                  // [kQBufs]
-    uint64_t *csync_bar = qempty + kQBufs;                              // consumer barrier
-    int4 *table = reinterpret_cast<int4 *>(base + lay.table);          // [2][kWin]
-    float *cbuf = reinterpret_cast<float *>(base + lay.cbuf);          // [warps][kVPR][32]
-    float *comb_m = reinterpret_cast<float *>(base + lay.comb);        // [warps][16]
-    float *comb_l = comb_m + kConsumerWarps * kGroup;                   // [warps][16]
-    int *s_flag = reinterpret_cast<int *>(base + lay.flags);           // [0] last, [1] abort
-    int *qt = reinterpret_cast<int *>(base + lay.qt);                  // [T + 1]
-    volatile int *abort_flag = s_flag + 1;
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    // ---- prologue: everything that does not read the previous kernel's output ----
-    if (threadIdx.x == 0) {
-        prefetch_tensormap(&kv_map);
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&empty[s]), kConsumerWarps);
-        }
-        for (int s = 0; s < kQBufs; ++s) {
-            mbar_init(smem_u32(&qfull[s]), 1);
-            mbar_init(smem_u32(&qempty[s]), kConsumerWarps);
-        }
-        mbar_init(smem_u32(csync_bar), kConsumers);
-        s_flag[0] = 0;
-        s_flag[1] = 0;
-        fence_mbar_init();
-    }
-    build_token_prefix(p, qt);
-    __syncthreads();
-
-    const long long P = (long long)p.Hkv * qt[p.T];
-    const int G = gridDim.x, c = blockIdx.x;
-    const long long x_begin = (long long)c * P / G, x_end = (long long)(c + 1) * P / G;
-    const int ntasks = (int)(x_end - x_begin);
-
-    // `selected` comes from the previous kernel of the step
-    grid_dependency_wait();
-    if (ntasks == 0)
-        return;
-
-    auto entry = [&](int l) -> int4 { return table[((l / kWin) & 1) * kWin + (l % kWin)]; };
-
-    if (warp == kConsumerWarps) {
-        // =================== producer warp ===================
-        auto fill_window = [&](int w) {
-            const int l0 = w * kWin;
-            int4 *dst = table + (w & 1) * kWin;
-            for (int i = lane; i < kWin && l0 + i < ntasks; i += 32)
-                dst[i] = make_entry(p, x_begin + l0 + i, qt);
-            __syncwarp();
-        };
-        fill_window(0);
-        if (ntasks > kWin)
-            fill_window(1);
-        int issued = 0;        // tiles issued (lane 0)
-        int q_issued = 0;      // query-row copies issued (lane 0)
-        int prod_units = 0, prod_last = -1;
-        bool ok = true;
-        for (int l = 0; l < ntasks && ok; ++l) {
-            // K stage of task l: wait until the consumers released its previous tile
-            const int zk = 2 * l;
-            if (lane == 0 && zk >= STAGES)
-                ok = mbar_wait_or_abort(smem_u32(&empty[zk % STAGES]), ((zk / STAGES) - 1) & 1,
-                                        abort_flag);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok)
-                break;
-            // the consumers have read every entry up to task l - S/2: the window
-            // before this one can be replaced by the one after it
-            if (l % kWin == C::kAhead && l >= kWin && (l / kWin + 1) * kWin < ntasks)
-                fill_window(l / kWin + 1);
-            if (lane == 0) {
-                const int4 e = entry(l);
-                const int u = e.w * p.T + e.z;
-                if (u != prod_last) {
-                    prod_last = u;
-                    const int qb = prod_units % kQBufs;
-                    if (prod_units >= kQBufs)
-                        ok = mbar_wait_or_abort(smem_u32(&qempty[qb]),
-                                                ((prod_units / kQBufs) - 1) & 1, abort_flag);
-                    if (ok) {
-                        const uint32_t qbar = smem_u32(&qfull[qb]);
-                        mbar_arrive_expect_tx(qbar, kQBytes);
-                        bulk_load(smem_u32(qbuf + qb * kQBytes),
-                                  p.q + ((size_t)e.z * p.Hkv * kGroup + (size_t)e.w * kGroup) * kDim,
-                                  kQBytes, qbar);
-                        q_issued = prod_units + 1;
-                    }
-                    ++prod_units;
-                }
-                for (int kv = 0; kv < 2 && ok; ++kv) {
-                    const int z = zk + kv;
-                    const int st = z % STAGES;
-                    if (kv == 1 && z >= STAGES)
-                        ok = mbar_wait_or_abort(smem_u32(&empty[st]), ((z / STAGES) - 1) & 1,
-                                                abort_flag);
-                    if (!ok)
-                        break;
-                    const uint32_t bar = smem_u32(&full[st]);
-                    issued = z + 1;
-                    if (e.x < 0) {
-                        mbar_arrive(bar); // completes the phase with no data; consumers skip the task
-                        continue;
-                    }
-                    const uint32_t dst = smem_u32(ring + (size_t)st * C::kTileBytes);
-                    const int row = e.x + kv * p.Hkv * kPage;
-                    mbar_arrive_expect_tx(bar, C::kTileBytes);
-                    tma_load_2d(dst, &kv_map, 0, row, bar);
-                    if (!FP8)
-                        tma_load_2d(dst + 16384, &kv_map, 64, row, bar);
-                }
-            }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-        }
-        if (!ok && lane == 0) {
-            set_error(p.err, kErrTimeout);
-            *abort_flag = 1;
-            // Wait (bounded) for every copy this warp issued, so none lands in
-            // shared memory after the CTA has exited.
-            for (int z = issued - STAGES < 0 ? 0 : issued - STAGES; z < issued; ++z)
-                (void)mbar_wait_bounded(smem_u32(&full[z % STAGES]), (z / STAGES) & 1);
-            for (int u = q_issued - kQBufs < 0 ? 0 : q_issued - kQBufs; u < q_issued; ++u)
-                (void)mbar_wait_bounded(smem_u32(&qfull[u % kQBufs]), (u / kQBufs) & 1);
-        }
-        return;
-    }
-
-    // =================== consumer warps 0..3 ===================
-    const int g8 = lane >> 2, q4 = lane & 3;
-    float o[16][4];
-    float m_run[2], l_run[2];
-    uint32_t qa[8][4];
-    int cur_unit = -1, cons_units = 0, cur_t = 0, cur_g = 0;
-    int sync_phase = 0;
-    bool ok = true;
-    const int tb = warp * kTPW; // this warp's tokens within a page
-
-    // bounded barrier of the 128 consumer threads
-    auto csync = [&]() {
-        mbar_arrive(smem_u32(csync_bar));
-        if (!mbar_wait_or_abort(smem_u32(csync_bar), sync_phase & 1, abort_flag))
-            ok = false;
-        ++sync_phase;
-    };
-
-    auto reset_state = [&]() {
-#pragma unroll
-        for (int n = 0; n < 16; ++n)
-            o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-        m_run[0] = m_run[1] = -INFINITY;
-        l_run[0] = l_run[1] = 0.f;
-    };
-
-    // query fragments of the current unit from its shared-memory buffer
-    auto load_q = [&](int qb) {
-        const uint8_t *qs = qbuf + qb * kQBytes;
-#pragma unroll
-        for (int s = 0; s < 8; ++s) {
-            const uint8_t *r0 = qs + g8 * (kDim * 2);
-            const uint8_t *r1 = qs + (g8 + 8) * (kDim * 2);
-            if (!FP8) {
-                qa[s][0] = *reinterpret_cast<const uint32_t *>(r0 + (16 * s + 2 * q4) * 2);
-                qa[s][1] = *reinterpret_cast<const uint32_t *>(r1 + (16 * s + 2 * q4) * 2);
-                qa[s][2] = *reinterpret_cast<const uint32_t *>(r0 + (16 * s + 8 + 2 * q4) * 2);
-                qa[s][3] = *reinterpret_cast<const uint32_t *>(r1 + (16 * s + 8 + 2 * q4) * 2);
-            } else {
-                // permuted k order matching the FP8 key fragments: k-step s covers
-                // dims 16s + 4q4 .. +3 (slots 2q4,2q4+1 <- +0,+1; 2q4+8,+9 <- +2,+3)
-                const uint2 v0 = *reinterpret_cast<const uint2 *>(r0 + (16 * s + 4 * q4) * 2);
-                const uint2 v1 = *reinterpret_cast<const uint2 *>(r1 + (16 * s + 4 * q4) * 2);
-                qa[s][0] = bf16x2_to_f16x2(v0.x);
-                qa[s][1] = bf16x2_to_f16x2(v1.x);
-                qa[s][2] = bf16x2_to_f16x2(v0.y);
-                qa[s][3] = bf16x2_to_f16x2(v1.y);
-            }
-        }
-    };
-
-    // Combine the warps' states of unit (t, g); write its output, or its
-    // partial and, if this CTA is the last of the unit to arrive, the merge.
-    auto finalize = [&](int t, int g) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
-            l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
-        }
-        if (q4 == 0) {
-            comb_m[warp * kGroup + g8] = m_run[0];
-            comb_m[warp * kGroup + g8 + 8] = m_run[1];
-            comb_l[warp * kGroup + g8] = l_run[0];
-            comb_l[warp * kGroup + g8 + 8] = l_run[1];
-        }
-        csync();
-        // per row (g8, g8 + 8): combined max M, denominator L, this warp's factor
-        float M[2], L[2], fac[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int row = g8 + 8 * h;
-            M[h] = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w)
-                M[h] = fmaxf(M[h], comb_m[w * kGroup + row]);
-            L[h] = 0.f;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w)
-                L[h] += (M[h] == -INFINITY) ? 0.f
-                                            : comb_l[w * kGroup + row] * ex2(comb_m[w * kGroup + row] - M[h]);
-            fac[h] = (M[h] == -INFINITY) ? 0.f : ex2(m_run[h] - M[h]);
-        }
-        const long long Pt = qt[p.T];
-        const long long u_first = (long long)g * Pt + qt[t];
-        const int n_u = qt[t + 1] - qt[t];
-        const int c_first = owner_of(u_first, P, G);
-        const int c_last = owner_of(u_first + n_u - 1, P, G);
-        const int u = g * p.T + t;
-        const bool whole = c_first == c_last;
-        float *slot = p.partial + (size_t)(c + u) * kPartialFloats;
-        const size_t hbase = (size_t)t * p.Hkv * kGroup + (size_t)g * kGroup;
-        // Sum the warps' accumulators in kConsumerWarps rounds of kVPR values per
-        // lane through an 8 KiB buffer laid out [warp][value][lane] (conflict-free);
-        // warp rr sums round rr in warp order (fixed, so bitwise reproducible)
-        // and writes those dimensions.
-#pragma unroll
-        for (int rr = 0; rr < kConsumerWarps; ++rr) {
-#pragma unroll
-            for (int i = 0; i < kVPR; ++i) {
-                const int n = rr * (kVPR / 4) + (i >> 2), e = i & 3;
-                cbuf[(warp * kVPR + i) * 32 + lane] = o[n][e] * fac[e >> 1];
-            }
-            csync();
-            if (warp == rr) {
-#pragma unroll
-                for (int i = 0; i < kVPR; i += 2) {
-                    const int n = rr * (kVPR / 4) + (i >> 2), e = i & 3; // e in {0, 2}: cols 2q4, 2q4+1 of row e/2
-                    float v0 = 0.f, v1 = 0.f;
-#pragma unroll
-                    for (int w = 0; w < kConsumerWarps; ++w) {
-                        v0 += cbuf[(w * kVPR + i) * 32 + lane];
-                        v1 += cbuf[(w * kVPR + i + 1) * 32 + lane];
-                    }
-                    const int h = e >> 1, row = g8 + 8 * h;
-                    v0 *= p.v_scale;
-                    v1 *= p.v_scale;
-                    const int d0 = o_dim<FP8>(n, 2 * q4), d1 = o_dim<FP8>(n, 2 * q4 + 1);
-                    if (whole) {
-                        const float inv = L[h] > 0.f ? 1.f / L[h] : 0.f;
-                        const uint32_t pk = pack_bf16(v0 * inv, v1 * inv);
-                        uint16_t *orow = p.out + (hbase + row) * kDim;
-                        if (!FP8) {
-                            *reinterpret_cast<uint32_t *>(orow + d0) = pk; // d1 == d0 + 1
-                        } else {
-                            orow[d0] = (uint16_t)(pk & 0xFFFFu);
-                            orow[d1] = (uint16_t)(pk >> 16);
-                        }
-                    } else {
-                        float *srow = slot + row * kDim;
-                        if (!FP8) {
-                            *reinterpret_cast<float2 *>(srow + d0) = make_float2(v0, v1);
-                        } else {
-                            srow[d0] = v0;
-                            srow[d1] = v1;
-                        }
-                    }
-                }
-            }
-            csync();
-        }
-        if (warp == 0 && q4 == 0) {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int row = g8 + 8 * h;
-                if (whole) {
-                    p.lse[hbase + row] =
-                        (M[h] == -INFINITY) ? -INFINITY : (M[h] + log2f(L[h])) * 0.69314718055994531f;
-                } else {
-                    slot[kGroup * kDim + row] = M[h];
-                    slot[kGroup * kDim + kGroup + row] = L[h];
-                }
-            }
-        }
-        if (whole)
-            return;
-        __threadfence(); // publish this CTA's slot before counting in
-        csync();
-        if (threadIdx.x == 0) {
-            int arrivals = 0;
-            for (int cc = c_first; cc <= c_last; ++cc)
-                arrivals += !range_empty(cc, P, G);
-            const int before = atomicAdd(&p.counters[u], 1);
-            s_flag[0] = before == arrivals - 1;
-        }
-        csync();
-        if (s_flag[0]) {
-            __threadfence();
-            // merge every slot of the unit, in slot order; one reciprocal per row
-            const float *base = p.partial + (size_t)(c_first + u) * kPartialFloats;
-            const int nslots = c_last - c_first + 1;
-            for (int e = threadIdx.x; e < kGroup * kDim / 8; e += kConsumers) {
-                const int row = e >> 4, d0 = (e & 15) * 8;
-                float Mx = -INFINITY;
-                for (int s = 0; s < nslots; ++s)
-                    if (!range_empty(c_first + s, P, G))
-                        Mx = fmaxf(Mx, __ldcg(base + (size_t)s * kPartialFloats + kGroup * kDim + row));
-                float Lx = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                for (int s = 0; s < nslots; ++s) {
-                    if (range_empty(c_first + s, P, G))
-                        continue;
-                    const float *sl = base + (size_t)s * kPartialFloats;
-                    const float ms = __ldcg(sl + kGroup * kDim + row);
-                    const float wgt = (Mx == -INFINITY) ? 0.f : ex2(ms - Mx);
-                    Lx += wgt * __ldcg(sl + kGroup * kDim + kGroup + row);
-                    const float4 a = __ldcg(reinterpret_cast<const float4 *>(sl + row * kDim + d0));
-                    const float4 b = __ldcg(reinterpret_cast<const float4 *>(sl + row * kDim + d0 + 4));
-                    acc[0] += wgt * a.x; acc[1] += wgt * a.y; acc[2] += wgt * a.z; acc[3] += wgt * a.w;
-                    acc[4] += wgt * b.x; acc[5] += wgt * b.y; acc[6] += wgt * b.z; acc[7] += wgt * b.w;
-                }
-                const float inv = Lx > 0.f ? 1.f / Lx : 0.f;
-                uint4 packed;
-                packed.x = pack_bf16(acc[0] * inv, acc[1] * inv);
-                packed.y = pack_bf16(acc[2] * inv, acc[3] * inv);
-                packed.z = pack_bf16(acc[4] * inv, acc[5] * inv);
-                packed.w = pack_bf16(acc[6] * inv, acc[7] * inv);
-                *reinterpret_cast<uint4 *>(p.out + (hbase + row) * kDim + d0) = packed;
-                if (d0 == 0)
-                    p.lse[hbase + row] =
-                        (Mx == -INFINITY) ? -INFINITY : (Mx + log2f(Lx)) * 0.69314718055994531f;
-            }
-            if (threadIdx.x == 0)
-                p.counters[u] = 0; // ready for the next call
-        }
-        csync(); // s_flag and cbuf are reused by the next unit
-    };
-
-    for (int l = 0; l < ntasks && ok; ++l) {
-        const int zk = 2 * l, zv = 2 * l + 1;
-        const int sk = zk % STAGES, sv = zv % STAGES;
-        if (!mbar_wait_or_abort(smem_u32(&full[sk]), (zk / STAGES) & 1, abort_flag)) {
-            ok = false;
-            break;
-        }
-        const int4 e = entry(l); // written before the producer armed full[sk]
-        const int u = e.w * p.T + e.z;
-        if (u != cur_unit) {
-            if (cur_unit >= 0) {
-                finalize(cur_t, cur_g);
-                if (!ok)
-                    break;
-            }
-            cur_unit = u;
-            cur_t = e.z;
-            cur_g = e.w;
-            reset_state();
-            const int qb = cons_units % kQBufs;
-            if (!mbar_wait_or_abort(smem_u32(&qfull[qb]), (cons_units / kQBufs) & 1, abort_flag)) {
-                ok = false;
-                break;
-            }
-            load_q(qb);
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(smem_u32(&qempty[qb]));
-            ++cons_units;
-        }
-        const int nvis = e.y; // visible tokens of this page
-        const uint32_t tileK = smem_u32(ring + (size_t)sk * C::kTileBytes);
-        const uint32_t tileV = smem_u32(ring + (size_t)sv * C::kTileBytes);
-        const bool live = e.x >= 0;
-
-        // ---- S = Q K^T over this warp's kTPW tokens: kNT n-tiles of 8 tokens ----
-        float s[kNT][4];
-#pragma unroll
-        for (int n = 0; n < kNT; ++n)
-            s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
-        if (live) {
-            if (!FP8) {
-#pragma unroll
-                for (int n2 = 0; n2 < kNT / 2; ++n2) {
-                    const int mi = lane >> 3;
-                    const int tok = tb + 16 * n2 + ((mi >> 1) << 3) + (lane & 7);
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const int chunk = 2 * ks + (mi & 1);
-                        const uint32_t addr = tileK + (chunk >> 3) * 16384 + tok * 128 +
-                                              (((chunk & 7) ^ (tok & 7)) << 4);
-                        uint32_t b[4];
-                        ldsm_x4(b, addr);
-                        mma_bf16(s[2 * n2], qa[ks], b[0], b[1]);
-                        mma_bf16(s[2 * n2 + 1], qa[ks], b[2], b[3]);
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int n2 = 0; n2 < kNT / 2; ++n2) {
-                    const int mi = lane >> 3;
-                    const int tok = tb + 16 * n2 + ((mi & 1) << 3) + (lane & 7);
-#pragma unroll
-                    for (int ks = 0; ks < 8; ks += 2) {
-                        const int chunk = ks + (mi >> 1);
-                        const uint32_t addr = tileK + tok * 128 + ((chunk ^ (tok & 7)) << 4);
-                        uint32_t b[4];
-                        ldsm_x4(b, addr);
-                        // b[0]: (n-tile 2n2, k-step ks), b[1]: (2n2+1, ks), b[2]: (2n2, ks+1), b[3]: (2n2+1, ks+1)
-                        mma_f16(s[2 * n2], qa[ks], e4m3x2_to_f16x2(b[0] & 0xFFFFu),
-                                e4m3x2_to_f16x2(b[0] >> 16));
-                        mma_f16(s[2 * n2 + 1], qa[ks], e4m3x2_to_f16x2(b[1] & 0xFFFFu),
-                                e4m3x2_to_f16x2(b[1] >> 16));
-                        mma_f16(s[2 * n2], qa[ks + 1], e4m3x2_to_f16x2(b[2] & 0xFFFFu),
-                                e4m3x2_to_f16x2(b[2] >> 16));
-                        mma_f16(s[2 * n2 + 1], qa[ks + 1], e4m3x2_to_f16x2(b[3] & 0xFFFFu),
-                                e4m3x2_to_f16x2(b[3] >> 16));
-                    }
-                }
-            }
-        }
-        // the K tile is no longer read: hand its stage back to the producer
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(smem_u32(&empty[sk]));
-
-        uint32_t pa[kKK][4];
-        if (live) {
-            // ---- scale, causal mask, online softmax (base 2) ----
-            const bool need_mask = tb + kTPW > nvis;
-            float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-            for (int n = 0; n < kNT; ++n) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    float v = s[n][k] * p.scale_log2;
-                    if (need_mask && tb + 8 * n + 2 * q4 + (k & 1) >= nvis)
-                        v = -INFINITY;
-                    s[n][k] = v;
-                    mx[k >> 1] = fmaxf(mx[k >> 1], v);
-                }
-            }
-            float ref[2], alpha[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
-                mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-                const float m_new = fmaxf(m_run[h], mx[h]);
-                ref[h] = (m_new == -INFINITY) ? 0.f : m_new;
-                alpha[h] = ex2(m_run[h] - ref[h]); // 0 when m_run is -inf
-                m_run[h] = m_new;
-                l_run[h] *= alpha[h];
-            }
-#pragma unroll
-            for (int n = 0; n < 16; ++n) {
-                o[n][0] *= alpha[0];
-                o[n][1] *= alpha[0];
-                o[n][2] *= alpha[1];
-                o[n][3] *= alpha[1];
-            }
-#pragma unroll
-            for (int n = 0; n < kNT; ++n) {
-                const float p0 = ex2(s[n][0] - ref[0]), p1 = ex2(s[n][1] - ref[0]);
-                const float p2 = ex2(s[n][2] - ref[1]), p3 = ex2(s[n][3] - ref[1]);
-                l_run[0] += p0 + p1;
-                l_run[1] += p2 + p3;
-                // A fragment of P for k-step n/2: n-tile 2kk -> regs 0,1; 2kk+1 -> regs 2,3
-                const int kk = n >> 1, hi = (n & 1) * 2;
-                pa[kk][hi + 0] = FP8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
-                pa[kk][hi + 1] = FP8 ? pack_f16(p2, p3) : pack_bf16(p2, p3);
-            }
-        }
-
-        if (!mbar_wait_or_abort(smem_u32(&full[sv]), (zv / STAGES) & 1, abort_flag)) {
-            ok = false;
-            break;
-        }
-        if (live) {
-            // ---- O += P V over this warp's kTPW tokens ----
-            if (!FP8) {
-#pragma unroll
-                for (int kk = 0; kk < kKK; ++kk) {
-                    const int mi = lane >> 3;
-                    const int tok = tb + 16 * kk + ((mi & 1) << 3) + (lane & 7);
-#pragma unroll
-                    for (int nd2 = 0; nd2 < 8; ++nd2) {
-                        const int chunk = 2 * nd2 + (mi >> 1);
-                        const uint32_t addr = tileV + (chunk >> 3) * 16384 + tok * 128 +
-                                              (((chunk & 7) ^ (tok & 7)) << 4);
-                        uint32_t b[4];
-                        ldsm_x4_t(b, addr);
-                        mma_bf16(o[2 * nd2], pa[kk], b[0], b[1]);
-                        mma_bf16(o[2 * nd2 + 1], pa[kk], b[2], b[3]);
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int kk = 0; kk < kKK; ++kk) {
-                    const int mi = lane >> 3;
-                    const int tok = tb + 16 * kk + ((mi & 1) << 3) + (lane & 7);
-#pragma unroll
-                    for (int C2 = 0; C2 < 8; C2 += 2) {
-                        const int chunk = C2 + (mi >> 1);
-                        const uint32_t addr = tileV + tok * 128 + ((chunk ^ (tok & 7)) << 4);
-                        uint32_t b[4];
-                        ldsm_x4_t(b, addr);
-                        // b[0]: tokens 0-7 of the k-step, chunk C2; b[1]: tokens 8-15, C2;
-                        // b[2], b[3]: chunk C2+1.  Bytes: {V[2q][2g], V[2q][2g+1], V[2q+1][2g], V[2q+1][2g+1]}
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const uint32_t lo = __byte_perm(b[2 * h], 0, 0x3120);
-                            const uint32_t hi = __byte_perm(b[2 * h + 1], 0, 0x3120);
-                            const int vn = 2 * (C2 + h); // even-dim virtual n-tile of chunk C2+h
-                            mma_f16(o[vn], pa[kk], e4m3x2_to_f16x2(lo & 0xFFFFu), e4m3x2_to_f16x2(hi & 0xFFFFu));
-                            mma_f16(o[vn + 1], pa[kk], e4m3x2_to_f16x2(lo >> 16), e4m3x2_to_f16x2(hi >> 16));
-                        }
-                    }
-                }
-            }
-        }
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(smem_u32(&empty[sv]));
-    }
-    if (ok && cur_unit >= 0)
-        finalize(cur_t, cur_g);
-    if (!ok) {
-        set_error(p.err, kErrTimeout);
-        *abort_flag = 1;
-    }
-}
-
 // ===========================================================================
-// bf16 KV: tcgen05 UMMA with TMEM accumulators
+// tcgen05 UMMA with TMEM accumulators
 // ===========================================================================
 //
 // Per page (task) of unit (t, g):
@@ -754,8 +150,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 // 128-byte swizzle; the V tile, as loaded, is the MN-major form of V^T; P^T is
 // written by the softmax warps in the K-major 128-byte-swizzled form.
 // Warps: 0 = TMA producer + task table, 1 = MMA issuer + TMEM owner,
-// 2..5 = softmax (thread = one TMEM lane: a token for S^T, a dimension for
-// O^T).  The softmax warps exchange per-head page maxima through shared memory,
+// 2..9 = softmax (thread = one TMEM lane: a token for S^T, a dimension for
+// O^T; two warps per lane quarter, 8 heads each), 10..13 = FP8 converters.  The softmax warps exchange per-head page maxima through shared memory,
 // keep the running max / denominator per head, and fold each page's O^T into
 // 16 registers (one per head) once the next page's P^T is written.
 
@@ -782,17 +178,17 @@ __host__ __device__ inline USmem umma_layout(int T, int stages, bool fp8)
     size_t off = 0;
     L.ring = off;                          // 1024-aligned tiles
     off += (size_t)stages * (fp8 ? kUTile / 2 : kUTile);
-    L.stage = off = align_to(off, 1024);   // FP8: K and V f16 tiles
-    off += fp8 ? 2 * kUTile : 0;
+    L.stage = off = align_to(off, 1024);   // FP8: f16 tiles K[2], V
+    off += fp8 ? 3 * kUTile : 0;
     L.qbuf = off = align_to(off, 1024);    // [2] query tiles (swizzle atoms: 1024-aligned)
     off += 2 * kUQTile;
     L.pbuf = off = align_to(off, 1024);    // [2] P^T tiles
     off += 2 * kUPTile;
     // full[S], empty[S], qfull[2], qempty[2], s_full[2], s_free[2], p_full[2],
     // p_free[2], o_full[2], o_free[2], softmax sync, done, then FP8 only:
-    // kst_full, kst_empty, vst_full, vst_empty, qconv[2]
+    // kst_full[2], kst_empty[2], vst_full, vst_empty, qconv[2]
     L.bars = off = align_to(off, 8);
-    off += (size_t)(2 * stages + 16 + 2 + 6) * 8;
+    off += (size_t)(2 * stages + 16 + 2 + 8) * 8;
     L.table = off = align_to(off, 16);     // [2][kWin] int4
     off += (size_t)2 * kWin * 16;
     L.xbuf = off = align_to(off, 16);      // [2][4 quarters][16] page maxima
@@ -832,8 +228,8 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const USmem lay = umma_layout(p.T, STAGES, FP8);
     uint8_t *ring = base + lay.ring;
-    uint8_t *kst = base + lay.stage;        // FP8: f16 K tile
-    uint8_t *vst = kst + kUTile;            // FP8: f16 V tile
+    uint8_t *kst = base + lay.stage;        // FP8: [2] f16 K tiles
+    uint8_t *vst = kst + 2 * kUTile;        // FP8: f16 V tile
     uint8_t *qbuf = base + lay.qbuf;
     uint8_t *pbuf = base + lay.pbuf;
     uint64_t *full = reinterpret_cast<uint64_t *>(base + lay.bars);
@@ -848,9 +244,9 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
     uint64_t *o_free = o_full + 2;
     uint64_t *smx_bar = o_free + 2;    // softmax-warps barrier (kUSoftmax arrivals)
     uint64_t *done_bar = smx_bar + 1;  // softmax warps finished with TMEM (kUSmxWarps arrivals)
-    uint64_t *kst_full = done_bar + 1; // FP8: staging K converted (kUCvtWarps)
-    uint64_t *kst_empty = kst_full + 1; // FP8: staging K read by the MMA (commit)
-    uint64_t *vst_full = kst_empty + 1;
+    uint64_t *kst_full = done_bar + 1; // FP8: [2] staging K converted (kUCvtWarps)
+    uint64_t *kst_empty = kst_full + 2; // FP8: [2] staging K read by the MMA (commit)
+    uint64_t *vst_full = kst_empty + 2;
     uint64_t *vst_empty = vst_full + 1;
     uint64_t *qconv = vst_empty + 1;   // FP8: [2] query tile widened to f16 (kUCvtWarps)
     int4 *table = reinterpret_cast<int4 *>(base + lay.table);
@@ -870,8 +266,10 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), FP8 ? kUCvtWarps : 1);
         }
-        mbar_init(smem_u32(kst_full), kUCvtWarps);
-        mbar_init(smem_u32(kst_empty), 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&kst_full[b]), kUCvtWarps);
+            mbar_init(smem_u32(&kst_empty[b]), 1);
+        }
         mbar_init(smem_u32(vst_full), kUCvtWarps);
         mbar_init(smem_u32(vst_empty), 1);
         for (int b = 0; b < 2; ++b) {
@@ -938,10 +336,11 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
             if (!ok)
                 break;
             // The softmax warps trail the MMA warp by up to two tasks and the MMA
-            // warp trails this one by up to kAhead (kAhead + 1 with the FP8
-            // converters between them): only kAhead + 3 (+ 1) tasks into a
-            // window has every reader left the window before it.
-            if (l % kWin == kAhead + 3 + (FP8 ? 1 : 0) && l >= kWin && (l / kWin + 1) * kWin < ntasks)
+            // warp trails this one by up to kAhead (kAhead + 2 with the FP8
+            // converters, which run a K tile ahead of the V tile, between
+            // them): only kAhead + 3 (+ 2) tasks into a window has every
+            // reader left the window before it.
+            if (l % kWin == kAhead + 3 + (FP8 ? 2 : 0) && l >= kWin && (l / kWin + 1) * kWin < ntasks)
                 fill_window(l / kWin + 1);
             if (lane == 0) {
                 const int4 e = entry(l);
@@ -1013,7 +412,7 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
                 const int zk = 2 * l, b = l & 1;
                 if (!FP8 && !mbar_wait_or_abort(smem_u32(&full[zk % STAGES]), (zk / STAGES) & 1, abort_flag))
                     return false;
-                if (FP8 && !mbar_wait_or_abort(smem_u32(kst_full), l & 1, abort_flag))
+                if (FP8 && !mbar_wait_or_abort(smem_u32(&kst_full[b]), (l >> 1) & 1, abort_flag))
                     return false;
                 const int4 e = entry(l);
                 const int u = unit_of(e);
@@ -1029,7 +428,7 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
                     return false;
                 tcgen05_after_sync();
                 if (e.x >= 0) {
-                    const uint32_t tileK = FP8 ? smem_u32(kst) : smem_u32(ring + (size_t)(zk % STAGES) * kRaw);
+                    const uint32_t tileK = FP8 ? smem_u32(kst + b * kUTile) : smem_u32(ring + (size_t)(zk % STAGES) * kRaw);
                     const uint32_t qtile = smem_u32(qbuf + qb * kUQTile);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
@@ -1039,7 +438,7 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
                     }
                 }
                 umma_commit(smem_u32(&s_full[b]));
-                umma_commit(FP8 ? smem_u32(kst_empty) : smem_u32(&empty[zk % STAGES])); // K tile read
+                umma_commit(FP8 ? smem_u32(&kst_empty[b]) : smem_u32(&empty[zk % STAGES])); // K tile read
                 // last task of its unit: the query tile can be replaced
                 if (l + 1 == ntasks || unit_of(entry(l + 1)) != u)
                     umma_commit(smem_u32(&qempty[qb]));
@@ -1105,39 +504,42 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
         const int ct = threadIdx.x - 32 * (2 + kUSmxWarps); // 0..127
         bool ok = true;
         int units = 0, cur = -1;
+        // Thread ct widens the 16-byte chunk c = ct % 8 (16 dims) of rows
+        // ct / 8 + 16 i, i < 8: all eight loads are issued before the first
+        // convert, so the converts of different rows overlap.
+        const int cch = ct & 7, r0 = ct >> 3, sw = r0 & 7; // r & 7 == sw for every row of the thread
         auto convert = [&](const uint8_t *raw, uint8_t *dst) {
-#pragma unroll 2
-            for (int item = ct; item < kPage * 8; item += 32 * kUCvtWarps) {
-                const int r = item >> 3, c = item & 7; // row, 16-byte chunk of 16 E4M3 dims
-                const uint4 w = *reinterpret_cast<const uint4 *>(raw + r * 128 + ((c ^ (r & 7)) << 4));
+            uint4 w[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                w[i] = *reinterpret_cast<const uint4 *>(raw + (r0 + 16 * i) * 128 + ((cch ^ sw) << 4));
+            const int c0 = 2 * (cch & 3); // first f16 chunk in the 64-dim box cch / 4
+            uint8_t *col_lo = dst + (cch >> 2) * (kUTile / 2) + ((c0 ^ sw) << 4);
+            uint8_t *col_hi = dst + (cch >> 2) * (kUTile / 2) + (((c0 + 1) ^ sw) << 4);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
                 uint4 lo, hi;
-                lo.x = e4m3x2_to_f16x2(w.x & 0xFFFFu);
-                lo.y = e4m3x2_to_f16x2(w.x >> 16);
-                lo.z = e4m3x2_to_f16x2(w.y & 0xFFFFu);
-                lo.w = e4m3x2_to_f16x2(w.y >> 16);
-                hi.x = e4m3x2_to_f16x2(w.z & 0xFFFFu);
-                hi.y = e4m3x2_to_f16x2(w.z >> 16);
-                hi.z = e4m3x2_to_f16x2(w.w & 0xFFFFu);
-                hi.w = e4m3x2_to_f16x2(w.w >> 16);
-                const int h = c >> 2, c0 = 2 * (c & 3);  // box (64 dims), first 8-dim chunk
-                uint8_t *row = dst + h * (kUTile / 2) + r * 128;
-                *reinterpret_cast<uint4 *>(row + ((c0 ^ (r & 7)) << 4)) = lo;
-                *reinterpret_cast<uint4 *>(row + (((c0 + 1) ^ (r & 7)) << 4)) = hi;
+                e4m3x4_to_f16x2x2(w[i].x, lo.x, lo.y);
+                e4m3x4_to_f16x2x2(w[i].y, lo.z, lo.w);
+                e4m3x4_to_f16x2x2(w[i].z, hi.x, hi.y);
+                e4m3x4_to_f16x2x2(w[i].w, hi.z, hi.w);
+                *reinterpret_cast<uint4 *>(col_lo + (r0 + 16 * i) * 128) = lo;
+                *reinterpret_cast<uint4 *>(col_hi + (r0 + 16 * i) * 128) = hi;
             }
             fence_async_smem();
         };
-        for (int l = 0; l < ntasks && ok; ++l) {
-            const int zk = 2 * l, zv = zk + 1;
-            ok = mbar_wait_or_abort(smem_u32(&full[zk % STAGES]), (zk / STAGES) & 1, abort_flag);
-            if (!ok)
-                break;
+        // K(l + 1) is widened before V(l): the MMA warp issues S(l + 1)
+        // before O(l), and K has two staging tiles, V one.
+        auto do_k = [&](int l) -> bool {
+            const int zk = 2 * l, kb = l & 1;
+            if (!mbar_wait_or_abort(smem_u32(&full[zk % STAGES]), (zk / STAGES) & 1, abort_flag))
+                return false;
             const int4 e = entry(l);
             const int u = unit_of(e);
             if (u != cur) {
                 const int qb = units & 1;
-                ok = mbar_wait_or_abort(smem_u32(&qfull[qb]), (units >> 1) & 1, abort_flag);
-                if (!ok)
-                    break;
+                if (!mbar_wait_or_abort(smem_u32(&qfull[qb]), (units >> 1) & 1, abort_flag))
+                    return false;
                 uint8_t *q = qbuf + qb * kUQTile;
                 for (int i = ct; i < kUQTile / 16; i += 32 * kUCvtWarps) {
                     uint4 v = reinterpret_cast<uint4 *>(q)[i];
@@ -1154,29 +556,39 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
                 cur = u;
                 ++units;
             }
-            if (l >= 1)
-                ok = mbar_wait_or_abort(smem_u32(kst_empty), (l - 1) & 1, abort_flag);
-            if (!ok)
-                break;
+            if (l >= 2 && !mbar_wait_or_abort(smem_u32(&kst_empty[kb]), ((l >> 1) - 1) & 1, abort_flag))
+                return false;
             if (e.x >= 0)
-                convert(ring + (size_t)(zk % STAGES) * kRaw, kst);
+                convert(ring + (size_t)(zk % STAGES) * kRaw, kst + kb * kUTile);
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(smem_u32(kst_full));
+                mbar_arrive(smem_u32(&kst_full[kb]));
                 mbar_arrive(smem_u32(&empty[zk % STAGES]));
             }
-            ok = mbar_wait_or_abort(smem_u32(&full[zv % STAGES]), (zv / STAGES) & 1, abort_flag);
-            if (ok && l >= 1)
-                ok = mbar_wait_or_abort(smem_u32(vst_empty), (l - 1) & 1, abort_flag);
-            if (!ok)
-                break;
-            if (e.x >= 0)
+            return true;
+        };
+        auto do_v = [&](int l) -> bool {
+            const int zv = 2 * l + 1;
+            if (!mbar_wait_or_abort(smem_u32(&full[zv % STAGES]), (zv / STAGES) & 1, abort_flag))
+                return false;
+            if (l >= 1 && !mbar_wait_or_abort(smem_u32(vst_empty), (l - 1) & 1, abort_flag))
+                return false;
+            if (entry(l).x >= 0)
                 convert(ring + (size_t)(zv % STAGES) * kRaw, vst);
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(smem_u32(vst_full));
                 mbar_arrive(smem_u32(&empty[zv % STAGES]));
             }
+            return true;
+        };
+        if (ntasks > 0)
+            ok = do_k(0);
+        for (int l = 0; l < ntasks && ok; ++l) {
+            if (l + 1 < ntasks)
+                ok = do_k(l + 1);
+            if (ok)
+                ok = do_v(l);
         }
         if (!ok) {
             set_error(p.err, kErrTimeout);
@@ -1293,18 +705,19 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
             slot[kGroup * kDim + h0 + idx] = Mi;
             slot[kGroup * kDim + kGroup + h0 + idx] = Li;
         }
-        __threadfence(); // publish this CTA's slot before counting in
+        // The CTA barrier orders every thread's slot writes before thread 0's
+        // release; its acquire makes the other CTAs' slots visible to the
+        // CTA that arrives last, and the barrier after it to all its threads.
         ssync();
         if (sidx == 0) {
             int arrivals = 0;
             for (int cc = c_first; cc <= c_last; ++cc)
                 arrivals += !range_empty(cc, P, G);
-            const int before = atomicAdd(&p.counters[u], 1);
+            const int before = atom_add_acq_rel_gpu(&p.counters[u], 1);
             s_flag[0] = before == arrivals - 1;
         }
         ssync();
         if (s_flag[0]) {
-            __threadfence();
             const float *sbase = p.partial + (size_t)(c_first + u) * kPartialFloats;
             const int nslots = c_last - c_first + 1;
             const size_t obase = (size_t)t * p.Hkv * kGroup + (size_t)g * kGroup;
@@ -1507,39 +920,6 @@ bool encode_kv_map(CUtensorMap *map, const void *kv_pool, int kv_dtype, int num_
     return r == CUDA_SUCCESS;
 }
 
-template <bool FP8, int STAGES>
-size_t decode_smem_bytes(int T)
-{
-    return decode_layout(T, STAGES, Cfg<FP8, STAGES>::kTileBytes).total;
-}
-
-template <bool FP8, int STAGES>
-cudaError_t launch_decode_t(const DecodeParams &p, const CUtensorMap &map, int ctas,
-                            cudaStream_t stream, bool pdl)
-{
-    const size_t smem = decode_smem_bytes<FP8, STAGES>(p.T);
-    cudaError_t e = cudaFuncSetAttribute(sparse_decode_kernel<FP8, STAGES>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess)
-        return e;
-    e = launch_kernel(sparse_decode_kernel<FP8, STAGES>, dim3(ctas), dim3(kDecThreads), smem,
-                      stream, pdl, map, p);
-    if (e != cudaSuccess)
-        return e;
-    return cudaGetLastError();
-}
-
-// The deepest ring that fits next to the token prefix (T + 1 ints).
-template <bool FP8>
-cudaError_t launch_decode_fit(const DecodeParams &p, const CUtensorMap &map, int ctas,
-                              cudaStream_t stream, bool pdl)
-{
-    constexpr int kDeep = FP8 ? 12 : 6, kShallow = FP8 ? 8 : 4;
-    if (decode_smem_bytes<FP8, kDeep>(p.T) <= (size_t)kMaxSmem)
-        return launch_decode_t<FP8, kDeep>(p, map, ctas, stream, pdl);
-    return launch_decode_t<FP8, kShallow>(p, map, ctas, stream, pdl);
-}
-
 // Query rows [T * Hq][128] bf16, boxes of 64 dims x 16 rows, 128-byte swizzle.
 bool encode_q_map(CUtensorMap *map, const void *q, int T, int Hkv)
 {
@@ -1573,6 +953,21 @@ cudaError_t launch_umma_t(const DecodeParams &p, const CUtensorMap &kv, const CU
 
 } // namespace
 
+bool encode_2d_sw128(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, uint64_t inner,
+                     uint64_t rows, uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows)
+{
+    EncodeFn enc = get_encode();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, dtype, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_sparse_decode(const DecodeParams &p, const void *kv_pool, int kv_dtype, int ctas,
                                  cudaStream_t stream, bool pdl)
 {
@@ -1583,8 +978,8 @@ cudaError_t launch_sparse_decode(const DecodeParams &p, const void *kv_pool, int
     if (!encode_q_map(&qmap, p.q, p.T, p.Hkv))
         return cudaErrorInvalidValue;
     if (kv_dtype == MSA_FP8_E4M3) {
-        if (umma_layout(p.T, 8, true).total <= (size_t)kMaxSmem)
-            return launch_umma_t<true, 8>(p, map, qmap, ctas, stream, pdl);
+        if (umma_layout(p.T, 6, true).total <= (size_t)kMaxSmem)
+            return launch_umma_t<true, 6>(p, map, qmap, ctas, stream, pdl);
         return launch_umma_t<true, 4>(p, map, qmap, ctas, stream, pdl);
     }
     if (umma_layout(p.T, 6, false).total <= (size_t)kMaxSmem)

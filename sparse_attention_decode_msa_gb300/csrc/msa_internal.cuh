@@ -92,6 +92,17 @@ cudaError_t launch_select(const SelectParams &p, cudaStream_t stream, bool pdl);
 cudaError_t launch_sparse_decode(const DecodeParams &p, const void *kv_pool, int kv_dtype,
                                  int ctas, cudaStream_t stream, bool pdl);
 
+__host__ __device__ constexpr size_t align_to(size_t v, size_t a)
+{
+    return (v + a - 1) / a * a;
+}
+
+// Tensor map of a row-major 2-D array [rows][inner] (row pitch `row_bytes`)
+// loaded in boxes of box_inner x box_rows with the 128-byte swizzle; false if
+// the driver's encoder is unavailable or rejects the map.
+bool encode_2d_sw128(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, uint64_t inner,
+                     uint64_t rows, uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows);
+
 // cudaLaunchKernelEx with an optional programmatic-stream-serialization attribute.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
@@ -148,15 +159,22 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// Longest time a waiting thread stays suspended in one try_wait (ns): the
+// thread resumes as soon as the phase completes, and suspended threads take
+// no issue slots from the warps that do the work.
+constexpr uint32_t kWaitSuspendNs = 1u << 20;
+
+// Test for the completion of phase `parity`, suspending the thread for up to
+// kWaitSuspendNs while it is incomplete.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile(
         "{\n .reg .pred p;\n"
-        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
         " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(kWaitSuspendNs)
         : "memory");
     return ok != 0;
 }
@@ -188,6 +206,14 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity
             return false;
     }
     return true;
+}
+
+// atomicAdd with acquire-release semantics at GPU scope; returns the old value.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int *addr, int v)
+{
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+    return old;
 }
 
 // ---- programmatic dependent launch ----------------------------------------
@@ -371,7 +397,7 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
 __device__ __forceinline__ float warp_max_f32(float x)
 {
     float r;
-    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+    asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
     return r;
 }
 
@@ -385,6 +411,16 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes)
         : "=r"(out)
         : "r"(two_codes));
     return out;
+}
+
+// Four E4M3 codes (bytes 0..3 of w) to two f16x2 words: lo = bytes 0, 1 and
+// hi = bytes 2, 3 (lower byte in the lower half).  Exact.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t &lo, uint32_t &hi)
+{
+    asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n cvt.rn.f16x2.e4m3x2 %0, a;\n"
+        " cvt.rn.f16x2.e4m3x2 %1, b;\n}\n"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
 }
 
 // Two E2M1 codes in one byte (low nibble -> low half) to f16x2.  Exact.

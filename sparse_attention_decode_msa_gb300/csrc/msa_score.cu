@@ -251,6 +251,356 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(const ScoreP
     }
 }
 
+// ---------------------------------------------------------------------------
+// tcgen05 scorer (bf16 index keys, many query tokens per request).  The pages
+// of the call, (request, block) in request-major order, are split into one
+// contiguous range per persistent CTA.  Per page: the producer warp brings
+// the 128 x 128 index-key tile into a shared-memory ring (TMA, 128-byte
+// swizzle); the MMA warp computes S = K_idx Q_idx^T for the request's query
+// tokens (M = 128 page tokens, N = q_per_req rounded up to 16) into one of
+// kSAcc TMEM accumulators; four epilogue warps read the 128 x N scores (one
+// token per TMEM lane), apply the causal limit and reduce each column to its
+// maximum (redux.sync.max.f32, then across the four warps).  Integer-valued
+// inputs make every product and partial sum exact in fp32, as in the
+// mma.sync path.
+constexpr int kSTile = kPage * kDim * 2; // bf16 tile
+constexpr int kSAcc = 4;                 // TMEM accumulators (pages whose scores are in flight)
+constexpr int kSThreads = 32 * 6;        // producer, MMA, 4 epilogue warps
+constexpr int kSMaxSmem = 232448;
+
+struct SLayout {
+    size_t ring, qbuf, bars, red, prefix, misc, total;
+};
+
+__host__ __device__ inline SLayout score_layout(int npad, int stages, int R)
+{
+    SLayout L{};
+    size_t off = 0;
+    L.ring = off; // 1024-aligned (swizzle atoms)
+    off += (size_t)stages * kSTile;
+    L.qbuf = off = align_to(off, 1024); // [2] query tiles of npad rows
+    off += 2 * (size_t)npad * kDim * 2;
+    // full[S], empty[S], qfull[2], qempty[2], acc_full[kSAcc], acc_empty[kSAcc], esync, done
+    L.bars = off = align_to(off, 8);
+    off += (size_t)(2 * stages + 4 + 2 * kSAcc + 2) * 8;
+    L.red = off = align_to(off, 16); // [2][4][npad] column maxima of the epilogue warps
+    off += 2 * 4 * (size_t)npad * 4;
+    L.prefix = off = align_to(off, 16); // [R + 1] pages before request r
+    off += (size_t)(R + 1) * 4;
+    L.misc = off = align_to(off, 16); // TMEM base, abort flag
+    off += 16;
+    L.total = off + 1024; // slack for aligning the dynamic base
+    return L;
+}
+
+template <int NPAD>
+constexpr uint32_t score_tmem_cols()
+{
+    return kSAcc * NPAD <= 32 ? 32 : kSAcc * NPAD <= 64 ? 64 : kSAcc * NPAD <= 128 ? 128
+           : kSAcc * NPAD <= 256 ? 256 : 512;
+}
+
+template <int NPAD, int STAGES>
+__global__ void __launch_bounds__(kSThreads, 1)
+    index_score_umma_kernel(const __grid_constant__ CUtensorMap k_map,
+                            const __grid_constant__ CUtensorMap q_map, const ScoreParams p)
+{
+    static_assert(NPAD % 16 == 0 && NPAD >= 16 && NPAD <= 64, "N of the MMA");
+    constexpr int kQTile = NPAD * kDim * 2;
+    constexpr uint32_t kCols = score_tmem_cols<NPAD>();
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const SLayout lay = score_layout(NPAD, STAGES, p.R);
+    uint8_t *ring = base + lay.ring;
+    uint8_t *qbuf = base + lay.qbuf;
+    uint64_t *full = reinterpret_cast<uint64_t *>(base + lay.bars);
+    uint64_t *empty = full + STAGES;
+    uint64_t *qfull = empty + STAGES;
+    uint64_t *qempty = qfull + 2;
+    uint64_t *acc_full = qempty + 2;        // [kSAcc] scores of a page in TMEM (MMA commit)
+    uint64_t *acc_empty = acc_full + kSAcc; // [kSAcc] TMEM accumulator read (4 epilogue warps)
+    uint64_t *esync = acc_empty + kSAcc;    // epilogue warps: column maxima written (4 warps)
+    uint64_t *done_bar = esync + 1;         // epilogue warps finished with TMEM (4 warps)
+    float *red = reinterpret_cast<float *>(base + lay.red);
+    int *prefix = reinterpret_cast<int *>(base + lay.prefix);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + lay.misc);
+    volatile int *abort_flag = reinterpret_cast<int *>(base + lay.misc) + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    launch_dependents(); // the select may start its prologue while pages are scored
+
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&k_map);
+        prefetch_tensormap(&q_map);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&qfull[b]), 1);
+            mbar_init(smem_u32(&qempty[b]), 1);
+        }
+        for (int b = 0; b < kSAcc; ++b) {
+            mbar_init(smem_u32(&acc_full[b]), 1);
+            mbar_init(smem_u32(&acc_empty[b]), 4);
+        }
+        mbar_init(smem_u32(esync), 4);
+        mbar_init(smem_u32(done_bar), 4);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1)
+        tmem_alloc(smem_u32(tmem_slot), kCols);
+    build_item_prefix<1>(p, prefix); // ends with __syncthreads
+    tcgen05_before_sync();
+    __syncthreads();
+    tcgen05_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    const int P = prefix[p.R];
+    const int x_begin = (int)((long long)blockIdx.x * P / gridDim.x);
+    const int n = (int)((long long)(blockIdx.x + 1) * P / gridDim.x) - x_begin;
+
+    // (request, block) of page x: the largest r with prefix[r] <= x has pages
+    auto request_of = [&](int x) {
+        int lo = 0, hi = p.R - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (prefix[mid] <= x)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        return lo;
+    };
+    int cur_r = 0, cur_b = 0; // cursor of each role over its pages
+    if (n > 0) {
+        cur_r = request_of(x_begin);
+        cur_b = x_begin - prefix[cur_r];
+    }
+    auto advance = [&](int &r, int &b) {
+        if (++b >= prefix[r + 1] - prefix[r]) {
+            b = 0;
+            do
+                ++r;
+            while (r < p.R && prefix[r + 1] == prefix[r]);
+        }
+    };
+
+    if (warp == 0) {
+        // =================== producer ===================
+        bool ok = true;
+        int units = 0, last_r = -1, issued = 0, q_issued = 0;
+        for (int l0 = 0; l0 < n && ok; l0 += 32) {
+            // page ids of the next 32 pages, one block-table read per lane
+            int page = 0, rr = 0;
+            if (l0 + lane < n) {
+                const int x = x_begin + l0 + lane;
+                rr = request_of(x);
+                const int bb = x - prefix[rr];
+                page = p.block_table[(size_t)rr * p.maxB + bb];
+                if (page < 0 || page >= p.num_pages) {
+                    set_error(p.err, kErrPage);
+                    page = 0; // stay in bounds; the call's outputs are void
+                }
+            }
+            const int cnt = n - l0 < 32 ? n - l0 : 32;
+            for (int i = 0; i < cnt; ++i) {
+                const int l = l0 + i;
+                const int pg = __shfl_sync(0xffffffffu, page, i);
+                const int ri = __shfl_sync(0xffffffffu, rr, i);
+                if (lane == 0) {
+                    const int slot = l % STAGES;
+                    if (l >= STAGES)
+                        ok = mbar_wait_or_abort(smem_u32(&empty[slot]), ((l / STAGES) - 1) & 1, abort_flag);
+                    if (ok && ri != last_r) {
+                        last_r = ri;
+                        const int qb = units & 1;
+                        if (units >= 2)
+                            ok = mbar_wait_or_abort(smem_u32(&qempty[qb]), ((units >> 1) - 1) & 1, abort_flag);
+                        if (ok) {
+                            const uint32_t qbar = smem_u32(&qfull[qb]);
+                            const uint32_t dst = smem_u32(qbuf + qb * kQTile);
+                            mbar_arrive_expect_tx(qbar, kQTile);
+                            tma_load_2d(dst, &q_map, 0, ri * p.nq, qbar);
+                            tma_load_2d(dst + kQTile / 2, &q_map, 64, ri * p.nq, qbar);
+                            q_issued = units + 1;
+                        }
+                        ++units;
+                    }
+                    if (ok) {
+                        const uint32_t bar = smem_u32(&full[slot]);
+                        const uint32_t dst = smem_u32(ring + (size_t)slot * kSTile);
+                        mbar_arrive_expect_tx(bar, kSTile);
+                        tma_load_2d(dst, &k_map, 0, pg * kPage, bar);
+                        tma_load_2d(dst + kSTile / 2, &k_map, 64, pg * kPage, bar);
+                        issued = l + 1;
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok)
+                    break;
+            }
+        }
+        if (!ok && lane == 0) {
+            set_error(p.err, kErrTimeout);
+            *abort_flag = 1;
+            // let the copies in flight land before the CTA's shared memory goes away
+            for (int z = issued - STAGES < 0 ? 0 : issued - STAGES; z < issued; ++z)
+                (void)mbar_wait_bounded(smem_u32(&full[z % STAGES]), (z / STAGES) & 1);
+            for (int u = q_issued - 2 < 0 ? 0 : q_issued - 2; u < q_issued; ++u)
+                (void)mbar_wait_bounded(smem_u32(&qfull[u & 1]), (u >> 1) & 1);
+        }
+        return;
+    }
+
+    if (warp == 1) {
+        // =================== MMA issuer (lane 0) ===================
+        constexpr uint32_t kIdesc = umma_idesc_bf16(128, NPAD, 0, 0); // both K-major
+        if (lane == 0 && n > 0) {
+            bool ok = true;
+            int units = 0, mma_r = -1, r = cur_r, b = cur_b;
+            for (int l = 0; l < n && ok; ++l) {
+                const int slot = l % STAGES, ab = l % kSAcc;
+                ok = mbar_wait_or_abort(smem_u32(&full[slot]), (l / STAGES) & 1, abort_flag);
+                if (ok && r != mma_r) {
+                    ok = mbar_wait_or_abort(smem_u32(&qfull[units & 1]), (units >> 1) & 1, abort_flag);
+                    mma_r = r;
+                    ++units;
+                }
+                if (ok && l >= kSAcc)
+                    ok = mbar_wait_or_abort(smem_u32(&acc_empty[ab]), ((l / kSAcc) - 1) & 1, abort_flag);
+                if (!ok)
+                    break;
+                tcgen05_after_sync();
+                const int qb = (units - 1) & 1;
+                const uint32_t tile = smem_u32(ring + (size_t)slot * kSTile);
+                const uint32_t qtile = smem_u32(qbuf + qb * kQTile);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint64_t a = umma_desc_sw128(tile + (ks >> 2) * (kSTile / 2) + (ks & 3) * 32, 16, 1024);
+                    const uint64_t bq = umma_desc_sw128(qtile + (ks >> 2) * (kQTile / 2) + (ks & 3) * 32, 16, 1024);
+                    umma_bf16(tmem + ab * NPAD, a, bq, kIdesc, ks > 0);
+                }
+                umma_commit(smem_u32(&acc_full[ab]));
+                umma_commit(smem_u32(&empty[slot])); // tile read
+                const int r_prev = r;
+                advance(r, b);
+                if (l + 1 == n || r != r_prev)
+                    umma_commit(smem_u32(&qempty[qb])); // last page of the request here
+            }
+            if (!ok) {
+                set_error(p.err, kErrTimeout);
+                *abort_flag = 1;
+            }
+        }
+        __syncwarp();
+        // free TMEM once the epilogue warps are done with it (they always
+        // arrive, also after an abort; the wait is bounded)
+        if (lane == 0)
+            (void)mbar_wait_bounded(smem_u32(done_bar), 0);
+        __syncwarp();
+        tcgen05_after_sync();
+        tmem_dealloc(tmem, kCols);
+        return;
+    }
+
+    // =================== epilogue warps 2..5 ===================
+    const int quarter = warp & 3;   // TMEM lanes 32 * quarter ..: page tokens
+    const int e = threadIdx.x - 64; // 0..127
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16);
+    bool ok = true;
+    int r = cur_r, b = cur_b, seq_r = -1, seq_len = 0;
+    for (int l = 0; l < n && ok; ++l) {
+        const int ab = l % kSAcc, rb2 = l & 1; // accumulator, red buffer
+        ok = mbar_wait_or_abort(smem_u32(&acc_full[ab]), (l / kSAcc) & 1, abort_flag);
+        if (!ok)
+            break;
+        tcgen05_after_sync();
+        float v[NPAD];
+#pragma unroll
+        for (int c16 = 0; c16 < NPAD / 16; ++c16)
+            tmem_ld16(lane_base + ab * NPAD + 16 * c16, *reinterpret_cast<float(*)[16]>(v + 16 * c16));
+        tcgen05_before_sync();
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_u32(&acc_empty[ab]));
+        if (r != seq_r) {
+            seq_r = r;
+            seq_len = p.seq_lens[r];
+        }
+        // token j of the request sees positions < seq_len + j
+        const int lim = seq_len - (b * kPage + 32 * quarter + lane); // visible iff j + lim > 0
+        float *rw = red + (rb2 * 4 + quarter) * NPAD;
+        float mine = -INFINITY; // maximum of column j, kept by lane j % 32
+#pragma unroll
+        for (int j = 0; j < NPAD; ++j) {
+            if (j < p.nq) {
+                const float m = warp_max_f32(j + lim > 0 ? v[j] : -INFINITY);
+                if (lane == (j & 31))
+                    mine = m;
+            }
+            if ((j & 31) == 31 || j == NPAD - 1) {
+                if (lane + (j & ~31) < p.nq && lane <= (j & 31))
+                    rw[lane + (j & ~31)] = mine;
+            }
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_u32(esync));
+        if (!mbar_wait_or_abort(smem_u32(esync), l & 1, abort_flag)) {
+            ok = false;
+            break;
+        }
+        if (e < p.nq) {
+            const float *rb = red + rb2 * 4 * NPAD;
+            const float m = fmaxf(fmaxf(rb[e], rb[NPAD + e]), fmaxf(rb[2 * NPAD + e], rb[3 * NPAD + e]));
+            p.block_scores[(size_t)(r * p.nq + e) * p.maxB + b] = m;
+        }
+        advance(r, b);
+    }
+    if (!ok) {
+        set_error(p.err, kErrTimeout);
+        *abort_flag = 1;
+    }
+    tcgen05_before_sync();
+    __syncwarp();
+    if (lane == 0)
+        mbar_arrive(smem_u32(done_bar));
+}
+
+template <int NPAD, int STAGES>
+cudaError_t launch_umma_t(const ScoreParams &p, const CUtensorMap &kmap, const CUtensorMap &qmap,
+                          int num_sms, cudaStream_t stream)
+{
+    auto kern = index_score_umma_kernel<NPAD, STAGES>;
+    const size_t smem = score_layout(NPAD, STAGES, p.R).total;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    long long grid = num_sms;
+    const long long max_pages = (long long)p.R * p.maxB;
+    if (grid > max_pages)
+        grid = max_pages;
+    if (grid < 1)
+        grid = 1;
+    kern<<<(unsigned)grid, kSThreads, smem, stream>>>(kmap, qmap, p);
+    return cudaGetLastError();
+}
+
+// The deepest ring that fits next to the request prefix (R + 1 ints).
+template <int NPAD>
+cudaError_t launch_umma_fit(const ScoreParams &p, const CUtensorMap &kmap, const CUtensorMap &qmap,
+                            int num_sms, cudaStream_t stream)
+{
+    if (score_layout(NPAD, 5, p.R).total <= (size_t)kSMaxSmem)
+        return launch_umma_t<NPAD, 5>(p, kmap, qmap, num_sms, stream);
+    if (score_layout(NPAD, 3, p.R).total > (size_t)kSMaxSmem)
+        return cudaErrorInvalidConfiguration; // not reached within the shape limits
+    return launch_umma_t<NPAD, 3>(p, kmap, qmap, num_sms, stream);
+}
+
 template <bool NVFP4, int NT, int PPI>
 cudaError_t launch_t(const ScoreParams &p, int num_sms, cudaStream_t stream)
 {
@@ -278,6 +628,27 @@ cudaError_t launch_t(const ScoreParams &p, int num_sms, cudaStream_t stream)
 cudaError_t launch_index_score(const ScoreParams &p, int index_dtype, int num_sms,
                                cudaStream_t stream)
 {
+    // Many query tokens per request (bf16 index keys): the tcgen05 scorer, one
+    // MMA per page for all of them.  Otherwise the mma.sync scorer, whose
+    // loads are all in flight from the start of the kernel: for a few query
+    // tokens per page the tensor work is small and the start-up of the
+    // TMA / MMA pipeline dominates, and for NVFP4 keys the in-register
+    // widening avoids the f16 staging traffic in shared memory.
+    if (index_dtype == MSA_BF16 && p.nq > 8) {
+        const int T = p.R * p.nq;
+        const int npad = (p.nq + 15) / 16 * 16;
+        CUtensorMap qmap, kmap;
+        if (!encode_2d_sw128(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.q_idx, kDim, T, kDim * 2, 64, npad) ||
+            !encode_2d_sw128(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.idxk, kDim,
+                             (uint64_t)p.num_pages * kPage, kDim * 2, 64, kPage))
+            return cudaErrorInvalidValue;
+        switch (npad) {
+        case 16: return launch_umma_fit<16>(p, kmap, qmap, num_sms, stream);
+        case 32: return launch_umma_fit<32>(p, kmap, qmap, num_sms, stream);
+        case 48: return launch_umma_fit<48>(p, kmap, qmap, num_sms, stream);
+        default: return launch_umma_fit<64>(p, kmap, qmap, num_sms, stream);
+        }
+    }
     const int nt = (p.nq + 7) / 8;
     if (index_dtype == MSA_NVFP4) {
         switch (nt) {

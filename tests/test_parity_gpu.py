@@ -93,6 +93,32 @@ def test_index_score_is_bit_exact(torch_cuda, idx):
     check_device_ok(dp)
 
 
+@pytest.mark.parametrize("nq", [1, 3, 8, 9, 16, 17, 33, 48, 64])
+@pytest.mark.parametrize("index_dtype", [synth.BF16, synth.NVFP4])
+def test_index_score_across_query_counts(torch_cuda, nq, index_dtype):
+    # both scorers (mma.sync for up to 8 query tokens per request or NVFP4
+    # keys, tcgen05 above), ragged contexts (cached tokens, >= nq): one
+    # position for the first query token, page edges, and a request with more
+    # pages than there are CTAs
+    ctx = [nq, nq + 127, max(nq, 128), nq + 128, 700, 2000, 40000]
+    pb = synth.make_problem(name=f"nq{nq}", contexts=ctx, q_per_req=nq, num_kv_heads=1, topk=4,
+                            index_dtype=index_dtype,
+                            index_range=(-4, 4) if index_dtype == synth.NVFP4 else (-8, 8),
+                            guard_page=True, seed=300 + nq)
+    dp = device_problem(pb)
+    dp.index_score()
+    res = dp.results()
+    rng = np.random.default_rng(nq)
+    tokens = sorted(set(rng.choice(pb.num_tokens, size=min(pb.num_tokens, 40), replace=False).tolist())
+                    | {0, pb.num_tokens - 1})
+    nb = pb.blocks_per_request()
+    for t in tokens:
+        want = oracle.block_scores(pb, t)
+        n = int(nb[t // pb.q_per_req])
+        assert np.array_equal(res["block_scores"][t, :n], want[:n]), (t, nq)
+    check_device_ok(dp)
+
+
 @pytest.mark.parametrize("idx", range(5))
 def test_select_is_bit_exact_on_oracle_scores(torch_cuda, idx):
     torch = torch_cuda
