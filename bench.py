@@ -238,6 +238,19 @@ def run_ours(args, rank, world, local):
     if args.replicas:
         nrep = args.replicas  # profiling runs: fewer device copies (ncu flushes caches itself)
     reps = [base] + [base.replicate() for _ in range(nrep - 1)]
+
+    if args.profile:
+        # for ncu: W + K fused steps through the C ABI, cycling the copies, no
+        # graphs and no other timing; the library's kernels before the first
+        # of them are the 3 of the check step above and 3 per warm-up step
+        for i in range(args.warmup + args.steps):
+            reps[i % nrep].decode_step(keep_intermediates=False)
+        torch.cuda.synchronize()
+        if rank == 0:
+            print(json.dumps({"profile": pb.name, "kernels_per_step": KERNELS_PER_STEP,
+                              "library_launches_before_steps": KERNELS_PER_STEP * (1 + args.warmup),
+                              "steps": args.steps, "replicas": nrep}))
+        return
     stream = torch.cuda.Stream()
 
     def capture(fn, count):
@@ -522,6 +535,8 @@ def main():
     ap.add_argument("--replicas", type=int, default=0,
                     help="device copies of the pools (default: enough that inputs exceed L2); "
                          "small values are for ncu captures only")
+    ap.add_argument("--profile", action="store_true",
+                    help="only run W + K fused steps (for ncu launch lists and captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
     uint64_t *p_free = p_full + 2;
     uint64_t *o_full = p_free + 2;
     uint64_t *o_free = o_full + 2;
-    uint64_t *smx_bar = o_free + 2;    // softmax-warps barrier (kUSoftmax arrivals)
+    uint64_t *smx_bar = o_free + 2;    // softmax-warps barrier (kUSmxWarps arrivals)
     uint64_t *done_bar = smx_bar + 1;  // softmax warps finished with TMEM (kUSmxWarps arrivals)
     uint64_t *kst_full = done_bar + 1; // FP8: [2] staging K converted (kUCvtWarps)
     uint64_t *kst_empty = kst_full + 2; // FP8: [2] staging K read by the MMA (commit)
@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
             mbar_init(smem_u32(&o_full[b]), 1);
             mbar_init(smem_u32(&o_free[b]), kUSmxWarps);
         }
-        mbar_init(smem_u32(smx_bar), kUSoftmax);
+        mbar_init(smem_u32(smx_bar), kUSmxWarps);
         mbar_init(smem_u32(done_bar), kUSmxWarps);
         s_flag[0] = 0;
         s_flag[1] = 0;
@@ -313,13 +313,11 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
             dst[i] = make_entry(p, x_begin + l0 + i, qt);
         __syncwarp();
     };
-    // the first two table windows, visible to every warp before anything starts
-    if (warp == 0) {
-        if (ntasks > 0)
-            fill_window(0);
-        if (ntasks > kWin)
-            fill_window(1);
-    }
+    // the first two table windows, filled by all threads (one round of the
+    // two dependent reads for up to blockDim.x tasks) and visible to every
+    // warp before anything starts
+    for (int i = threadIdx.x; i < 2 * kWin && i < ntasks; i += blockDim.x)
+        table[i] = make_entry(p, x_begin + i, qt);
     __syncthreads();
 
     if (warp == 0) {
@@ -609,8 +607,13 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
     const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16) + h0;
     int sync_phase = 0;
     bool ok = true;
+    // barrier of the softmax warps: one arrival per warp after __syncwarp
+    // (which orders the warp's shared and global writes before lane 0's
+    // release arrival)
     auto ssync = [&]() {
-        mbar_arrive(smem_u32(smx_bar));
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_u32(smx_bar));
         if (!mbar_wait_or_abort(smem_u32(smx_bar), sync_phase & 1, abort_flag))
             ok = false;
         ++sync_phase;

@@ -601,6 +601,236 @@ cudaError_t launch_umma_fit(const ScoreParams &p, const CUtensorMap &kmap, const
     return launch_umma_t<NPAD, 3>(p, kmap, qmap, num_sms, stream);
 }
 
+// ---------------------------------------------------------------------------
+// NVFP4 scorer with a bulk-copy page ring (up to 16 query tokens a request).
+// One persistent CTA per SM takes a contiguous range of the call's pages
+// (request-major).  Warp 0 streams each page's packed E2M1 codes (8 KiB) and
+// E4M3 scales (1 KiB) into a ring of shared-memory stages with two 1-D bulk
+// copies; consumer warp w scores pages w, w + 8, ... of the range on its own:
+// 16-byte loads of 32 codes per row and thread, widened in registers
+// (cvt.rn.f16x2.e2m1x2 times the power-of-two f16 scale: exact), mma.sync
+// m16n8k16 against the request's query tokens kept as f16 fragments in
+// registers, causal mask, maximum over the page's 128 rows in registers and
+// shuffles, one write per (query token, block).  No global load waits in the
+// consumers' path and no cross-warp reduction.
+constexpr int kF4Consumers = 8;
+constexpr int kF4Threads = 32 * (1 + kF4Consumers);
+constexpr int kF4Codes = kPage * kDim / 2;      // 8 KiB
+constexpr int kF4Scales = kPage * kDim / 16;    // 1 KiB
+constexpr int kF4Stage = kF4Codes + kF4Scales;  // 9 KiB
+constexpr int kF4Stages = 16;
+
+__host__ __device__ inline size_t fp4_smem_bytes(int R)
+{
+    // ring, full[S], empty[S], abort flag, request prefix [R + 1]
+    return align_to((size_t)kF4Stages * kF4Stage, 16) + 2 * kF4Stages * 8 + 16 + (size_t)(R + 1) * 4 + 128;
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kF4Threads, 1) index_score_fp4_kernel(const ScoreParams p)
+{
+    extern __shared__ __align__(128) uint8_t smem_f4[];
+    uint8_t *ring = smem_f4;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem_f4 + align_to((size_t)kF4Stages * kF4Stage, 16));
+    uint64_t *empty = full + kF4Stages;
+    volatile int *abort_flag = reinterpret_cast<int *>(empty + kF4Stages);
+    int *prefix = reinterpret_cast<int *>(empty + kF4Stages) + 4;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    launch_dependents(); // the select may start its prologue while pages are scored
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kF4Stages; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    build_item_prefix<1>(p, prefix); // ends with __syncthreads
+
+    const int P = prefix[p.R];
+    const int x_begin = (int)((long long)blockIdx.x * P / gridDim.x);
+    const int n = (int)((long long)(blockIdx.x + 1) * P / gridDim.x) - x_begin;
+    auto request_of = [&](int x) { // largest r with prefix[r] <= x (a request with pages)
+        int lo = 0, hi = p.R - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (prefix[mid] <= x)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        return lo;
+    };
+
+    if (warp == 0) {
+        // =================== producer ===================
+        bool ok = true;
+        int issued = 0;
+        for (int l0 = 0; l0 < n && ok; l0 += 32) {
+            int page = 0;
+            if (l0 + lane < n) {
+                const int x = x_begin + l0 + lane;
+                const int rr = request_of(x);
+                page = p.block_table[(size_t)rr * p.maxB + (x - prefix[rr])];
+                if (page < 0 || page >= p.num_pages) {
+                    set_error(p.err, kErrPage);
+                    page = 0; // stay in bounds; the call's outputs are void
+                }
+            }
+            const int cnt = n - l0 < 32 ? n - l0 : 32;
+            for (int i = 0; i < cnt; ++i) {
+                const int l = l0 + i;
+                const int pg = __shfl_sync(0xffffffffu, page, i);
+                if (lane == 0) {
+                    const int slot = l % kF4Stages;
+                    if (l >= kF4Stages)
+                        ok = mbar_wait_or_abort(smem_u32(&empty[slot]), ((l / kF4Stages) - 1) & 1, abort_flag);
+                    if (ok) {
+                        const uint32_t bar = smem_u32(&full[slot]);
+                        const uint32_t dst = smem_u32(ring + (size_t)slot * kF4Stage);
+                        mbar_arrive_expect_tx(bar, kF4Stage);
+                        bulk_load(dst, p.idxk + (size_t)pg * kF4Codes, kF4Codes, bar);
+                        bulk_load(dst + kF4Codes, p.scales + (size_t)pg * kF4Scales, kF4Scales, bar);
+                        issued = l + 1;
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok)
+                    break;
+            }
+        }
+        if (!ok && lane == 0) {
+            set_error(p.err, kErrTimeout);
+            *abort_flag = 1;
+            for (int z = issued - kF4Stages < 0 ? 0 : issued - kF4Stages; z < issued; ++z)
+                (void)mbar_wait_bounded(smem_u32(&full[z % kF4Stages]), (z / kF4Stages) & 1);
+        }
+        return;
+    }
+
+    // =================== consumer warps 1..8 ===================
+    const int cw = warp - 1;
+    const int g = lane >> 2, q = lane & 3;
+    uint32_t bq[NT][8][2]; // query fragments of the current request, f16
+    int frag_r = -1, seq_len = 0;
+    bool ok = true;
+    for (int l = cw; l < n && ok; l += kF4Consumers) {
+        const int slot = l % kF4Stages;
+        const int x = x_begin + l;
+        const int r = request_of(x), b = x - prefix[r];
+        if (r != frag_r) {
+            frag_r = r;
+            seq_len = p.seq_lens[r];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int j = nt * 8 + g;
+                const uint16_t *qrow = p.q_idx + (size_t)(r * p.nq + (j < p.nq ? j : 0)) * kDim;
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    // k-step s covers dims 32 q + 4 s .. + 3 (the codes' order below)
+                    uint2 v = make_uint2(0, 0);
+                    if (j < p.nq)
+                        v = __ldg(reinterpret_cast<const uint2 *>(qrow + 32 * q + 4 * s));
+                    bq[nt][s][0] = bf16x2_to_f16x2(v.x);
+                    bq[nt][s][1] = bf16x2_to_f16x2(v.y);
+                }
+            }
+        }
+        if (!mbar_wait_or_abort(smem_u32(&full[slot]), (l / kF4Stages) & 1, abort_flag)) {
+            ok = false;
+            break;
+        }
+        const uint8_t *codes = ring + (size_t)slot * kF4Stage;
+        const uint8_t *scl = codes + kF4Codes;
+        float rmax[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+            rmax[nt][0] = rmax[nt][1] = -INFINITY;
+        const bool need_mask = (b + 1) * kPage > seq_len;
+#pragma unroll 2
+        for (int mt = 0; mt < kPage / 16; ++mt) {
+            const int row0 = 16 * mt + g;
+            const uint4 c0 = *reinterpret_cast<const uint4 *>(codes + row0 * 64 + 16 * q);
+            const uint4 c1 = *reinterpret_cast<const uint4 *>(codes + (row0 + 8) * 64 + 16 * q);
+            const uint32_t s0 = *reinterpret_cast<const uint16_t *>(scl + row0 * 8 + 2 * q);
+            const uint32_t s1 = *reinterpret_cast<const uint16_t *>(scl + (row0 + 8) * 8 + 2 * q);
+            uint32_t a[8][4];
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                // bytes 2s, 2s+1 of the 16: dims 32q + 4s .. + 3; scale byte s / 4
+                const uint32_t w0 = (&c0.x)[s >> 1], w1 = (&c1.x)[s >> 1];
+                const int sh = (s & 1) * 16, ssh = (s >> 2) * 8;
+                const uint32_t e0 = (s0 >> ssh) & 0xFFu, e1 = (s1 >> ssh) & 0xFFu;
+                const uint32_t f0 = e4m3x2_to_f16x2(e0 | (e0 << 8));
+                const uint32_t f1 = e4m3x2_to_f16x2(e1 | (e1 << 8));
+                a[s][0] = hmul2_u32(e2m1x2_to_f16x2((w0 >> sh) & 0xFFu), f0);
+                a[s][1] = hmul2_u32(e2m1x2_to_f16x2((w1 >> sh) & 0xFFu), f1);
+                a[s][2] = hmul2_u32(e2m1x2_to_f16x2((w0 >> (sh + 8)) & 0xFFu), f0);
+                a[s][3] = hmul2_u32(e2m1x2_to_f16x2((w1 >> (sh + 8)) & 0xFFu), f1);
+            }
+            const int pos_g = b * kPage + row0;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    mma_f16(acc, a[s], bq[nt][s][0], bq[nt][s][1]);
+                // acc: (row g, cols 2q, 2q+1), (row g + 8, cols 2q, 2q+1); col = query token
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    float v0 = acc[c], v1 = acc[2 + c];
+                    if (need_mask) {
+                        const int L = seq_len + nt * 8 + 2 * q + c;
+                        if (pos_g >= L)
+                            v0 = -INFINITY;
+                        if (pos_g + 8 >= L)
+                            v1 = -INFINITY;
+                    }
+                    rmax[nt][c] = fmaxf(rmax[nt][c], fmaxf(v0, v1));
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_u32(&empty[slot])); // the page's codes are in registers
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                float v = rmax[nt][c];
+                v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+                v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+                v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+                const int jj = nt * 8 + 2 * q + c;
+                if (g == 0 && jj < p.nq)
+                    p.block_scores[(size_t)(r * p.nq + jj) * p.maxB + b] = v;
+            }
+    }
+    if (!ok) {
+        set_error(p.err, kErrTimeout);
+        *abort_flag = 1;
+    }
+}
+
+template <int NT>
+cudaError_t launch_fp4_t(const ScoreParams &p, int num_sms, cudaStream_t stream)
+{
+    const size_t smem = fp4_smem_bytes(p.R);
+    cudaError_t e = cudaFuncSetAttribute(index_score_fp4_kernel<NT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    long long grid = num_sms;
+    const long long max_pages = (long long)p.R * p.maxB;
+    if (grid > max_pages)
+        grid = max_pages;
+    if (grid < 1)
+        grid = 1;
+    index_score_fp4_kernel<NT><<<(unsigned)grid, kF4Threads, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
 template <bool NVFP4, int NT, int PPI>
 cudaError_t launch_t(const ScoreParams &p, int num_sms, cudaStream_t stream)
 {
@@ -650,6 +880,8 @@ cudaError_t launch_index_score(const ScoreParams &p, int index_dtype, int num_sm
         }
     }
     const int nt = (p.nq + 7) / 8;
+    if (index_dtype == MSA_NVFP4 && nt <= 2 && fp4_smem_bytes(p.R) <= (size_t)kSMaxSmem)
+        return nt == 1 ? launch_fp4_t<1>(p, num_sms, stream) : launch_fp4_t<2>(p, num_sms, stream);
     if (index_dtype == MSA_NVFP4) {
         switch (nt) {
         case 1: return launch_t<true, 1, 4>(p, num_sms, stream);
