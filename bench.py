@@ -92,6 +92,13 @@ def hbm_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def score_kernel_name(index_dtype: str, q_per_req: int) -> str:
+    """The index scorer the library launches for this shape (its dispatch rule)."""
+    if index_dtype == "bf16":
+        return "index_score_umma_kernel" if q_per_req > 8 else "index_score_kernel"
+    return "index_score_fp4_kernel" if q_per_req <= 16 else "index_score_kernel"
+
+
 def source_digest(files) -> str:
     h = hashlib.sha256()
     for f in files:
@@ -385,12 +392,12 @@ def run_ours(args, rank, world, local):
         dom_bytes = nbytes["kv"] + nbytes["small"]
         src = ["sparse_attention_decode_msa_gb300/csrc/msa_decode.cu",
                "sparse_attention_decode_msa_gb300/csrc/msa_internal.cuh"]
-        kernel_key = "sparse_decode_kernel"
+        kernel_key = "sparse_decode_umma_kernel"
     else:
         dom_bytes = nbytes["index"] + nbytes["scores_io"] + T * 256
         src = ["sparse_attention_decode_msa_gb300/csrc/msa_score.cu",
                "sparse_attention_decode_msa_gb300/csrc/msa_internal.cuh"]
-        kernel_key = "index_score_kernel"
+        kernel_key = score_kernel_name(pb.index_dtype, pb.q_per_req)
     achieved = dom_bytes / (stage_ms[dominant] / 1e3) / 1e9
 
     result = {
@@ -422,7 +429,7 @@ def run_ours(args, rank, world, local):
         "frac_of_8tbs": round(nbytes["total"] / (ms_step_max / 1e3) / 8e12, 4),
         "stages_us": {k: round(v * 1e3, 2) for k, v in stage_ms.items()},
         "roofline": {
-            "kernel": kernel_key + (" (+ merge kernel)" if dominant == "sparse_decode" else ""),
+            "kernel": kernel_key,
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,
@@ -436,6 +443,9 @@ def run_ours(args, rank, world, local):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 5)},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "kernels": [score_kernel_name(pb.index_dtype, pb.q_per_req),
+                    "select_topk_warp_kernel" if pb.max_blocks <= 2048 else "select_topk_kernel",
+                    "sparse_decode_umma_kernel"],
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

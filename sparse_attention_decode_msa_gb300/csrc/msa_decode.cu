@@ -655,7 +655,8 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
         pending = false;
     };
 
-    auto finalize = [&](int t, int g) {
+    // final: the CTA's last unit (the usual place for it to arrive last)
+    auto finalize = [&](int t, int g, bool final) {
         // denominators: reduce lsum over the 128 token lanes
 #pragma unroll
         for (int h = 0; h < kUHeads; ++h) {
@@ -701,57 +702,89 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
                 p.lse[hbase + idx] = (Mi == -INFINITY) ? -INFINITY : (Mi + log2f(Li)) * 0.69314718055994531f;
             return;
         }
+        int arrivals = 0; // CTAs with tasks of this unit
+        for (int cc = c_first; cc <= c_last; ++cc)
+            arrivals += !range_empty(cc, P, G);
+        // Fast path for the CTA's last unit: when every other CTA of the unit
+        // is already in (the usual case there), this one merges at once from
+        // its registers and their slots, without publishing its own.  A unit
+        // at the start of the range is usually first in and skips the check.
+        bool last = false;
+        if (final) {
+            if (sidx == 0)
+                s_flag[0] = ld_acquire_gpu(&p.counters[u]) == arrivals - 1;
+            ssync();
+            last = s_flag[0] != 0;
+            ssync(); // s_flag is read by every thread before it is rewritten
+        }
+        if (!last) {
 #pragma unroll
-        for (int h = 0; h < kUHeads; ++h)
-            slot[(h0 + h) * kDim + idx] = o[h];
-        if (idx < kUHeads) {
-            slot[kGroup * kDim + h0 + idx] = Mi;
-            slot[kGroup * kDim + kGroup + h0 + idx] = Li;
+            for (int h = 0; h < kUHeads; ++h)
+                slot[(h0 + h) * kDim + idx] = o[h];
+            if (idx < kUHeads) {
+                slot[kGroup * kDim + h0 + idx] = Mi;
+                slot[kGroup * kDim + kGroup + h0 + idx] = Li;
+            }
+            // The CTA barrier orders every thread's slot writes before thread
+            // 0's release; its acquire makes the other CTAs' slots visible to
+            // the CTA that arrives last, and the barrier after it to all its
+            // threads.
+            ssync();
+            if (sidx == 0)
+                s_flag[0] = atom_add_acq_rel_gpu(&p.counters[u], 1) == arrivals - 1;
+            ssync();
+            last = s_flag[0] != 0;
         }
-        // The CTA barrier orders every thread's slot writes before thread 0's
-        // release; its acquire makes the other CTAs' slots visible to the
-        // CTA that arrives last, and the barrier after it to all its threads.
-        ssync();
-        if (sidx == 0) {
-            int arrivals = 0;
-            for (int cc = c_first; cc <= c_last; ++cc)
-                arrivals += !range_empty(cc, P, G);
-            const int before = atom_add_acq_rel_gpu(&p.counters[u], 1);
-            s_flag[0] = before == arrivals - 1;
-        }
-        ssync();
-        if (s_flag[0]) {
-            const float *sbase = p.partial + (size_t)(c_first + u) * kPartialFloats;
-            const int nslots = c_last - c_first + 1;
-            const size_t obase = (size_t)t * p.Hkv * kGroup + (size_t)g * kGroup;
-            for (int e = sidx; e < kGroup * kDim / 8; e += kUSoftmax) {
-                const int row = e >> 4, d0 = (e & 15) * 8;
-                float Mx = -INFINITY;
-                for (int s = 0; s < nslots; ++s)
-                    if (!range_empty(c_first + s, P, G))
-                        Mx = fmaxf(Mx, __ldcg(sbase + (size_t)s * kPartialFloats + kGroup * kDim + row));
-                float Lx = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                for (int s = 0; s < nslots; ++s) {
-                    if (range_empty(c_first + s, P, G))
-                        continue;
-                    const float *sl = sbase + (size_t)s * kPartialFloats;
-                    const float ms = __ldcg(sl + kGroup * kDim + row);
-                    const float wgt = (Mx == -INFINITY) ? 0.f : ex2(ms - Mx);
-                    Lx += wgt * __ldcg(sl + kGroup * kDim + kGroup + row);
-                    const float4 a = __ldcg(reinterpret_cast<const float4 *>(sl + row * kDim + d0));
-                    const float4 bb = __ldcg(reinterpret_cast<const float4 *>(sl + row * kDim + d0 + 4));
-                    acc[0] += wgt * a.x; acc[1] += wgt * a.y; acc[2] += wgt * a.z; acc[3] += wgt * a.w;
-                    acc[4] += wgt * bb.x; acc[5] += wgt * bb.y; acc[6] += wgt * bb.z; acc[7] += wgt * bb.w;
+        if (last) {
+            // Combine the unit's slots in slot (CTA) order, this CTA's own
+            // part from registers (thread = dimension idx for 8 heads), with a
+            // running maximum.  All loads of a slot are issued before any
+            // arithmetic and the stores come after the last slot, so each
+            // slot costs one round trip to L2.
+            float Mx[kUHeads], Lx[kUHeads], acc[kUHeads];
+#pragma unroll
+            for (int h = 0; h < kUHeads; ++h) {
+                Mx[h] = -INFINITY;
+                Lx[h] = 0.f;
+                acc[h] = 0.f;
+            }
+            for (int cc = c_first; cc <= c_last; ++cc) {
+                if (range_empty(cc, P, G))
+                    continue;
+                float ms[kUHeads], ls[kUHeads], os[kUHeads];
+                if (cc == c) {
+#pragma unroll
+                    for (int h = 0; h < kUHeads; ++h) {
+                        ms[h] = m_run[h];
+                        ls[h] = L[h];
+                        os[h] = o[h];
+                    }
+                } else {
+                    const float *sl = p.partial + (size_t)(cc + u) * kPartialFloats;
+#pragma unroll
+                    for (int h = 0; h < kUHeads; ++h) {
+                        ms[h] = __ldcg(sl + kGroup * kDim + h0 + h);
+                        ls[h] = __ldcg(sl + kGroup * kDim + kGroup + h0 + h);
+                        os[h] = __ldcg(sl + (h0 + h) * kDim + idx);
+                    }
                 }
-                const float inv = Lx > 0.f ? 1.f / Lx : 0.f;
-                uint4 packed;
-                packed.x = pack_bf16(acc[0] * inv, acc[1] * inv);
-                packed.y = pack_bf16(acc[2] * inv, acc[3] * inv);
-                packed.z = pack_bf16(acc[4] * inv, acc[5] * inv);
-                packed.w = pack_bf16(acc[6] * inv, acc[7] * inv);
-                *reinterpret_cast<uint4 *>(p.out + (obase + row) * kDim + d0) = packed;
-                if (d0 == 0)
-                    p.lse[obase + row] = (Mx == -INFINITY) ? -INFINITY : (Mx + log2f(Lx)) * 0.69314718055994531f;
+#pragma unroll
+                for (int h = 0; h < kUHeads; ++h) {
+                    const float m_new = fmaxf(Mx[h], ms[h]);
+                    const float ref = (m_new == -INFINITY) ? 0.f : m_new;
+                    const float a_old = ex2(Mx[h] - ref), a_s = ex2(ms[h] - ref); // 0 for -inf
+                    Lx[h] = Lx[h] * a_old + ls[h] * a_s;
+                    acc[h] = acc[h] * a_old + os[h] * a_s;
+                    Mx[h] = m_new;
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < kUHeads; ++h) {
+                const float inv = Lx[h] > 0.f ? 1.f / Lx[h] : 0.f;
+                p.out[(hbase + h) * kDim + idx] = (uint16_t)(pack_bf16(acc[h] * inv, 0.f) & 0xFFFFu);
+                if (idx == h)
+                    p.lse[hbase + h] = (Mx[h] == -INFINITY) ? -INFINITY
+                                                             : (Mx[h] + log2f(Lx[h])) * 0.69314718055994531f;
             }
             if (sidx == 0)
                 p.counters[u] = 0; // ready for the next call
@@ -784,7 +817,7 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
                     fold(l_last);
                 if (!ok)
                     break;
-                finalize(cur_t, cur_g);
+                finalize(cur_t, cur_g, false);
                 if (!ok)
                     break;
             }
@@ -869,7 +902,7 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
         if (l_last >= 0)
             fold(l_last);
         if (ok)
-            finalize(cur_t, cur_g);
+            finalize(cur_t, cur_g, true);
     }
     if (!ok) {
         set_error(p.err, kErrTimeout);

@@ -216,6 +216,14 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int *addr, int v)
     return old;
 }
 
+// Load with acquire semantics at GPU scope.
+__device__ __forceinline__ int ld_acquire_gpu(const int *addr)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+    return v;
+}
+
 // ---- programmatic dependent launch ----------------------------------------
 
 // Block until the kernels this grid depends on have completed and their
