@@ -156,45 +156,44 @@ __device__ int4 make_entry(const DecodeParams &p, long long x, const int *qt)
 // 16 registers (one per head) once the next page's P^T is written.
 
 constexpr int kUSmxWarps = 8;              // softmax warps: two per TMEM lane quarter
-constexpr int kUCvtWarps = 4;              // FP8 only: E4M3 -> f16 converter warps
 constexpr int kUSoftmax = 32 * kUSmxWarps; // softmax threads
-template <bool FP8>
-constexpr int kUThreadsT = 32 * (2 + kUSmxWarps + (FP8 ? kUCvtWarps : 0)); // producer, MMA, softmax[, converters]
+constexpr int kUThreads = 32 * (2 + kUSmxWarps); // producer, MMA, softmax
+constexpr int kUQScales = 16;              // FP8: ring of per-unit query scales (> units in flight)
+constexpr float kPScale = 256.f;           // FP8: P^T is stored as 256 * P (E4M3 hi + lo)
 constexpr int kUHeads = 8;                 // heads per softmax thread (half of the group)
 constexpr int kUTmemCols = 64;             // S[2] + O[2], 16 columns each
 constexpr int kUTile = 32768;              // bf16 K or V tile of one (page, KV head)
-constexpr int kUQTile = 4096;              // 16 query rows of one unit, two 64-dim boxes
-constexpr int kUPTile = 4096;              // P^T of one page: [16 heads][128 tokens] bf16
+constexpr int kUQTile = 4096;              // 16 query rows of one unit: bf16 (two 64-dim boxes) or E4M3 hi + lo
+constexpr int kUPTile = 4096;              // P^T of one page, [16 heads][128 tokens]: bf16, or E4M3 hi + lo
 
 struct USmem {
-    size_t ring, stage, qbuf, pbuf, bars, table, xbuf, lbuf, misc, qt, total;
+    size_t ring, qbuf, pbuf, bars, table, xbuf, lbuf, qsc, misc, qt, total;
 };
 
-// bf16: the ring holds the MMA operands.  FP8: the ring holds E4M3 tiles
-// (16 KiB) and one f16 staging tile each for K and V feeds the MMA.
+// The ring holds the MMA operands as loaded: bf16 tiles (32 KiB) or E4M3
+// tiles (16 KiB, read by the FP8 MMA as they are).
 __host__ __device__ inline USmem umma_layout(int T, int stages, bool fp8)
 {
     USmem L{};
     size_t off = 0;
     L.ring = off;                          // 1024-aligned tiles
     off += (size_t)stages * (fp8 ? kUTile / 2 : kUTile);
-    L.stage = off = align_to(off, 1024);   // FP8: f16 tiles K[2], V
-    off += fp8 ? 3 * kUTile : 0;
     L.qbuf = off = align_to(off, 1024);    // [2] query tiles (swizzle atoms: 1024-aligned)
     off += 2 * kUQTile;
     L.pbuf = off = align_to(off, 1024);    // [2] P^T tiles
     off += 2 * kUPTile;
     // full[S], empty[S], qfull[2], qempty[2], s_full[2], s_free[2], p_full[2],
-    // p_free[2], o_full[2], o_free[2], softmax sync, done, then FP8 only:
-    // kst_full[2], kst_empty[2], vst_full, vst_empty, qconv[2]
+    // p_free[2], o_full[2], o_free[2], softmax sync, done
     L.bars = off = align_to(off, 8);
-    off += (size_t)(2 * stages + 16 + 2 + 8) * 8;
+    off += (size_t)(2 * stages + 16 + 2) * 8;
     L.table = off = align_to(off, 16);     // [2][kWin] int4
     off += (size_t)2 * kWin * 16;
     L.xbuf = off = align_to(off, 16);      // [2][4 quarters][16] page maxima
     off += 2 * 4 * 16 * 4;
     L.lbuf = off = align_to(off, 16);      // [4 quarters][16] denominators
     off += 4 * 16 * 4;
+    L.qsc = off = align_to(off, 16);       // FP8: [kUQScales] 1 / query scale of a unit
+    off += kUQScales * 4;
     L.misc = off = align_to(off, 16);      // tmem base, flags
     off += 16;
     L.qt = off = align_to(off, 16);        // [T + 1]
@@ -217,8 +216,29 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8])
         v[i] = __uint_as_float(r[i]);
 }
 
+// Two floats to E4M3 (round to nearest, saturating): a -> high byte, b -> low byte.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float a, float b)
+{
+    uint32_t out;
+    asm("{\n .reg .b16 t;\n cvt.rn.satfinite.e4m3x2.f32 t, %1, %2;\n cvt.u32.u16 %0, t;\n}\n"
+        : "=r"(out)
+        : "f"(a), "f"(b));
+    return out;
+}
+
+// x0, x1 as E4M3 pairs hi + lo with x - hi exact in fp32 and lo its rounding:
+// hi + lo carries 8 significant bits (bf16's) for values in E4M3's normal
+// range.  Returns (hi1 << 8 | hi0) and (lo1 << 8 | lo0).
+__device__ __forceinline__ void split_e4m3x2(float x0, float x1, uint32_t &hi, uint32_t &lo)
+{
+    hi = f32x2_to_e4m3x2(x1, x0);
+    float h0, h1;
+    f16x2_to_f32x2(e4m3x2_to_f16x2(hi), h0, h1);
+    lo = f32x2_to_e4m3x2(x1 - h1, x0 - h0);
+}
+
 template <bool FP8, int STAGES>
-__global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
+__global__ void __launch_bounds__(kUThreads, 1)
     sparse_decode_umma_kernel(const __grid_constant__ CUtensorMap kv_map,
                               const __grid_constant__ CUtensorMap q_map, const DecodeParams p)
 {
@@ -228,8 +248,6 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const USmem lay = umma_layout(p.T, STAGES, FP8);
     uint8_t *ring = base + lay.ring;
-    uint8_t *kst = base + lay.stage;        // FP8: [2] f16 K tiles
-    uint8_t *vst = kst + 2 * kUTile;        // FP8: f16 V tile
     uint8_t *qbuf = base + lay.qbuf;
     uint8_t *pbuf = base + lay.pbuf;
     uint64_t *full = reinterpret_cast<uint64_t *>(base + lay.bars);
@@ -244,11 +262,7 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
     uint64_t *o_free = o_full + 2;
     uint64_t *smx_bar = o_free + 2;    // softmax-warps barrier (kUSmxWarps arrivals)
     uint64_t *done_bar = smx_bar + 1;  // softmax warps finished with TMEM (kUSmxWarps arrivals)
-    uint64_t *kst_full = done_bar + 1; // FP8: [2] staging K converted (kUCvtWarps)
-    uint64_t *kst_empty = kst_full + 2; // FP8: [2] staging K read by the MMA (commit)
-    uint64_t *vst_full = kst_empty + 2;
-    uint64_t *vst_empty = vst_full + 1;
-    uint64_t *qconv = vst_empty + 1;   // FP8: [2] query tile widened to f16 (kUCvtWarps)
+    float *qscale = reinterpret_cast<float *>(base + lay.qsc);
     int4 *table = reinterpret_cast<int4 *>(base + lay.table);
     float *xbuf = reinterpret_cast<float *>(base + lay.xbuf);
     float *lbuf = reinterpret_cast<float *>(base + lay.lbuf);
@@ -264,16 +278,9 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
         prefetch_tensormap(&q_map);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&empty[s]), FP8 ? kUCvtWarps : 1);
+            mbar_init(smem_u32(&empty[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_u32(&kst_full[b]), kUCvtWarps);
-            mbar_init(smem_u32(&kst_empty[b]), 1);
-        }
-        mbar_init(smem_u32(vst_full), kUCvtWarps);
-        mbar_init(smem_u32(vst_empty), 1);
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_u32(&qconv[b]), kUCvtWarps);
             mbar_init(smem_u32(&qfull[b]), 1);
             mbar_init(smem_u32(&qempty[b]), 1);
             mbar_init(smem_u32(&s_full[b]), 1);
@@ -334,32 +341,82 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
             if (!ok)
                 break;
             // The softmax warps trail the MMA warp by up to two tasks and the MMA
-            // warp trails this one by up to kAhead (kAhead + 2 with the FP8
-            // converters, which run a K tile ahead of the V tile, between
-            // them): only kAhead + 3 (+ 2) tasks into a window has every
-            // reader left the window before it.
-            if (l % kWin == kAhead + 3 + (FP8 ? 2 : 0) && l >= kWin && (l / kWin + 1) * kWin < ntasks)
+            // warp trails this one by up to kAhead: only kAhead + 3 tasks into
+            // a window has every reader left the window before it.
+            if (l % kWin == kAhead + 3 && l >= kWin && (l / kWin + 1) * kWin < ntasks)
                 fill_window(l / kWin + 1);
-            if (lane == 0) {
-                const int4 e = entry(l);
-                const int u = unit_of(e);
-                if (u != prod_last) {
-                    prod_last = u;
-                    const int qb = prod_units & 1;
-                    if (prod_units >= 2)
-                        ok = mbar_wait_or_abort(smem_u32(&qempty[qb]), ((prod_units >> 1) - 1) & 1,
-                                                abort_flag);
-                    if (ok) {
+            const int4 e = entry(l);
+            const int u = unit_of(e);
+            if (u != prod_last) {
+                // the unit's 16 query rows into query buffer qb
+                prod_last = u;
+                const int qb = prod_units & 1;
+                if (lane == 0 && prod_units >= 2)
+                    ok = mbar_wait_or_abort(smem_u32(&qempty[qb]), ((prod_units >> 1) - 1) & 1, abort_flag);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok)
+                    break;
+                const int row = (e.z * p.Hkv + e.w) * kGroup;
+                if (!FP8) {
+                    if (lane == 0) {
                         const uint32_t qbar = smem_u32(&qfull[qb]);
                         const uint32_t dst = smem_u32(qbuf + qb * kUQTile);
-                        const int row = (e.z * p.Hkv + e.w) * kGroup;
                         mbar_arrive_expect_tx(qbar, kUQTile);
                         tma_load_2d(dst, &q_map, 0, row, qbar);
                         tma_load_2d(dst + kUQTile / 2, &q_map, 64, row, qbar);
                         q_issued = prod_units + 1;
                     }
-                    ++prod_units;
+                } else {
+                    // E4M3 hi + lo tiles of s * q (K-major, 128-byte swizzle),
+                    // s = 2^k with max |s q| in [128, 256): lane = (row, 64 dims)
+                    const int r = lane >> 1, hf = lane & 1;
+                    const uint4 *src = reinterpret_cast<const uint4 *>(p.q + (size_t)(row + r) * kDim + hf * 64);
+                    uint4 v[8];
+                    float mx = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        v[i] = __ldg(src + i);
+                        const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w4[j] << 16)),
+                                                 fabsf(__uint_as_float(w4[j] & 0xFFFF0000u))));
+                    }
+                    mx = warp_max_f32(mx);
+                    int k = 0;
+                    if (mx > 0.f && mx < INFINITY) {
+                        k = 7 - ((int)((__float_as_uint(mx) >> 23) & 0xFFu) - 127);
+                        k = k < -100 ? -100 : (k > 100 ? 100 : k);
+                    }
+                    const float sq = __uint_as_float((uint32_t)(127 + k) << 23);
+                    uint8_t *qhi = qbuf + qb * kUQTile, *qlo = qhi + kUQTile / 2;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) { // 16 dims = one 16-byte chunk of E4M3
+                        uint32_t hw[4], lw[4];
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) { // 4 dims = 2 words of the bf16 input
+                            const int i = 2 * j + (w >> 1);
+                            const uint32_t a = (&v[i].x)[2 * (w & 1)], b = (&v[i].x)[2 * (w & 1) + 1];
+                            uint32_t h01, l01, h23, l23;
+                            split_e4m3x2(__uint_as_float(a << 16) * sq, __uint_as_float(a & 0xFFFF0000u) * sq, h01, l01);
+                            split_e4m3x2(__uint_as_float(b << 16) * sq, __uint_as_float(b & 0xFFFF0000u) * sq, h23, l23);
+                            hw[w] = h01 | (h23 << 16);
+                            lw[w] = l01 | (l23 << 16);
+                        }
+                        const int off = r * 128 + (((4 * hf + j) ^ (r & 7)) << 4);
+                        *reinterpret_cast<uint4 *>(qhi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        *reinterpret_cast<uint4 *>(qlo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    }
+                    if (lane == 0)
+                        qscale[prod_units % kUQScales] = __uint_as_float((uint32_t)(127 - k) << 23);
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(smem_u32(&qfull[qb]));
                 }
+                ++prod_units;
+            }
+            if (lane == 0) {
                 for (int kv = 0; kv < 2 && ok; ++kv) {
                     const int z = zk + kv;
                     const int st = z % STAGES;
@@ -375,11 +432,11 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
                         continue;
                     }
                     const uint32_t dst = smem_u32(ring + (size_t)st * kRaw);
-                    const int row = e.x + kv * p.Hkv * kPage;
+                    const int krow = e.x + kv * p.Hkv * kPage;
                     mbar_arrive_expect_tx(bar, kRaw);
-                    tma_load_2d(dst, &kv_map, 0, row, bar);
+                    tma_load_2d(dst, &kv_map, 0, krow, bar);
                     if (!FP8)
-                        tma_load_2d(dst + kUTile / 2, &kv_map, 64, row, bar);
+                        tma_load_2d(dst + kUTile / 2, &kv_map, 64, krow, bar);
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -399,24 +456,23 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
         // =================== MMA issuer (lane 0) ===================
         // S^T(l + 1) is issued before P^T(l) is awaited, so the tensor core
         // works on the next page while the softmax warps work on this one.
-        // bf16 operands, or f16 for FP8 KV (widened E4M3, f16 Q and P)
-        constexpr uint32_t kF16 = FP8 ? ~((7u << 7) | (7u << 10)) : ~0u;
-        constexpr uint32_t kIdescS = umma_idesc_bf16(128, 16, 0, 0) & kF16; // K and Q^T both K-major
-        constexpr uint32_t kIdescO = umma_idesc_bf16(128, 16, 1, 0) & kF16; // V^T MN-major, P^T K-major
+        // bf16: kind::f16, 8 steps of K = 16.  FP8: kind::f8f6f4 on the E4M3
+        // tiles as loaded, 4 steps of K = 32 for each of the hi and lo parts
+        // of Q (in S^T) and of P (in O^T); operand types E4M3 = 0.
+        constexpr uint32_t kE4M3 = FP8 ? ~((7u << 7) | (7u << 10)) : ~0u;
+        constexpr uint32_t kIdescS = umma_idesc_bf16(128, 16, 0, 0) & kE4M3; // K and Q^T both K-major
+        constexpr uint32_t kIdescO = umma_idesc_bf16(128, 16, 1, 0) & kE4M3; // V^T MN-major, P^T K-major
         bool ok = true;
         if (lane == 0) {
             int s_units = 0, s_unit = -1;
             auto issue_s = [&](int l) -> bool {
                 const int zk = 2 * l, b = l & 1;
-                if (!FP8 && !mbar_wait_or_abort(smem_u32(&full[zk % STAGES]), (zk / STAGES) & 1, abort_flag))
-                    return false;
-                if (FP8 && !mbar_wait_or_abort(smem_u32(&kst_full[b]), (l >> 1) & 1, abort_flag))
+                if (!mbar_wait_or_abort(smem_u32(&full[zk % STAGES]), (zk / STAGES) & 1, abort_flag))
                     return false;
                 const int4 e = entry(l);
                 const int u = unit_of(e);
                 if (u != s_unit) {
-                    uint64_t *qb_bar = FP8 ? qconv : qfull;
-                    if (!mbar_wait_or_abort(smem_u32(&qb_bar[s_units & 1]), (s_units >> 1) & 1, abort_flag))
+                    if (!mbar_wait_or_abort(smem_u32(&qfull[s_units & 1]), (s_units >> 1) & 1, abort_flag))
                         return false;
                     s_unit = u;
                     ++s_units;
@@ -426,17 +482,23 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
                     return false;
                 tcgen05_after_sync();
                 if (e.x >= 0) {
-                    const uint32_t tileK = FP8 ? smem_u32(kst + b * kUTile) : smem_u32(ring + (size_t)(zk % STAGES) * kRaw);
+                    const uint32_t tileK = smem_u32(ring + (size_t)(zk % STAGES) * kRaw);
                     const uint32_t qtile = smem_u32(qbuf + qb * kUQTile);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
-                        const uint64_t a = umma_desc_sw128(tileK + (ks >> 2) * (kUTile / 2) + (ks & 3) * 32, 16, 1024);
-                        const uint64_t bq = umma_desc_sw128(qtile + (ks >> 2) * (kUQTile / 2) + (ks & 3) * 32, 16, 1024);
-                        umma_bf16(tmem + 16 * b, a, bq, kIdescS, ks > 0);
+                        if (!FP8) {
+                            const uint64_t a = umma_desc_sw128(tileK + (ks >> 2) * (kUTile / 2) + (ks & 3) * 32, 16, 1024);
+                            const uint64_t bq = umma_desc_sw128(qtile + (ks >> 2) * (kUQTile / 2) + (ks & 3) * 32, 16, 1024);
+                            umma_bf16(tmem + 16 * b, a, bq, kIdescS, ks > 0);
+                        } else { // steps 0..3: Q hi, 4..7: Q lo; 32 dims (bytes) per step
+                            const uint64_t a = umma_desc_sw128(tileK + (ks & 3) * 32, 16, 1024);
+                            const uint64_t bq = umma_desc_sw128(qtile + (ks >> 2) * (kUQTile / 2) + (ks & 3) * 32, 16, 1024);
+                            umma_f8(tmem + 16 * b, a, bq, kIdescS, ks > 0);
+                        }
                     }
                 }
                 umma_commit(smem_u32(&s_full[b]));
-                umma_commit(FP8 ? smem_u32(&kst_empty[b]) : smem_u32(&empty[zk % STAGES])); // K tile read
+                umma_commit(smem_u32(&empty[zk % STAGES])); // K tile read
                 // last task of its unit: the query tile can be replaced
                 if (l + 1 == ntasks || unit_of(entry(l + 1)) != u)
                     umma_commit(smem_u32(&qempty[qb]));
@@ -444,9 +506,7 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
             };
             auto issue_pv = [&](int l) -> bool {
                 const int zv = 2 * l + 1, b = l & 1;
-                if (!FP8 && !mbar_wait_or_abort(smem_u32(&full[zv % STAGES]), (zv / STAGES) & 1, abort_flag))
-                    return false;
-                if (FP8 && !mbar_wait_or_abort(smem_u32(vst_full), l & 1, abort_flag))
+                if (!mbar_wait_or_abort(smem_u32(&full[zv % STAGES]), (zv / STAGES) & 1, abort_flag))
                     return false;
                 if (!mbar_wait_or_abort(smem_u32(&p_full[b]), (l >> 1) & 1, abort_flag))
                     return false;
@@ -454,20 +514,28 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
                     return false;
                 tcgen05_after_sync();
                 if (entry(l).x >= 0) {
-                    const uint32_t tileV = FP8 ? smem_u32(vst) : smem_u32(ring + (size_t)(zv % STAGES) * kRaw);
+                    const uint32_t tileV = smem_u32(ring + (size_t)(zv % STAGES) * kRaw);
                     const uint32_t ptile = smem_u32(pbuf + b * kUPTile);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
-                        // V^T, MN-major: 16 tokens per k-step = 16 rows of 128 bytes;
-                        // the two 64-dim halves of a row are 16 KiB apart (LBO)
-                        const uint64_t a = umma_desc_sw128(tileV + ks * 2048, kUTile / 2, 1024);
-                        const uint64_t bp = umma_desc_sw128(ptile + (ks >> 2) * (kUPTile / 2) + (ks & 3) * 32, 16, 1024);
-                        umma_bf16(tmem + 32 + 16 * b, a, bp, kIdescO, ks > 0);
+                        if (!FP8) {
+                            // V^T, MN-major: 16 tokens per k-step = 16 rows of 128 bytes;
+                            // the two 64-dim halves of a row are 16 KiB apart (LBO)
+                            const uint64_t a = umma_desc_sw128(tileV + ks * 2048, kUTile / 2, 1024);
+                            const uint64_t bp = umma_desc_sw128(ptile + (ks >> 2) * (kUPTile / 2) + (ks & 3) * 32, 16, 1024);
+                            umma_bf16(tmem + 32 + 16 * b, a, bp, kIdescO, ks > 0);
+                        } else {
+                            // V^T, MN-major: 32 tokens per k-step = 32 rows of 128 bytes
+                            // (all 128 dims in one swizzle atom); steps 0..3: P hi, 4..7: P lo
+                            const uint64_t a = umma_desc_sw128(tileV + (ks & 3) * 4096, kUTile / 2, 1024);
+                            const uint64_t bp = umma_desc_sw128(ptile + (ks >> 2) * (kUPTile / 2) + (ks & 3) * 32, 16, 1024);
+                            umma_f8(tmem + 32 + 16 * b, a, bp, kIdescO, ks > 0);
+                        }
                     }
                 }
                 umma_commit(smem_u32(&o_full[b]));
                 umma_commit(smem_u32(&p_free[b]));
-                umma_commit(FP8 ? smem_u32(vst_empty) : smem_u32(&empty[zv % STAGES])); // V tile read
+                umma_commit(smem_u32(&empty[zv % STAGES])); // V tile read
                 return true;
             };
             if (ntasks > 0)
@@ -491,107 +559,6 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
         __syncwarp();
         tcgen05_after_sync();
         tmem_dealloc(tmem, kUTmemCols);
-        return;
-    }
-
-    if (FP8 && warp >= 2 + kUSmxWarps) {
-        // =================== converter warps (FP8) ===================
-        // E4M3 K / V tiles from the ring into the f16 staging tiles, in the
-        // two-64-dim-box, 128-byte-swizzled layout the MMA descriptors read;
-        // the query tile of each new unit is widened from bf16 to f16 in place.
-        const int ct = threadIdx.x - 32 * (2 + kUSmxWarps); // 0..127
-        bool ok = true;
-        int units = 0, cur = -1;
-        // Thread ct widens the 16-byte chunk c = ct % 8 (16 dims) of rows
-        // ct / 8 + 16 i, i < 8: all eight loads are issued before the first
-        // convert, so the converts of different rows overlap.
-        const int cch = ct & 7, r0 = ct >> 3, sw = r0 & 7; // r & 7 == sw for every row of the thread
-        auto convert = [&](const uint8_t *raw, uint8_t *dst) {
-            uint4 w[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                w[i] = *reinterpret_cast<const uint4 *>(raw + (r0 + 16 * i) * 128 + ((cch ^ sw) << 4));
-            const int c0 = 2 * (cch & 3); // first f16 chunk in the 64-dim box cch / 4
-            uint8_t *col_lo = dst + (cch >> 2) * (kUTile / 2) + ((c0 ^ sw) << 4);
-            uint8_t *col_hi = dst + (cch >> 2) * (kUTile / 2) + (((c0 + 1) ^ sw) << 4);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                uint4 lo, hi;
-                e4m3x4_to_f16x2x2(w[i].x, lo.x, lo.y);
-                e4m3x4_to_f16x2x2(w[i].y, lo.z, lo.w);
-                e4m3x4_to_f16x2x2(w[i].z, hi.x, hi.y);
-                e4m3x4_to_f16x2x2(w[i].w, hi.z, hi.w);
-                *reinterpret_cast<uint4 *>(col_lo + (r0 + 16 * i) * 128) = lo;
-                *reinterpret_cast<uint4 *>(col_hi + (r0 + 16 * i) * 128) = hi;
-            }
-            fence_async_smem();
-        };
-        // K(l + 1) is widened before V(l): the MMA warp issues S(l + 1)
-        // before O(l), and K has two staging tiles, V one.
-        auto do_k = [&](int l) -> bool {
-            const int zk = 2 * l, kb = l & 1;
-            if (!mbar_wait_or_abort(smem_u32(&full[zk % STAGES]), (zk / STAGES) & 1, abort_flag))
-                return false;
-            const int4 e = entry(l);
-            const int u = unit_of(e);
-            if (u != cur) {
-                const int qb = units & 1;
-                if (!mbar_wait_or_abort(smem_u32(&qfull[qb]), (units >> 1) & 1, abort_flag))
-                    return false;
-                uint8_t *q = qbuf + qb * kUQTile;
-                for (int i = ct; i < kUQTile / 16; i += 32 * kUCvtWarps) {
-                    uint4 v = reinterpret_cast<uint4 *>(q)[i];
-                    v.x = bf16x2_to_f16x2(v.x);
-                    v.y = bf16x2_to_f16x2(v.y);
-                    v.z = bf16x2_to_f16x2(v.z);
-                    v.w = bf16x2_to_f16x2(v.w);
-                    reinterpret_cast<uint4 *>(q)[i] = v;
-                }
-                fence_async_smem();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(smem_u32(&qconv[qb]));
-                cur = u;
-                ++units;
-            }
-            if (l >= 2 && !mbar_wait_or_abort(smem_u32(&kst_empty[kb]), ((l >> 1) - 1) & 1, abort_flag))
-                return false;
-            if (e.x >= 0)
-                convert(ring + (size_t)(zk % STAGES) * kRaw, kst + kb * kUTile);
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(smem_u32(&kst_full[kb]));
-                mbar_arrive(smem_u32(&empty[zk % STAGES]));
-            }
-            return true;
-        };
-        auto do_v = [&](int l) -> bool {
-            const int zv = 2 * l + 1;
-            if (!mbar_wait_or_abort(smem_u32(&full[zv % STAGES]), (zv / STAGES) & 1, abort_flag))
-                return false;
-            if (l >= 1 && !mbar_wait_or_abort(smem_u32(vst_empty), (l - 1) & 1, abort_flag))
-                return false;
-            if (entry(l).x >= 0)
-                convert(ring + (size_t)(zv % STAGES) * kRaw, vst);
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(smem_u32(vst_full));
-                mbar_arrive(smem_u32(&empty[zv % STAGES]));
-            }
-            return true;
-        };
-        if (ntasks > 0)
-            ok = do_k(0);
-        for (int l = 0; l < ntasks && ok; ++l) {
-            if (l + 1 < ntasks)
-                ok = do_k(l + 1);
-            if (ok)
-                ok = do_v(l);
-        }
-        if (!ok) {
-            set_error(p.err, kErrTimeout);
-            *abort_flag = 1;
-        }
         return;
     }
 
@@ -691,7 +658,7 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
             }
 #pragma unroll
         for (int h = 0; h < kUHeads; ++h)
-            o[h] *= p.v_scale; // 1 for bf16 values
+            o[h] *= FP8 ? p.v_scale / kPScale : p.v_scale; // 1 for bf16 values
         if (whole) {
 #pragma unroll
             for (int h = 0; h < kUHeads; ++h) {
@@ -792,7 +759,8 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
         ssync(); // s_flag is reused by the next unit
     };
 
-    int l_last = -1;
+    int l_last = -1, sm_units = 0;
+    float unit_scale = p.scale_log2; // logits to base 2 (FP8: / the unit's query scale)
     for (int l = 0; l < ntasks && ok; ++l) {
         const int b = l & 1;
         if (!mbar_wait_or_abort(smem_u32(&s_full[b]), (l >> 1) & 1, abort_flag)) {
@@ -826,6 +794,11 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
             cur_g = e.w;
             reset();
             l_last = -1;
+            // the producer wrote the unit's query scale before the Q tile it
+            // made, which S^T of this page waited for
+            if (FP8)
+                unit_scale = p.scale_log2 * qscale[sm_units % kUQScales];
+            ++sm_units;
         }
 
         // page maxima per head (log2 domain) across the 128 tokens
@@ -833,7 +806,7 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
         float wmax[kUHeads];
 #pragma unroll
         for (int h = 0; h < kUHeads; ++h) {
-            sv[h] = visible ? sv[h] * p.scale_log2 : -INFINITY;
+            sv[h] = visible ? sv[h] * unit_scale : -INFINITY;
             wmax[h] = warp_max_f32(sv[h]);
         }
         if (lane == 0) {
@@ -869,15 +842,31 @@ __global__ void __launch_bounds__(kUThreadsT<FP8>, 1)
             ok = false;
             break;
         }
-        if (live) {
+        if (live && !FP8) {
             uint8_t *pt = pbuf + b * kUPTile + (idx >> 6) * (kUPTile / 2);
             const int col = idx & 63;
 #pragma unroll
             for (int h = 0; h < kUHeads; ++h) {
                 const int hh = h0 + h;
                 const uint32_t off = hh * 128 + ((((col >> 3) ^ (hh & 7))) << 4) + (col & 7) * 2;
-                const uint32_t pk = FP8 ? pack_f16(pv[h], 0.f) : pack_bf16(pv[h], 0.f);
-                *reinterpret_cast<uint16_t *>(pt + off) = (uint16_t)(pk & 0xFFFFu);
+                *reinterpret_cast<uint16_t *>(pt + off) = (uint16_t)(pack_bf16(pv[h], 0.f) & 0xFFFFu);
+            }
+            fence_async_smem();
+        } else if (live) {
+            // FP8: 256 P as E4M3 hi + lo, one byte per (head row, token) in
+            // each of two K-major tiles of 16 rows x 128 bytes
+            uint8_t *phi = pbuf + b * kUPTile, *plo = phi + kUPTile / 2;
+#pragma unroll
+            for (int h = 0; h < kUHeads; h += 2) {
+                uint32_t hi, lo;
+                split_e4m3x2(pv[h] * kPScale, pv[h + 1] * kPScale, hi, lo);
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int hh = h0 + h + k;
+                    const uint32_t off = hh * 128 + ((((idx >> 4) ^ (hh & 7))) << 4) + (idx & 15);
+                    phi[off] = (uint8_t)(hi >> (8 * k));
+                    plo[off] = (uint8_t)(lo >> (8 * k));
+                }
             }
             fence_async_smem();
         }
@@ -980,7 +969,7 @@ cudaError_t launch_umma_t(const DecodeParams &p, const CUtensorMap &kv, const CU
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
-    e = launch_kernel(sparse_decode_umma_kernel<FP8, STAGES>, dim3(ctas), dim3(kUThreadsT<FP8>), smem,
+    e = launch_kernel(sparse_decode_umma_kernel<FP8, STAGES>, dim3(ctas), dim3(kUThreads), smem,
                       stream, pdl, kv, qm, p);
     if (e != cudaSuccess)
         return e;
@@ -1014,9 +1003,9 @@ cudaError_t launch_sparse_decode(const DecodeParams &p, const void *kv_pool, int
     if (!encode_q_map(&qmap, p.q, p.T, p.Hkv))
         return cudaErrorInvalidValue;
     if (kv_dtype == MSA_FP8_E4M3) {
-        if (umma_layout(p.T, 6, true).total <= (size_t)kMaxSmem)
-            return launch_umma_t<true, 6>(p, map, qmap, ctas, stream, pdl);
-        return launch_umma_t<true, 4>(p, map, qmap, ctas, stream, pdl);
+        if (umma_layout(p.T, 12, true).total <= (size_t)kMaxSmem)
+            return launch_umma_t<true, 12>(p, map, qmap, ctas, stream, pdl);
+        return launch_umma_t<true, 6>(p, map, qmap, ctas, stream, pdl);
     }
     if (umma_layout(p.T, 6, false).total <= (size_t)kMaxSmem)
         return launch_umma_t<false, 6>(p, map, qmap, ctas, stream, pdl);

@@ -376,6 +376,17 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
         : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem], 8-bit operands (kind::f8f6f4), issued by one thread.
+__device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on the mbarrier when every tcgen05 operation this thread
 // issued so far has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar)
@@ -429,6 +440,14 @@ __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t &lo, uint
         " cvt.rn.f16x2.e4m3x2 %1, b;\n}\n"
         : "=r"(lo), "=r"(hi)
         : "r"(w));
+}
+
+// f16x2 to two floats (lo = lower half).  Exact.
+__device__ __forceinline__ void f16x2_to_f32x2(uint32_t v, float &lo, float &hi)
+{
+    asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n cvt.f32.f16 %0, a;\n cvt.f32.f16 %1, b;\n}\n"
+        : "=f"(lo), "=f"(hi)
+        : "r"(v));
 }
 
 // Two E2M1 codes in one byte (low nibble -> low half) to f16x2.  Exact.
