@@ -330,6 +330,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
     if (warp == 0) {
         // =================== producer ===================
         constexpr int kAhead = STAGES / 2;
+        const uint64_t kv_policy = l2_evict_first_policy(); // pages are streamed
         int issued = 0, q_issued = 0, prod_units = 0, prod_last = -1;
         bool ok = true;
         for (int l = 0; l < ntasks && ok; ++l) {
@@ -434,9 +435,9 @@ __global__ void __launch_bounds__(kUThreads, 1)
                     const uint32_t dst = smem_u32(ring + (size_t)st * kRaw);
                     const int krow = e.x + kv * p.Hkv * kPage;
                     mbar_arrive_expect_tx(bar, kRaw);
-                    tma_load_2d(dst, &kv_map, 0, krow, bar);
+                    tma_load_2d_hint(dst, &kv_map, 0, krow, bar, kv_policy);
                     if (!FP8)
-                        tma_load_2d(dst + kUTile / 2, &kv_map, 64, krow, bar);
+                        tma_load_2d_hint(dst + kUTile / 2, &kv_map, 64, krow, bar, kv_policy);
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);

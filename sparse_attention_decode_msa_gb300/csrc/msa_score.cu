@@ -390,6 +390,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
 
     if (warp == 0) {
         // =================== producer ===================
+        const uint64_t k_policy = l2_evict_first_policy(); // index-key pages are streamed
         bool ok = true;
         int units = 0, last_r = -1, issued = 0, q_issued = 0;
         for (int l0 = 0; l0 < n && ok; l0 += 32) {
@@ -433,8 +434,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
                         const uint32_t bar = smem_u32(&full[slot]);
                         const uint32_t dst = smem_u32(ring + (size_t)slot * kSTile);
                         mbar_arrive_expect_tx(bar, kSTile);
-                        tma_load_2d(dst, &k_map, 0, pg * kPage, bar);
-                        tma_load_2d(dst + kSTile / 2, &k_map, 64, pg * kPage, bar);
+                        tma_load_2d_hint(dst, &k_map, 0, pg * kPage, bar, k_policy);
+                        tma_load_2d_hint(dst + kSTile / 2, &k_map, 64, pg * kPage, bar, k_policy);
                         issued = l + 1;
                     }
                 }
@@ -665,6 +666,7 @@ __global__ void __launch_bounds__(kF4Threads, 1) index_score_fp4_kernel(const Sc
 
     if (warp == 0) {
         // =================== producer ===================
+        const uint64_t k_policy = l2_evict_first_policy(); // index-key pages are streamed
         bool ok = true;
         int issued = 0;
         for (int l0 = 0; l0 < n && ok; l0 += 32) {
@@ -690,8 +692,8 @@ __global__ void __launch_bounds__(kF4Threads, 1) index_score_fp4_kernel(const Sc
                         const uint32_t bar = smem_u32(&full[slot]);
                         const uint32_t dst = smem_u32(ring + (size_t)slot * kF4Stage);
                         mbar_arrive_expect_tx(bar, kF4Stage);
-                        bulk_load(dst, p.idxk + (size_t)pg * kF4Codes, kF4Codes, bar);
-                        bulk_load(dst + kF4Codes, p.scales + (size_t)pg * kF4Scales, kF4Scales, bar);
+                        bulk_load_hint(dst, p.idxk + (size_t)pg * kF4Codes, kF4Codes, bar, k_policy);
+                        bulk_load_hint(dst + kF4Codes, p.scales + (size_t)pg * kF4Scales, kF4Scales, bar, k_policy);
                         issued = l + 1;
                     }
                 }
