@@ -42,10 +42,14 @@ class OracleShape(ctypes.Structure):
         ("softmax_scale", ctypes.c_double),
         ("k_scale", ctypes.c_double),
         ("v_scale", ctypes.c_double),
+        ("num_index_heads", ctypes.c_int32),
+        ("init_blocks", ctypes.c_int32),
+        ("local_blocks", ctypes.c_int32),
     ]
 
 
-ERRORS = {1: "page id out of range", 2: "bad seq_len", 3: "bad selection", 4: "out of memory"}
+ERRORS = {1: "page id out of range", 2: "bad seq_len", 3: "bad selection", 4: "out of memory",
+          5: "bad shape"}
 
 
 class OracleError(RuntimeError):
@@ -80,9 +84,14 @@ def lib():
         L.oracle_e2m1.restype = ctypes.c_double
         L.oracle_e2m1.argtypes = [ctypes.c_uint8]
         L.oracle_block_scores.restype = ctypes.c_int
-        L.oracle_block_scores.argtypes = [ctypes.POINTER(OracleShape), p, p, p, p, p, ctypes.c_int, p]
+        L.oracle_block_scores.argtypes = [ctypes.POINTER(OracleShape), p, p, p, p, p, ctypes.c_int,
+                                          ctypes.c_int, p]
         L.oracle_select.restype = ctypes.c_int
         L.oracle_select.argtypes = [p, ctypes.c_int, ctypes.c_int, p]
+        L.oracle_select_forced.restype = ctypes.c_int
+        L.oracle_select_forced.argtypes = [p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, p]
+        L.oracle_reduce_heads.restype = None
+        L.oracle_reduce_heads.argtypes = [ctypes.POINTER(OracleShape), p, ctypes.c_int, p]
         L.oracle_attend.restype = ctypes.c_int
         L.oracle_attend.argtypes = [ctypes.POINTER(OracleShape), p, p, p, p, ctypes.c_int, p, p, p]
         L.oracle_decode_step.restype = ctypes.c_int
@@ -105,7 +114,14 @@ def shape_of(pb) -> OracleShape:
         page_size=pb.kv_pool.shape[3], num_pages=pb.num_pages, max_blocks=pb.max_blocks,
         topk=pb.topk, kv_fp8=int(pb.kv_dtype == "fp8"), index_nvfp4=int(pb.index_dtype == "nvfp4"),
         softmax_scale=pb.softmax_scale, k_scale=pb.k_scale, v_scale=pb.v_scale,
+        num_index_heads=pb.num_index_heads, init_blocks=pb.init_blocks,
+        local_blocks=pb.local_blocks,
     )
+
+
+def selection_heads(pb) -> int:
+    """Tables per token: 1 with one index head, else one per KV head."""
+    return 1 if pb.num_index_heads == 1 else pb.num_kv_heads
 
 
 def _check(rc):
@@ -129,29 +145,47 @@ def e2m1(nibble) -> float:
     return lib().oracle_e2m1(int(nibble))
 
 
-def block_scores(pb, t: int) -> np.ndarray:
-    """float64 [max_blocks] per-block max index scores of token t."""
+def block_scores(pb, t: int, head: int = 0) -> np.ndarray:
+    """float64 [max_blocks] per-block max index scores of token t, index head `head`."""
     s = shape_of(pb)
     out = np.empty(pb.max_blocks, dtype=np.float64)
     arrs = [_c(pb.q_idx), _c(pb.idxk_pool), _c(pb.idxk_scales), _c(pb.block_table), _c(pb.seq_lens)]
-    _check(lib().oracle_block_scores(ctypes.byref(s), *[_ptr(a) for a in arrs], int(t), _ptr(out)))
+    _check(lib().oracle_block_scores(ctypes.byref(s), *[_ptr(a) for a in arrs], int(t), int(head),
+                                     _ptr(out)))
     return out
 
 
-def select(scores, n_valid: int, k: int) -> np.ndarray:
-    """int32 [k] top-k block table (ascending, -1 padded) of a score row."""
+def select(scores, n_valid: int, k: int, init: int = 0, local: int = 0) -> np.ndarray:
+    """int32 [k] top-k block table (ascending, -1 padded) of a score row,
+    keeping the first `init` and the last `local` of the n_valid blocks."""
     sc = np.ascontiguousarray(scores, dtype=np.float64)
     sel = np.empty(k, dtype=np.int32)
-    _check(lib().oracle_select(_ptr(sc), int(n_valid), int(k), _ptr(sel)))
+    if init == 0 and local == 0:
+        _check(lib().oracle_select(_ptr(sc), int(n_valid), int(k), _ptr(sel)))
+    else:
+        _check(lib().oracle_select_forced(_ptr(sc), int(n_valid), int(k), int(init), int(local),
+                                          _ptr(sel)))
     return sel
 
 
+def reduce_heads(pb, scores_by_head, gs: int) -> np.ndarray:
+    """float64 [max_blocks]: the scores of selection head gs from [Hi, max_blocks]."""
+    s = shape_of(pb)
+    sc = np.ascontiguousarray(scores_by_head, dtype=np.float64)
+    if sc.shape != (pb.num_index_heads, pb.max_blocks):
+        raise ValueError("scores must be [num_index_heads, max_blocks]")
+    out = np.empty(pb.max_blocks, dtype=np.float64)
+    lib().oracle_reduce_heads(ctypes.byref(s), _ptr(sc), int(gs), _ptr(out))
+    return out
+
+
 def attend(pb, t: int, sel) -> tuple[np.ndarray, np.ndarray]:
-    """(out float64 [Hq, D], lse float64 [Hq]) of token t over selection sel."""
+    """(out float64 [Hq, D], lse float64 [Hq]) of token t over its tables
+    sel ([topk] with one table, else [Hs, topk])."""
     s = shape_of(pb)
     sel = np.ascontiguousarray(sel, dtype=np.int32)
-    if sel.shape[0] != pb.topk:
-        raise ValueError("selection must have topk entries")
+    if sel.size != selection_heads(pb) * pb.topk:
+        raise ValueError("selection must have Hs x topk entries")
     out = np.empty((pb.num_q_heads, pb.q.shape[-1]), dtype=np.float64)
     lse = np.empty(pb.num_q_heads, dtype=np.float64)
     arrs = [_c(pb.q), _c(pb.kv_pool), _c(pb.block_table), _c(pb.seq_lens)]
@@ -163,22 +197,27 @@ def attend(pb, t: int, sel) -> tuple[np.ndarray, np.ndarray]:
 def decode_step(pb, tokens=None, threads: int = 1) -> dict:
     """Run the whole step for the given tokens (default: all).
 
-    Returns block_scores float32 [n, max_blocks], selected int32 [n, topk],
-    out float64 [n, Hq, D], lse float64 [n, Hq], tokens int32 [n].
+    Returns block_scores float32 [n, max_blocks] ([n, Hi, max_blocks] with
+    several index heads), selected int32 [n, topk] ([n, Hs, topk] with
+    several index heads), out float64 [n, Hq, D], lse float64 [n, Hq],
+    tokens int32 [n].
     """
     if tokens is None:
         tokens = np.arange(pb.num_tokens, dtype=np.int32)
     tokens = np.ascontiguousarray(tokens, dtype=np.int32)
     n = int(tokens.shape[0])
     s = shape_of(pb)
-    bs = np.empty((n, pb.max_blocks), dtype=np.float32)
-    sel = np.empty((n, pb.topk), dtype=np.int32)
+    Hi, Hs = pb.num_index_heads, selection_heads(pb)
+    bs = np.empty((n, Hi, pb.max_blocks), dtype=np.float32)
+    sel = np.empty((n, Hs, pb.topk), dtype=np.int32)
     out = np.empty((n, pb.num_q_heads, pb.q.shape[-1]), dtype=np.float64)
     lse = np.empty((n, pb.num_q_heads), dtype=np.float64)
     arrs = [_c(pb.q_idx), _c(pb.idxk_pool), _c(pb.idxk_scales), _c(pb.q), _c(pb.kv_pool),
             _c(pb.block_table), _c(pb.seq_lens)]
     _check(lib().oracle_decode_step(ctypes.byref(s), *[_ptr(a) for a in arrs], _ptr(tokens), n,
                                     int(threads), _ptr(bs), _ptr(sel), _ptr(out), _ptr(lse)))
+    if Hi == 1:
+        bs, sel = bs[:, 0], sel[:, 0]
     return {"block_scores": bs, "selected": sel, "out": out, "lse": lse, "tokens": tokens}
 
 

@@ -25,15 +25,16 @@
  * Everything is computed in double precision with plain loops, one token at
  * a time, in the order the definition states.  No blocking, no fusion.
  *
- * Layouts are those of the synthetic-input module (row-major, Hi = 1 index
- * head):
- *   q_idx       bf16 bits  [T][Di]
- *   idxk_pool   bf16 bits  [pages][P][Di]      or NVFP4 bytes [pages][P][Di/2]
- *   idxk_scales E4M3 codes [pages][P][Di/16]   (NVFP4 only)
+ * Layouts are those of the synthetic-input module (row-major; Hi index
+ * heads, Hs selection heads: Hs = 1 when Hi = 1, else Hs = Hkv):
+ *   q_idx       bf16 bits  [T][Hi][Di]
+ *   idxk_pool   bf16 bits  [pages][Hi][P][Di]  or NVFP4 bytes [pages][Hi][P][Di/2]
+ *   idxk_scales E4M3 codes [pages][Hi][P][Di/16]   (NVFP4 only)
  *   q           bf16 bits  [T][Hq][D]
  *   kv_pool     bf16 bits or E4M3 codes [pages][2][Hkv][P][D]  (K then V)
  *   block_table int32      [R][max_blocks]
  *   seq_lens    int32      [R]
+ *   selected    int32      [T][Hs][topk]
  */
 #include <math.h>
 #include <stdint.h>
@@ -59,6 +60,9 @@ typedef struct oracle_shape {
     double softmax_scale;
     double k_scale;
     double v_scale;
+    int32_t num_index_heads; /* Hi: 1, or a multiple of num_kv_heads */
+    int32_t init_blocks;     /* first blocks every token keeps (0: none) */
+    int32_t local_blocks;    /* most recent blocks every token keeps (0: none) */
 } oracle_shape;
 
 enum {
@@ -67,7 +71,19 @@ enum {
     ORACLE_BAD_SEQ_LEN = 2,
     ORACLE_BAD_SELECTION = 3,
     ORACLE_NO_MEMORY = 4,
+    ORACLE_BAD_SHAPE = 5,
 };
+
+/* Selection heads: one table per token shared by every KV head when there is
+ * one index head, else one table per KV head.  [M31-RUBIN] selector-hook
+ * commit: the selector is offered "KV-head-reduced scores"; the select op's
+ * table is [tokens, heads, topk]; [M3-DECODE] restructure of the targets:
+ * "4 KV / index heads".  READING: index head i belongs to KV head
+ * i / (Hi / Hkv) (consecutive, as for query heads). */
+static int selection_heads(const oracle_shape *s)
+{
+    return s->num_index_heads == 1 ? 1 : s->num_kv_heads;
+}
 
 /* ---- element decoders --------------------------------------------------- */
 
@@ -135,9 +151,9 @@ static int64_t page_of(const oracle_shape *s, const int32_t *block_table, int r,
  * low nibble of byte i, one E4M3 scale covers 16 consecutive dimensions,
  * and there is no second-level (global) scale. */
 static double index_key(const oracle_shape *s, const void *pool, const uint8_t *scales,
-                        int64_t page, int tok, int d)
+                        int64_t page, int head, int tok, int d)
 {
-    int64_t row = page * s->page_size + tok;
+    int64_t row = (page * s->num_index_heads + head) * s->page_size + tok;
     if (!s->index_nvfp4)
         return oracle_bf16(((const uint16_t *)pool)[row * s->index_dim + d]);
     uint8_t byte = ((const uint8_t *)pool)[row * (s->index_dim / 2) + d / 2];
@@ -178,23 +194,25 @@ static int check_request(const oracle_shape *s, const int32_t *seq_lens, int r)
 /* ---- (a) index score and per-block max ---------------------------------- */
 
 /* out[b] = max over visible positions pos of block b of the dot product of
- * the token's index query with the index key at pos; -inf for a block with
- * no visible position.  [M3-DECODE] "The TP4 decode target" (index scorer
+ * the token's index query of index head `head` with that head's index key
+ * at pos; -inf for a block with no visible position.  [M3-DECODE] "The TP4 decode target" (index scorer
  * over index-K pages) and [M31-RUBIN] prefill-select commit (per-block
  * "proxy" max score).  READING: the score is the plain dot product (no
  * weights, activation or scaling appear on the pages). */
 int oracle_block_scores(const oracle_shape *s, const uint16_t *q_idx, const void *idxk_pool,
                         const uint8_t *idxk_scales, const int32_t *block_table,
-                        const int32_t *seq_lens, int t, double *out)
+                        const int32_t *seq_lens, int t, int head, double *out)
 {
     int r = t / s->q_per_req;
+    if (head < 0 || head >= s->num_index_heads)
+        return ORACLE_BAD_SHAPE;
     int rc = check_request(s, seq_lens, r);
     if (rc)
         return rc;
     for (int b = 0; b < s->max_blocks; ++b)
         out[b] = -INFINITY;
     int64_t L = visible(s, seq_lens, t);
-    const uint16_t *qi = q_idx + (int64_t)t * s->index_dim;
+    const uint16_t *qi = q_idx + ((int64_t)t * s->num_index_heads + head) * s->index_dim;
     for (int64_t pos = 0; pos < L; ++pos) {
         int64_t b = pos / s->page_size;
         int64_t page = page_of(s, block_table, r, b);
@@ -203,7 +221,7 @@ int oracle_block_scores(const oracle_shape *s, const uint16_t *q_idx, const void
         double score = 0.0;
         for (int d = 0; d < s->index_dim; ++d)
             score += oracle_bf16(qi[d])
-                     * index_key(s, idxk_pool, idxk_scales, page, (int)(pos % s->page_size), d);
+                     * index_key(s, idxk_pool, idxk_scales, page, head, (int)(pos % s->page_size), d);
         if (score > out[b])
             out[b] = score;
     }
@@ -231,32 +249,87 @@ static int ascending(const void *pa, const void *pb)
     return (a > b) - (a < b);
 }
 
-/* Order blocks 0..n_valid-1 by score descending and, on equal scores, by
- * block index ascending ([M3-DECODE] "The TP4 decode target": ties go to
- * the smaller block); keep the first min(k, n_valid); write them in
- * ascending block order followed by -1 up to k ([M31-RUBIN] q8kv4 indexer
- * commit: "the ascending, -1-padded contract").  READING: only blocks that
- * hold a visible position (finite score) are candidates. */
-int oracle_select(const double *scores, int n_valid, int k, int32_t *sel)
+/* Top-k selection with forced blocks.  Forced: the first min(init, n_valid)
+ * blocks and the last min(local, n_valid) of blocks 0..n_valid-1
+ * ([M31-RUBIN] prefill-select commit: the tile select reproduces the stock
+ * table "including tie order and init / local forcing").  READING: forced
+ * blocks are always kept (the pages give no further rule), init + local <= k,
+ * and the remaining k - |forced| places go to the other blocks in the order
+ * (score descending, block index ascending) ([M3-DECODE] "The TP4 decode
+ * target": ties go to the smaller block).  The kept blocks are written in
+ * ascending order followed by -1 up to k ([M31-RUBIN] q8kv4 indexer commit:
+ * "the ascending, -1-padded contract").  READING: only blocks that hold a
+ * visible position (finite score) are candidates. */
+int oracle_select_forced(const double *scores, int n_valid, int k, int init, int local,
+                         int32_t *sel)
 {
+    if (init < 0 || local < 0 || init + local > k)
+        return ORACLE_BAD_SHAPE;
     int *order = (int *)malloc(sizeof(int) * (size_t)(n_valid > 0 ? n_valid : 1));
-    if (!order)
+    char *forced = (char *)calloc((size_t)(n_valid > 0 ? n_valid : 1), 1);
+    if (!order || !forced) {
+        free(order);
+        free(forced);
         return ORACLE_NO_MEMORY;
+    }
+    int n_forced = 0;
+    for (int b = 0; b < n_valid; ++b) {
+        forced[b] = (char)(b < init || b >= n_valid - local);
+        n_forced += forced[b];
+    }
+    /* the other blocks, best first */
+    int n_other = 0;
     for (int b = 0; b < n_valid; ++b)
-        order[b] = b;
+        if (!forced[b])
+            order[n_other++] = b;
 #ifdef _OPENMP
 #pragma omp critical(oracle_qsort)
 #endif
     {
         g_sort_scores = scores;
-        qsort(order, (size_t)n_valid, sizeof(int), by_score_then_index);
+        qsort(order, (size_t)n_other, sizeof(int), by_score_then_index);
     }
-    int keep = n_valid < k ? n_valid : k;
-    qsort(order, (size_t)keep, sizeof(int), ascending);
-    for (int i = 0; i < k; ++i)
-        sel[i] = i < keep ? order[i] : -1;
+    int room = k - n_forced;
+    int keep_other = n_other < room ? n_other : room;
+    /* kept = forced blocks + the best keep_other others, in ascending order */
+    int keep = 0;
+    for (int b = 0; b < n_valid; ++b)
+        if (forced[b])
+            sel[keep++] = b;
+    for (int i = 0; i < keep_other; ++i)
+        sel[keep++] = order[i];
+    qsort(sel, (size_t)keep, sizeof(int32_t), ascending);
+    for (int i = keep; i < k; ++i)
+        sel[i] = -1;
     free(order);
+    free(forced);
     return ORACLE_OK;
+}
+
+/* The plain top-k: no forced blocks. */
+int oracle_select(const double *scores, int n_valid, int k, int32_t *sel)
+{
+    return oracle_select_forced(scores, n_valid, k, 0, 0, sel);
+}
+
+/* Scores of selection head gs: for each block the maximum over the group's
+ * index heads i = gs * r .. gs * r + r - 1 (r = Hi / Hs) of their block
+ * scores.  READING: the pages name "KV-head-reduced scores" without the
+ * reduction; max keeps a block score the largest index score of any
+ * position in the block under any index head of the group, as the per-block
+ * max does for one head.  scores_by_head: [Hi][max_blocks]. */
+void oracle_reduce_heads(const oracle_shape *s, const double *scores_by_head, int gs, double *out)
+{
+    int r = s->num_index_heads / selection_heads(s);
+    for (int b = 0; b < s->max_blocks; ++b) {
+        double m = -INFINITY;
+        for (int i = gs * r; i < gs * r + r; ++i) {
+            double v = scores_by_head[(int64_t)i * s->max_blocks + b];
+            if (v > m)
+                m = v;
+        }
+        out[b] = m;
+    }
 }
 
 /* ---- (c) attention over the selected pages ------------------------------ */
@@ -271,8 +344,10 @@ int oracle_select(const double *scores, int n_valid, int k, int32_t *sel)
  * softmax denominator of the scaled logits.  FP8 K and V are dequantised
  * with their own per-tensor scale.  [M31-RUBIN] "Items and numerics"
  * checks the split-K merge against a float64 reference; this is that
- * reference with no split at all.  sel holds block indices (ascending,
- * -1 padded), as produced by oracle_select. */
+ * reference with no split at all.  sel holds the token's tables
+ * [Hs][topk] of block indices (ascending, -1 padded), as produced by
+ * oracle_select_forced; query head h reads the table of its KV head g when
+ * Hs > 1 ([M31-RUBIN]: the select op's table is [tokens, heads, topk]). */
 int oracle_attend(const oracle_shape *s, const uint16_t *q, const void *kv_pool,
                   const int32_t *block_table, const int32_t *seq_lens, int t,
                   const int32_t *sel, double *out, double *lse)
@@ -285,7 +360,8 @@ int oracle_attend(const oracle_shape *s, const uint16_t *q, const void *kv_pool,
     int P = s->page_size, D = s->head_dim;
     int group = s->num_q_heads / s->num_kv_heads;
 
-    /* positions attended: the visible positions of the selected blocks */
+    /* positions attended by the heads of one table: the visible positions
+     * of its selected blocks (rebuilt when the table changes) */
     int64_t npos = 0;
     int64_t *pos_page = (int64_t *)malloc(sizeof(int64_t) * (size_t)s->topk * P);
     int *pos_tok = (int *)malloc(sizeof(int) * (size_t)s->topk * P);
@@ -294,26 +370,32 @@ int oracle_attend(const oracle_shape *s, const uint16_t *q, const void *kv_pool,
         free(pos_page); free(pos_tok); free(z);
         return ORACLE_NO_MEMORY;
     }
-    for (int i = 0; i < s->topk; ++i) {
-        int32_t b = sel[i];
-        if (b < 0)
-            continue;
-        int64_t page = page_of(s, block_table, r, b);
-        if (page < 0 || (int64_t)b * P >= L) {
-            free(pos_page); free(pos_tok); free(z);
-            return page < 0 ? ORACLE_BAD_PAGE : ORACLE_BAD_SELECTION;
-        }
-        for (int tok = 0; tok < P; ++tok) {
-            if ((int64_t)b * P + tok >= L)
-                break;
-            pos_page[npos] = page;
-            pos_tok[npos] = tok;
-            ++npos;
-        }
-    }
-
+    int hs = selection_heads(s), table = -1;
     for (int h = 0; h < s->num_q_heads; ++h) {
         int g = h / group;
+        int gs = hs > 1 ? g : 0;
+        if (gs != table) {
+            table = gs;
+            npos = 0;
+            const int32_t *sl = sel + (int64_t)gs * s->topk;
+            for (int i = 0; i < s->topk; ++i) {
+                int32_t b = sl[i];
+                if (b < 0)
+                    continue;
+                int64_t page = page_of(s, block_table, r, b);
+                if (page < 0 || (int64_t)b * P >= L) {
+                    free(pos_page); free(pos_tok); free(z);
+                    return page < 0 ? ORACLE_BAD_PAGE : ORACLE_BAD_SELECTION;
+                }
+                for (int tok = 0; tok < P; ++tok) {
+                    if ((int64_t)b * P + tok >= L)
+                        break;
+                    pos_page[npos] = page;
+                    pos_tok[npos] = tok;
+                    ++npos;
+                }
+            }
+        }
         const uint16_t *qh = q + ((int64_t)t * s->num_q_heads + h) * D;
         double M = -INFINITY;
         for (int64_t n = 0; n < npos; ++n) {
@@ -348,9 +430,10 @@ int oracle_attend(const oracle_shape *s, const uint16_t *q, const void *kv_pool,
 
 /* Runs (a), (b) and (c) for each token in tokens[0..n_tokens) and writes
  * row i of every output for tokens[i]:
- *   block_scores [n][max_blocks] float (every score is exact in binary32:
- *                integer-valued or NVFP4 inputs; the test suite checks this)
- *   selected     [n][topk]
+ *   block_scores [n][Hi][max_blocks] float (every score is exact in
+ *                binary32: integer-valued or NVFP4 inputs; the test suite
+ *                checks this)
+ *   selected     [n][Hs][topk]
  *   out          [n][Hq][D] double,  lse [n][Hq] double
  * num_threads > 1 spreads tokens over OpenMP threads (each token is still
  * computed by one thread in the same order). */
@@ -360,6 +443,9 @@ int oracle_decode_step(const oracle_shape *s, const uint16_t *q_idx, const void 
                        const int32_t *tokens, int n_tokens, int num_threads,
                        float *block_scores, int32_t *selected, double *out, double *lse)
 {
+    int Hi = s->num_index_heads, hs = selection_heads(s);
+    if (Hi < 1 || (Hi > 1 && Hi % s->num_kv_heads != 0))
+        return ORACLE_BAD_SHAPE;
     int err = ORACLE_OK;
 #ifdef _OPENMP
     if (num_threads < 1)
@@ -368,23 +454,30 @@ int oracle_decode_step(const oracle_shape *s, const uint16_t *q_idx, const void 
 #endif
     for (int i = 0; i < n_tokens; ++i) {
         int t = tokens[i];
-        double *bs = (double *)malloc(sizeof(double) * (size_t)s->max_blocks);
-        int rc = bs ? ORACLE_OK : ORACLE_NO_MEMORY;
-        if (!rc)
-            rc = oracle_block_scores(s, q_idx, idxk_pool, idxk_scales, block_table, seq_lens, t, bs);
+        double *bs = (double *)malloc(sizeof(double) * (size_t)s->max_blocks * (size_t)Hi);
+        double *red = (double *)malloc(sizeof(double) * (size_t)s->max_blocks);
+        int rc = (bs && red) ? ORACLE_OK : ORACLE_NO_MEMORY;
+        for (int head = 0; head < Hi && !rc; ++head)
+            rc = oracle_block_scores(s, q_idx, idxk_pool, idxk_scales, block_table, seq_lens, t,
+                                     head, bs + (int64_t)head * s->max_blocks);
+        int32_t *sel_t = selected + (int64_t)i * hs * s->topk;
         if (!rc) {
             int64_t L = visible(s, seq_lens, t);
             int n_valid = (int)((L + s->page_size - 1) / s->page_size);
-            for (int b = 0; b < s->max_blocks; ++b)
-                block_scores[(int64_t)i * s->max_blocks + b] = (float)bs[b];
-            rc = oracle_select(bs, n_valid, s->topk, selected + (int64_t)i * s->topk);
+            for (int64_t x = 0; x < (int64_t)Hi * s->max_blocks; ++x)
+                block_scores[(int64_t)i * Hi * s->max_blocks + x] = (float)bs[x];
+            for (int gs = 0; gs < hs && !rc; ++gs) {
+                oracle_reduce_heads(s, bs, gs, red);
+                rc = oracle_select_forced(red, n_valid, s->topk, s->init_blocks, s->local_blocks,
+                                          sel_t + (int64_t)gs * s->topk);
+            }
         }
         if (!rc)
-            rc = oracle_attend(s, q, kv_pool, block_table, seq_lens, t,
-                               selected + (int64_t)i * s->topk,
+            rc = oracle_attend(s, q, kv_pool, block_table, seq_lens, t, sel_t,
                                out + (int64_t)i * s->num_q_heads * s->head_dim,
                                lse + (int64_t)i * s->num_q_heads);
         free(bs);
+        free(red);
         if (rc) {
 #ifdef _OPENMP
 #pragma omp critical(oracle_err)

@@ -7,11 +7,11 @@ consume exactly the arrays built here, so they see the same bytes.
 
 Layouts (all C-contiguous, element types as stored):
 
-    q_idx        uint16 (bf16 bits)  [T, Hi=1, 128]
-    idxk_pool    bf16:  uint16       [num_pages, Hi=1, 128 tokens, 128 dims]
-                 nvfp4: uint8        [num_pages, Hi=1, 128 tokens, 64]   two e2m1 codes
+    q_idx        uint16 (bf16 bits)  [T, Hi, 128]   (Hi index heads; 1 in the workloads)
+    idxk_pool    bf16:  uint16       [num_pages, Hi, 128 tokens, 128 dims]
+                 nvfp4: uint8        [num_pages, Hi, 128 tokens, 64]   two e2m1 codes
                                      per byte, dimension 2i in the low nibble
-    idxk_scales  nvfp4 only: uint8   [num_pages, Hi=1, 128 tokens, 8]    one E4M3
+    idxk_scales  nvfp4 only: uint8   [num_pages, Hi, 128 tokens, 8]    one E4M3
                                      scale per 16 consecutive dimensions
     q            uint16 (bf16 bits)  [T, Hq, 128]
     kv_pool      bf16: uint16 / fp8: uint8 (E4M3)
@@ -73,6 +73,9 @@ class Problem:
     seq_lens: np.ndarray
     seed: int = 0
     recipe: str = ""
+    num_index_heads: int = 1   # Hi: 1, or a multiple of num_kv_heads
+    init_blocks: int = 0       # first blocks every token keeps
+    local_blocks: int = 0      # most recent blocks every token keeps
 
     @property
     def num_tokens(self) -> int:
@@ -197,6 +200,9 @@ def make_problem(
     seed: int = 0,
     softmax_scale: Optional[float] = None,
     recipe: str = "",
+    num_index_heads: int = 1,
+    init_blocks: int = 0,
+    local_blocks: int = 0,
 ) -> Problem:
     """Build a seeded problem.
 
@@ -235,17 +241,19 @@ def make_problem(
 
     # index query and index-K pool
     lo, hi = index_range
-    q_idx = ints_bf16(rng, (T, 1, INDEX_DIM), lo, hi)
+    Hi = int(num_index_heads)
+    q_idx = ints_bf16(rng, (T, Hi, INDEX_DIM), lo, hi)
     if index_dtype == BF16:
-        idxk = np.empty((num_pages, 1, PAGE, INDEX_DIM), dtype=np.uint16)
-        _fill_chunked(idxk, lambda n: ints_bf16(rng, (n, 1, PAGE, INDEX_DIM), lo, hi), 1024)
+        idxk = np.empty((num_pages, Hi, PAGE, INDEX_DIM), dtype=np.uint16)
+        _fill_chunked(idxk, lambda n: ints_bf16(rng, (n, Hi, PAGE, INDEX_DIM), lo, hi),
+                      max(1, 1024 // Hi))
         scales = None
     elif index_dtype == NVFP4:
-        idxk = np.empty((num_pages, 1, PAGE, INDEX_DIM // 2), dtype=np.uint8)
-        _fill_chunked(idxk, lambda n: rng.integers(0, 256, size=(n, 1, PAGE, INDEX_DIM // 2),
-                                                   dtype=np.uint8), 4096)
+        idxk = np.empty((num_pages, Hi, PAGE, INDEX_DIM // 2), dtype=np.uint8)
+        _fill_chunked(idxk, lambda n: rng.integers(0, 256, size=(n, Hi, PAGE, INDEX_DIM // 2),
+                                                   dtype=np.uint8), max(1, 4096 // Hi))
         # E4M3 scale codes of 2^e, e uniform in [-4, 4]: code = (e + 7) << 3
-        e = rng.integers(-4, 5, size=(num_pages, 1, PAGE, INDEX_DIM // 16))
+        e = rng.integers(-4, 5, size=(num_pages, Hi, PAGE, INDEX_DIM // 16))
         scales = ((e + 7) << 3).astype(np.uint8)
     else:
         raise ValueError(index_dtype)
@@ -278,6 +286,7 @@ def make_problem(
         softmax_scale=float(softmax_scale), k_scale=float(k_scale), v_scale=float(v_scale),
         q_idx=q_idx, idxk_pool=idxk, idxk_scales=scales, q=q, kv_pool=kv,
         block_table=block_table, seq_lens=seq_lens, seed=seed, recipe=recipe,
+        num_index_heads=Hi, init_blocks=int(init_blocks), local_blocks=int(local_blocks),
     )
 
 
