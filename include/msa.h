@@ -34,6 +34,16 @@
  *     visible positions, -inf for a block with none;
  *   - only blocks with a visible position can be selected;
  *   - query head h uses KV head h / 16;
+ *   - with one index head every KV head of a token uses one table; with
+ *     Hi = num_index_heads > 1 (a multiple of Hkv), index head i belongs to
+ *     KV head i / (Hi / Hkv) and each KV head g gets its own table, selected
+ *     on the maximum over its index heads of their block scores
+ *     ("KV-head-reduced scores", selector-hook commit of "Add Rubin (sm_107)
+ *     ..."; the select op's table is [tokens, heads, topk]);
+ *   - init / local forcing (prefill-select commit of "Add Rubin (sm_107)
+ *     ..."): the first init_blocks and the last local_blocks blocks a token
+ *     sees are always selected (init_blocks + local_blocks <= topk); the
+ *     other places go to the best block scores as above;
  *   - logits are softmax_scale * q . k (FP8 keys times k_scale), the output
  *     is the softmax-weighted mean of V (FP8 values times v_scale), and
  *     lse = ln(sum exp(logit)) (natural log);
@@ -57,8 +67,8 @@
  *   - Every device pointer must be 16-byte aligned.
  *
  * Layouts (row-major, element type as stored; T = num_requests * q_per_req,
- * Hi = num_index_heads = 1, P = page_size = 128, D = head_dim = 128,
- * Di = index_dim = 128):
+ * Hi = num_index_heads, Hs = 1 if Hi == 1 else num_kv_heads (tables per
+ * token), P = page_size = 128, D = head_dim = 128, Di = index_dim = 128):
  *   q_idx        bf16 [T][Hi][Di]
  *   idxk_pool    MSA_BF16:  bf16 [num_pages][Hi][P][Di]
  *                MSA_NVFP4: uint8 [num_pages][Hi][P][Di/2]  (e2m1 pairs)
@@ -73,7 +83,7 @@
  *   block_scores fp32 [T][Hi][max_blocks_per_seq]; entries b < the
  *                request's cached block count are written (-inf where the
  *                token sees no position of block b); the rest are untouched
- *   selected     int32 [T][Hi][topk], ascending, -1 padded
+ *   selected     int32 [T][Hs][topk], ascending, -1 padded
  *   out          bf16 [T][Hq][D] (round to nearest even from fp32)
  *   lse          fp32 [T][Hq]
  */
@@ -105,8 +115,9 @@ typedef enum msa_dtype {
 } msa_dtype;
 
 /* Shape and scalars of one call.  Covered today: head_dim = index_dim =
- * page_size = 128, num_q_heads = 16 * num_kv_heads, num_index_heads = 1,
- * 1 <= q_per_req <= 64, 1 <= topk <= 256, max_blocks_per_seq <= 16384,
+ * page_size = 128, num_q_heads = 16 * num_kv_heads, num_index_heads = 1 or
+ * a multiple of num_kv_heads up to 64, 1 <= q_per_req <= 64,
+ * 1 <= topk <= 256, max_blocks_per_seq <= 16384,
  * num_requests * q_per_req <= 8192, kv_dtype in {BF16, FP8_E4M3},
  * index_dtype in {BF16, NVFP4}. */
 typedef struct msa_shape {
@@ -127,6 +138,8 @@ typedef struct msa_shape {
     float softmax_scale;        /* multiplies q . k (1/sqrt(128) in the workloads) */
     float k_scale;              /* FP8 K dequantisation scale (ignored for bf16) */
     float v_scale;              /* FP8 V dequantisation scale (ignored for bf16) */
+    int32_t init_blocks;        /* first blocks every token keeps (0: none) */
+    int32_t local_blocks;       /* most recent blocks every token keeps (0: none) */
 } msa_shape;
 
 /* Bytes of device workspace the calls below need for `shape` (0 if the
@@ -138,8 +151,9 @@ size_t msa_workspace_bytes(const msa_shape *shape);
  * MSA_ERR_TIMEOUT; every other call leaves the counters at zero. */
 msa_status msa_workspace_init(void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
-/* Stage (a): block_scores[t][0][b] = max over the visible positions of
- * block b of dot(q_idx[t], index key).  Exact in fp32 for integer-valued
+/* Stage (a): block_scores[t][i][b] = max over the visible positions of
+ * block b of dot(q_idx[t][i], index key of head i).  One pass per index
+ * head.  Exact in fp32 for integer-valued
  * bf16 inputs with |score| < 2^24 and for NVFP4 keys with power-of-two
  * scales.  ("MiniMax-M3 NVFP4 low-latency decode megakernel ...", "The TP4
  * decode target": the index scorer; prefill-select commit of "Add Rubin
@@ -149,9 +163,13 @@ msa_status msa_index_score(const msa_shape *shape, const void *q_idx, const void
                            const int32_t *seq_lens, float *block_scores, void *workspace,
                            size_t workspace_bytes, cudaStream_t stream);
 
-/* Stage (b): for each token, the topk blocks with the largest block_scores
+/* Stage (b): for each token (and KV head, when Hs > 1), the topk blocks
+ * with the largest block score (the maximum over the KV head's index heads)
  * among blocks 0 .. ceil((seq_lens[r] + j) / 128) - 1, ties to the smaller
- * block index, written ascending and -1 padded.  Bit-exact.
+ * block index, after the init_blocks first and local_blocks last of them,
+ * which are always kept; written ascending and -1 padded.  Bit-exact.
+ * init_blocks + local_blocks > topk, or either negative, returns
+ * MSA_ERR_INVALID_ARGUMENT.
  * ("MiniMax-M3 NVFP4 low-latency decode megakernel ...", "The TP4 decode
  * target": tie contract; q8kv4 indexer commit of "Add Rubin (sm_107) ...":
  * the ascending, -1-padded table.) */

@@ -51,6 +51,8 @@ class MsaShape(ctypes.Structure):
         ("softmax_scale", ctypes.c_float),
         ("k_scale", ctypes.c_float),
         ("v_scale", ctypes.c_float),
+        ("init_blocks", ctypes.c_int32),
+        ("local_blocks", ctypes.c_int32),
     ]
 
 
@@ -127,7 +129,7 @@ def _check(status: int, where: str):
 def make_shape(*, num_requests, q_per_req, num_kv_heads, num_pages, max_blocks_per_seq, topk,
                kv_dtype="bf16", index_dtype="bf16", softmax_scale=128 ** -0.5, k_scale=1.0,
                v_scale=1.0, decode_ctas=0, head_dim=128, index_dim=128, page_size=128,
-               num_index_heads=1, num_q_heads=None) -> MsaShape:
+               num_index_heads=1, num_q_heads=None, init_blocks=0, local_blocks=0) -> MsaShape:
     if isinstance(kv_dtype, str):
         kv_dtype = DTYPE_CODES[kv_dtype]
     if isinstance(index_dtype, str):
@@ -139,7 +141,7 @@ def make_shape(*, num_requests, q_per_req, num_kv_heads, num_pages, max_blocks_p
         index_dim=index_dim, page_size=page_size, num_pages=num_pages,
         max_blocks_per_seq=max_blocks_per_seq, topk=topk, kv_dtype=kv_dtype,
         index_dtype=index_dtype, decode_ctas=decode_ctas, softmax_scale=softmax_scale,
-        k_scale=k_scale, v_scale=v_scale)
+        k_scale=k_scale, v_scale=v_scale, init_blocks=init_blocks, local_blocks=local_blocks)
 
 
 def msa_workspace_bytes(shape: MsaShape) -> int:

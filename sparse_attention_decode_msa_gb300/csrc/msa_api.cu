@@ -33,8 +33,15 @@ msa_status check_shape(const msa_shape *s)
     if (!std::isfinite(s->softmax_scale) || !std::isfinite(s->k_scale) ||
         !std::isfinite(s->v_scale))
         return MSA_ERR_INVALID_ARGUMENT;
+    if (s->num_index_heads < 1 || s->init_blocks < 0 || s->local_blocks < 0 ||
+        (long long)s->init_blocks + s->local_blocks > s->topk)
+        return MSA_ERR_INVALID_ARGUMENT;
     if (s->head_dim != kDim || s->index_dim != kDim || s->page_size != kPage ||
-        s->num_index_heads != 1 || s->num_q_heads != kGroup * s->num_kv_heads)
+        s->num_q_heads != kGroup * s->num_kv_heads)
+        return MSA_ERR_UNSUPPORTED;
+    // one index head (one table per token) or a whole number per KV head
+    if (s->num_index_heads > kMaxIndexHeads ||
+        (s->num_index_heads > 1 && s->num_index_heads % s->num_kv_heads != 0))
         return MSA_ERR_UNSUPPORTED;
     if (s->q_per_req > kMaxQPerReq || s->topk > kMaxTopk || s->max_blocks_per_seq > kMaxBlocks ||
         s->num_requests > kMaxRequests ||
@@ -44,8 +51,9 @@ msa_status check_shape(const msa_shape *s)
         return MSA_ERR_UNSUPPORTED;
     if (s->index_dtype != MSA_BF16 && s->index_dtype != MSA_NVFP4)
         return MSA_ERR_UNSUPPORTED;
-    // page row index of the KV tensor map must fit in int32
-    if ((long long)s->num_pages * 2 * s->num_kv_heads * kPage > 0x7FFFFFFFll)
+    // page row indices of the KV and index-key tensor maps must fit in int32
+    if ((long long)s->num_pages * 2 * s->num_kv_heads * kPage > 0x7FFFFFFFll ||
+        (long long)s->num_pages * s->num_index_heads * kPage > 0x7FFFFFFFll)
         return MSA_ERR_UNSUPPORTED;
     return MSA_OK;
 }
@@ -53,6 +61,13 @@ msa_status check_shape(const msa_shape *s)
 int tokens_of(const msa_shape *s)
 {
     return s->num_requests * s->q_per_req;
+}
+
+// Selection tables per token: one shared by every KV head with one index
+// head, else one per KV head.
+int selection_heads(const msa_shape *s)
+{
+    return s->num_index_heads == 1 ? 1 : s->num_kv_heads;
 }
 
 int cta_bound(const msa_shape *s)
@@ -68,9 +83,9 @@ WorkspaceLayout layout_of(const msa_shape *s)
     w.counters_off = off;
     off = align_up(off + T * s->num_kv_heads * sizeof(int32_t));
     w.scores_off = off;
-    off = align_up(off + T * s->max_blocks_per_seq * sizeof(float));
+    off = align_up(off + T * s->num_index_heads * s->max_blocks_per_seq * sizeof(float));
     w.selected_off = off;
-    off = align_up(off + T * s->topk * sizeof(int32_t));
+    off = align_up(off + T * selection_heads(s) * s->topk * sizeof(int32_t));
     w.partial_off = off;
     w.slots = (int64_t)cta_bound(s) + (int64_t)T * s->num_kv_heads;
     off = align_up(off + (size_t)w.slots * kPartialBytes);
@@ -126,10 +141,18 @@ msa_status score_impl(const msa_shape *s, const void *q_idx, const void *idxk_po
     p.nq = s->q_per_req;
     p.maxB = s->max_blocks_per_seq;
     p.num_pages = s->num_pages;
+    p.heads = s->num_index_heads;
     const int sms = num_sms_current();
     if (sms < 1)
         return MSA_ERR_CUDA;
-    return cuda_status(launch_index_score(p, s->index_dtype, sms, stream));
+    // one pass of the scorer per index head
+    for (int h = 0; h < p.heads; ++h) {
+        p.head = h;
+        const cudaError_t e = launch_index_score(p, s->index_dtype, sms, stream);
+        if (e != cudaSuccess)
+            return MSA_ERR_CUDA;
+    }
+    return MSA_OK;
 }
 
 msa_status select_impl(const msa_shape *s, const float *block_scores, const int32_t *seq_lens,
@@ -144,6 +167,10 @@ msa_status select_impl(const msa_shape *s, const float *block_scores, const int3
     p.nq = s->q_per_req;
     p.maxB = s->max_blocks_per_seq;
     p.k = s->topk;
+    p.Hi = s->num_index_heads;
+    p.Hs = selection_heads(s);
+    p.init = s->init_blocks;
+    p.local = s->local_blocks;
     return cuda_status(launch_select(p, stream, pdl));
 }
 
@@ -170,6 +197,7 @@ msa_status decode_impl(const msa_shape *s, const void *q, const void *kv_pool,
     p.maxB = s->max_blocks_per_seq;
     p.k = s->topk;
     p.num_pages = s->num_pages;
+    p.Hs = selection_heads(s);
     const bool fp8 = s->kv_dtype == MSA_FP8_E4M3;
     p.scale_log2 = s->softmax_scale * 1.4426950408889634f * (fp8 ? s->k_scale : 1.f);
     p.v_scale = fp8 ? s->v_scale : 1.f;

@@ -121,7 +121,7 @@ __device__ int4 make_entry(const DecodeParams &p, long long x, const int *qt)
     const Task tk = task_of(x, qt, p.T);
     const int r = tk.t / p.nq, j = tk.t - r * p.nq;
     const int n_vis = ceil_div(p.seq_lens[r] + j, kPage);
-    const int b = p.selected[(size_t)tk.t * p.k + tk.i];
+    const int b = p.selected[((size_t)tk.t * p.Hs + (p.Hs > 1 ? tk.g : 0)) * p.k + tk.i];
     int row = -1;
     if (b < 0 || b >= n_vis) {
         set_error(p.err, kErrSelection);

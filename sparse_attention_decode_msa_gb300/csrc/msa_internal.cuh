@@ -24,6 +24,7 @@ constexpr int kMaxBlocks = 16384;
 constexpr int kMaxTopk = 256;
 constexpr int kMaxQPerReq = 64;
 constexpr int kMaxRequests = 8192;
+constexpr int kMaxIndexHeads = 64;
 constexpr int kDefaultCtaBound = 1024; // workspace bound on default persistent decode CTAs
 
 // Bits of the workspace error word.
@@ -47,36 +48,44 @@ struct WorkspaceLayout {
     size_t total;
 };
 
+// One index head `head` of `heads`: its query row of token t is
+// q_idx + (t * heads + head) * Di, the keys of page pg sit at page row
+// pg * heads + head of the pool, its block scores at row t * heads + head.
 struct ScoreParams {
-    const uint16_t *q_idx;  // bf16 bits [T][Di]
-    const uint8_t *idxk;    // bf16 [pages][P][Di] or nvfp4 bytes [pages][P][Di/2]
-    const uint8_t *scales;  // E4M3 [pages][P][Di/16] (nvfp4)
+    const uint16_t *q_idx;  // bf16 bits [T][heads][Di]
+    const uint8_t *idxk;    // bf16 [pages][heads][P][Di] or nvfp4 bytes [pages][heads][P][Di/2]
+    const uint8_t *scales;  // E4M3 [pages][heads][P][Di/16] (nvfp4)
     const int32_t *block_table;
     const int32_t *seq_lens;
-    float *block_scores;    // [T][maxB]
+    float *block_scores;    // [T][heads][maxB]
     uint32_t *err;
     int R, nq, maxB, num_pages;
+    int heads, head;
 };
 
+// Rows x = t * Hs + gs: selection head gs of token t reads the block scores
+// of index heads gs * (Hi / Hs) .. (gs + 1) * (Hi / Hs) - 1 (their maximum)
+// and keeps the first `init` and the last `local` visible blocks.
 struct SelectParams {
-    const float *block_scores;
+    const float *block_scores; // [T][Hi][maxB]
     const int32_t *seq_lens;
-    int32_t *selected;
+    int32_t *selected;         // [T][Hs][k]
     uint32_t *err;
     int R, nq, maxB, k;
+    int Hi, Hs, init, local;
 };
 
 struct DecodeParams {
     const uint16_t *q; // bf16 bits [T][Hq][D]
     const int32_t *block_table;
     const int32_t *seq_lens;
-    const int32_t *selected; // [T][k]
+    const int32_t *selected; // [T][Hs][k]: one table per token (Hs = 1) or per KV head (Hs = Hkv)
     uint16_t *out;           // bf16 bits [T][Hq][D]
     float *lse;              // [T][Hq]
     float *partial;          // slots of kPartialFloats
     int *counters;           // [T * Hkv], zero between calls
     uint32_t *err;
-    int R, nq, T, Hkv, maxB, k, num_pages;
+    int R, nq, T, Hkv, maxB, k, num_pages, Hs;
     float scale_log2; // softmax_scale * log2(e) (* k_scale for FP8 keys)
     float v_scale;    // 1 for bf16 values
 };

@@ -127,6 +127,7 @@ extern "C" msa_status msa_sparse_decode_noalloc(const msa_shape *shape, const vo
     p.maxB = shape->max_blocks_per_seq;
     p.k = shape->topk;
     p.num_pages = shape->num_pages;
+    p.Hs = shape->num_index_heads == 1 ? 1 : shape->num_kv_heads; // tables per token
     const bool fp8 = shape->kv_dtype == MSA_FP8_E4M3;
     p.scale_log2 = shape->softmax_scale * 1.4426950408889634f * (fp8 ? shape->k_scale : 1.f);
     p.v_scale = fp8 ? shape->v_scale : 1.f;

@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(const ScoreP
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int row = (mt & 7) * 16 + g + 8 * h;
-                const size_t grow = (size_t)page * kPage + row;
+                const size_t grow = ((size_t)page * p.heads + p.head) * kPage + row;
                 if (!NVFP4) {
                     const uint4 *src = reinterpret_cast<const uint4 *>(p.idxk + grow * (kDim * 2));
 #pragma unroll
@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(const ScoreP
             // B fragments of query tokens nt*8 + g, in this thread's dimension order
             const int j = nt * 8 + g;
             uint32_t bq[8][2];
-            const uint16_t *qrow = p.q_idx + (size_t)(t0 + (j < p.nq ? j : 0)) * kDim;
+            const uint16_t *qrow = p.q_idx + ((size_t)(t0 + (j < p.nq ? j : 0)) * p.heads + p.head) * kDim;
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
                 // bf16: k-step s = 2c + hh covers dims 32c + 8q + 4hh .. +3
@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(const ScoreP
             if (b < nb) {
                 const float v = fmaxf(fmaxf(red[0][pg][jj], red[1][pg][jj]),
                                       fmaxf(red[2][pg][jj], red[3][pg][jj]));
-                p.block_scores[(size_t)(t0 + jj) * p.maxB + b] = v;
+                p.block_scores[((size_t)(t0 + jj) * p.heads + p.head) * p.maxB + b] = v;
             }
         }
         __syncthreads();
@@ -434,8 +434,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
                         const uint32_t bar = smem_u32(&full[slot]);
                         const uint32_t dst = smem_u32(ring + (size_t)slot * kSTile);
                         mbar_arrive_expect_tx(bar, kSTile);
-                        tma_load_2d_hint(dst, &k_map, 0, pg * kPage, bar, k_policy);
-                        tma_load_2d_hint(dst + kSTile / 2, &k_map, 64, pg * kPage, bar, k_policy);
+                        const int krow = (pg * p.heads + p.head) * kPage;
+                        tma_load_2d_hint(dst, &k_map, 0, krow, bar, k_policy);
+                        tma_load_2d_hint(dst + kSTile / 2, &k_map, 64, krow, bar, k_policy);
                         issued = l + 1;
                     }
                 }
@@ -557,7 +558,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
         if (e < p.nq) {
             const float *rb = red + rb2 * 4 * NPAD;
             const float m = fmaxf(fmaxf(rb[e], rb[NPAD + e]), fmaxf(rb[2 * NPAD + e], rb[3 * NPAD + e]));
-            p.block_scores[(size_t)(r * p.nq + e) * p.maxB + b] = m;
+            p.block_scores[((size_t)(r * p.nq + e) * p.heads + p.head) * p.maxB + b] = m;
         }
         advance(r, b);
     }
@@ -692,8 +693,9 @@ __global__ void __launch_bounds__(kF4Threads, 1) index_score_fp4_kernel(const Sc
                         const uint32_t bar = smem_u32(&full[slot]);
                         const uint32_t dst = smem_u32(ring + (size_t)slot * kF4Stage);
                         mbar_arrive_expect_tx(bar, kF4Stage);
-                        bulk_load_hint(dst, p.idxk + (size_t)pg * kF4Codes, kF4Codes, bar, k_policy);
-                        bulk_load_hint(dst + kF4Codes, p.scales + (size_t)pg * kF4Scales, kF4Scales, bar, k_policy);
+                        const size_t prow = (size_t)pg * p.heads + p.head;
+                        bulk_load_hint(dst, p.idxk + prow * kF4Codes, kF4Codes, bar, k_policy);
+                        bulk_load_hint(dst + kF4Codes, p.scales + prow * kF4Scales, kF4Scales, bar, k_policy);
                         issued = l + 1;
                     }
                 }
@@ -727,7 +729,7 @@ __global__ void __launch_bounds__(kF4Threads, 1) index_score_fp4_kernel(const Sc
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 const int j = nt * 8 + g;
-                const uint16_t *qrow = p.q_idx + (size_t)(r * p.nq + (j < p.nq ? j : 0)) * kDim;
+                const uint16_t *qrow = p.q_idx + ((size_t)(r * p.nq + (j < p.nq ? j : 0)) * p.heads + p.head) * kDim;
 #pragma unroll
                 for (int s = 0; s < 8; ++s) {
                     // k-step s covers dims 32 q + 4 s .. + 3 (the codes' order below)
@@ -806,7 +808,7 @@ __global__ void __launch_bounds__(kF4Threads, 1) index_score_fp4_kernel(const Sc
                 v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
                 const int jj = nt * 8 + 2 * q + c;
                 if (g == 0 && jj < p.nq)
-                    p.block_scores[(size_t)(r * p.nq + jj) * p.maxB + b] = v;
+                    p.block_scores[((size_t)(r * p.nq + jj) * p.heads + p.head) * p.maxB + b] = v;
             }
     }
     if (!ok) {
@@ -870,9 +872,11 @@ cudaError_t launch_index_score(const ScoreParams &p, int index_dtype, int num_sm
         const int T = p.R * p.nq;
         const int npad = (p.nq + 15) / 16 * 16;
         CUtensorMap qmap, kmap;
-        if (!encode_2d_sw128(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.q_idx, kDim, T, kDim * 2, 64, npad) ||
+        // this head's query rows: T rows, heads * Di apart; keys: every page row
+        if (!encode_2d_sw128(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.q_idx + (size_t)p.head * kDim, kDim, T,
+                             (uint64_t)p.heads * kDim * 2, 64, npad) ||
             !encode_2d_sw128(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.idxk, kDim,
-                             (uint64_t)p.num_pages * kPage, kDim * 2, 64, kPage))
+                             (uint64_t)p.num_pages * p.heads * kPage, kDim * 2, 64, kPage))
             return cudaErrorInvalidValue;
         switch (npad) {
         case 16: return launch_umma_fit<16>(p, kmap, qmap, num_sms, stream);

@@ -6,6 +6,12 @@
 // any tie width.  Output ("Add Rubin (sm_107) MiniMax-M3.1 low-latency decode
 // targets", q8kv4 indexer commit): ascending block ids, -1 padded to k.
 //
+// With several index heads a row is (token, KV head) and its score per block
+// is the maximum over the KV head's group of index heads (the maximum of the
+// order-preserving keys).  Forced blocks (the first `init` and the last
+// `local` visible blocks) take the largest key, above every score, so they
+// are always kept and the remaining places go to the best scores.
+//
 // Scores map to order-preserving 32-bit keys.  Rows of up to 2048 blocks take
 // one warp per token (below); longer rows one CTA per token, where an
 // MSB-first radix select (four 8-bit digits) finds the k-th largest key theta
@@ -58,6 +64,21 @@ __device__ int cta_exclusive_scan(int v, int *tmp, int *total)
     return res;
 }
 
+// Key of block b of row (t, gs): forced -> the largest key, else the largest
+// key over the group's index heads.
+__device__ __forceinline__ uint32_t row_key(const SelectParams &p, const float *row, int b, int n)
+{
+    if (b < p.init || b >= n - p.local)
+        return 0xFFFFFFFFu;
+    const int r = p.Hi / p.Hs;
+    uint32_t k = order_key(row[b]);
+    for (int i = 1; i < r; ++i) {
+        const uint32_t v = order_key(row[(size_t)i * p.maxB + b]);
+        k = v > k ? v : k;
+    }
+    return k;
+}
+
 __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(const SelectParams p)
 {
     extern __shared__ uint32_t keys[]; // [maxB]
@@ -67,9 +88,10 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(const SelectPa
     __shared__ int s_need;
 
     launch_dependents(); // the decode may start its prologue while tokens are selected
-    const int t = blockIdx.x;
+    const int x = blockIdx.x; // row: token t, selection head gs
+    const int t = x / p.Hs, gs = x - t * p.Hs;
     const int r = t / p.nq, j = t - r * p.nq;
-    int32_t *out = p.selected + (size_t)t * p.k;
+    int32_t *out = p.selected + (size_t)x * p.k;
     const int seq_len = p.seq_lens[r];
     const long long nb_req = ((long long)seq_len + p.nq - 1 + kPage - 1) / kPage;
     if (seq_len < 1 || nb_req > p.maxB) {
@@ -88,9 +110,9 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(const SelectPa
 
     // block_scores come from the previous kernel of the step
     grid_dependency_wait();
-    const float *row = p.block_scores + (size_t)t * p.maxB;
+    const float *row = p.block_scores + ((size_t)t * p.Hi + (size_t)gs * (p.Hi / p.Hs)) * p.maxB;
     for (int b = threadIdx.x; b < n; b += kSelThreads)
-        keys[b] = order_key(row[b]);
+        keys[b] = row_key(p, row, b, n);
     if (threadIdx.x == 0) {
         s_prefix = 0u;
         s_need = p.k;
@@ -195,12 +217,13 @@ __global__ void __launch_bounds__(32 * kWarpSelWarps) select_topk_warp_kernel(co
 {
     launch_dependents();
     const int lane = threadIdx.x & 31;
-    const int T = p.R * p.nq;
-    const int t = blockIdx.x * kWarpSelWarps + (threadIdx.x >> 5);
-    if (t >= T)
+    const int rows = p.R * p.nq * p.Hs;
+    const int x = blockIdx.x * kWarpSelWarps + (threadIdx.x >> 5); // row: token t, selection head gs
+    if (x >= rows)
         return;
+    const int t = x / p.Hs, gs = x - t * p.Hs;
     const int r = t / p.nq, j = t - r * p.nq;
-    int32_t *out = p.selected + (size_t)t * p.k;
+    int32_t *out = p.selected + (size_t)x * p.k;
     const int seq_len = p.seq_lens[r];
     const long long nb_req = ((long long)seq_len + p.nq - 1 + kPage - 1) / kPage;
     if (seq_len < 1 || nb_req > p.maxB) {
@@ -217,13 +240,13 @@ __global__ void __launch_bounds__(32 * kWarpSelWarps) select_topk_warp_kernel(co
         return;
     }
     grid_dependency_wait(); // block_scores come from the previous kernel of the step
-    const float *row = p.block_scores + (size_t)t * p.maxB;
+    const float *row = p.block_scores + ((size_t)t * p.Hi + (size_t)gs * (p.Hi / p.Hs)) * p.maxB;
     uint32_t key[S];
 #pragma unroll
     for (int s = 0; s < S; ++s) {
         const int b = lane + 32 * s;
         // blocks past n take key 0, below every candidate tried (all >= 1)
-        key[s] = b < n ? order_key(row[b]) : 0u;
+        key[s] = b < n ? row_key(p, row, b, n) : 0u;
     }
     uint32_t theta = 0;
 #pragma unroll 1
@@ -264,7 +287,7 @@ __global__ void __launch_bounds__(32 * kWarpSelWarps) select_topk_warp_kernel(co
 cudaError_t launch_select(const SelectParams &p, cudaStream_t stream, bool pdl)
 {
     if (p.maxB <= kWarpSelMaxN) {
-        const dim3 grid((p.R * p.nq + kWarpSelWarps - 1) / kWarpSelWarps), block(32 * kWarpSelWarps);
+        const dim3 grid((p.R * p.nq * p.Hs + kWarpSelWarps - 1) / kWarpSelWarps), block(32 * kWarpSelWarps);
         cudaError_t e;
         if (p.maxB <= 256)
             e = launch_kernel(select_topk_warp_kernel<8>, grid, block, 0, stream, pdl, p);
@@ -285,8 +308,8 @@ cudaError_t launch_select(const SelectParams &p, cudaStream_t stream, bool pdl)
         if (e != cudaSuccess)
             return e;
     }
-    const int T = p.R * p.nq;
-    cudaError_t e = launch_kernel(select_topk_kernel, dim3(T), dim3(kSelThreads), smem, stream, pdl, p);
+    const int rows = p.R * p.nq * p.Hs;
+    cudaError_t e = launch_kernel(select_topk_kernel, dim3(rows), dim3(kSelThreads), smem, stream, pdl, p);
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();

@@ -33,7 +33,9 @@ class DeviceProblem:
             num_requests=pb.num_requests, q_per_req=pb.q_per_req, num_kv_heads=pb.num_kv_heads,
             num_pages=pb.num_pages, max_blocks_per_seq=pb.max_blocks, topk=pb.topk,
             kv_dtype=pb.kv_dtype, index_dtype=pb.index_dtype, softmax_scale=pb.softmax_scale,
-            k_scale=pb.k_scale, v_scale=pb.v_scale, decode_ctas=decode_ctas)
+            k_scale=pb.k_scale, v_scale=pb.v_scale, decode_ctas=decode_ctas,
+            num_index_heads=getattr(pb, "num_index_heads", 1),
+            init_blocks=getattr(pb, "init_blocks", 0), local_blocks=getattr(pb, "local_blocks", 0))
         self.q_idx = _dev(pb.q_idx, device)
         self.idxk = _dev(pb.idxk_pool, device)
         self.idxk_scales = None if pb.idxk_scales is None else _dev(pb.idxk_scales, device)
@@ -42,8 +44,10 @@ class DeviceProblem:
         self.block_table = _dev(pb.block_table, device)
         self.seq_lens = _dev(pb.seq_lens, device)
         T, Hq = pb.num_tokens, pb.num_q_heads
-        self.block_scores = torch.full((T, 1, pb.max_blocks), float("nan"), device=device)
-        self.selected = torch.full((T, 1, pb.topk), -7, dtype=torch.int32, device=device)
+        Hi = self.shape.num_index_heads
+        Hs = 1 if Hi == 1 else pb.num_kv_heads      # selection tables per token
+        self.block_scores = torch.full((T, Hi, pb.max_blocks), float("nan"), device=device)
+        self.selected = torch.full((T, Hs, pb.topk), -7, dtype=torch.int32, device=device)
         self.out = torch.full((T, Hq, 128), float("nan"), dtype=torch.bfloat16, device=device)
         self.lse = torch.full((T, Hq), float("nan"), device=device)
         self.ws_bytes = msa_workspace_bytes(self.shape)
@@ -105,9 +109,10 @@ class DeviceProblem:
         import torch
 
         torch.cuda.synchronize()
+        one = self.shape.num_index_heads == 1   # one index head: [T, maxB] and [T, k]
         return {
-            "block_scores": self.block_scores[:, 0].cpu().numpy(),
-            "selected": self.selected[:, 0].cpu().numpy(),
+            "block_scores": (self.block_scores[:, 0] if one else self.block_scores).cpu().numpy(),
+            "selected": (self.selected[:, 0] if one else self.selected).cpu().numpy(),
             "out": self.out.float().cpu().numpy().astype(np.float64),
             "lse": self.lse.cpu().numpy().astype(np.float64),
         }

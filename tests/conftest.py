@@ -8,6 +8,20 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
+@pytest.fixture(scope="session")
+def torch_cuda():
+    """torch with CUDA initialised and the library built and loaded."""
+    import torch
+
+    import sparse_attention_decode_msa_gb300 as msa
+    from sparse_attention_decode_msa_gb300 import build
+
+    build.build()
+    msa.load()
+    torch.cuda.init()
+    return torch
+
+
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a) and the built library")
 

@@ -73,7 +73,8 @@ def test_workspace_bytes_cover_the_layout(lib):
 
 @pytest.mark.parametrize("field,value", [
     ("head_dim", 64), ("index_dim", 64), ("page_size", 64), ("num_q_heads", 32),
-    ("num_index_heads", 2), ("kv_dtype", 2), ("index_dtype", 1), ("q_per_req", 65),
+    ("num_index_heads", 2), ("num_index_heads", 6), ("num_index_heads", 128),
+    ("kv_dtype", 2), ("index_dtype", 1), ("q_per_req", 65),
     ("topk", 257), ("max_blocks_per_seq", 16385),
 ])
 def test_unsupported_shapes_are_rejected(lib, field, value):
@@ -86,7 +87,8 @@ def test_unsupported_shapes_are_rejected(lib, field, value):
 
 @pytest.mark.parametrize("field,value", [
     ("num_requests", -1), ("q_per_req", 0), ("topk", 0), ("num_pages", 0),
-    ("max_blocks_per_seq", 0), ("decode_ctas", -3),
+    ("max_blocks_per_seq", 0), ("decode_ctas", -3), ("num_index_heads", 0),
+    ("init_blocks", -1), ("local_blocks", -1), ("init_blocks", 17), ("local_blocks", 17),
 ])
 def test_invalid_shapes_are_rejected(lib, field, value):
     s = shape()
@@ -124,3 +126,17 @@ def test_zero_requests_is_a_validated_no_op(lib):
     ws_bytes = msa.msa_workspace_bytes(s)
     fake = 0x10000
     assert lib.msa_decode_step(msa.ctypes.byref(s), *([fake] * 11), fake, ws_bytes, None) == 0
+
+
+def test_forced_blocks_may_fill_but_not_exceed_topk(lib):
+    assert msa.msa_workspace_bytes(shape(init_blocks=8, local_blocks=8)) > 0
+    assert msa.msa_workspace_bytes(shape(init_blocks=9, local_blocks=8)) == 0
+
+
+def test_index_heads_per_kv_head_grow_the_score_and_table_buffers(lib):
+    one = msa.msa_workspace_bytes(shape())
+    per_kv = msa.msa_workspace_bytes(shape(num_index_heads=4))     # one table per KV head
+    two_per_kv = msa.msa_workspace_bytes(shape(num_index_heads=8))
+    T, maxB, k = 32, 256, 16
+    assert per_kv >= one + 3 * T * maxB * 4 + 3 * T * k * 4 - 2 * 256
+    assert two_per_kv >= per_kv + 4 * T * maxB * 4 - 256

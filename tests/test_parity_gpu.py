@@ -20,19 +20,6 @@ LSE_RTOL = 1e-4
 THREADS = max(1, min(32, os.cpu_count() or 1))
 
 
-@pytest.fixture(scope="session")
-def torch_cuda():
-    import torch
-
-    import sparse_attention_decode_msa_gb300 as msa
-    from sparse_attention_decode_msa_gb300 import build
-
-    build.build()
-    msa.load()
-    torch.cuda.init()
-    return torch
-
-
 def device_problem(pb, **kw):
     from sparse_attention_decode_msa_gb300.runner import DeviceProblem
 
