@@ -97,6 +97,12 @@ def lib():
         L.oracle_decode_step.restype = ctypes.c_int
         L.oracle_decode_step.argtypes = [ctypes.POINTER(OracleShape), p, p, p, p, p, p, p, p,
                                          ctypes.c_int, ctypes.c_int, p, p, p, p]
+        L.oracle_encode_e4m3.restype = ctypes.c_uint8
+        L.oracle_encode_e4m3.argtypes = [ctypes.c_double]
+        L.oracle_encode_e2m1.restype = ctypes.c_uint8
+        L.oracle_encode_e2m1.argtypes = [ctypes.c_double]
+        L.oracle_kv_update.restype = ctypes.c_int
+        L.oracle_kv_update.argtypes = [ctypes.POINTER(OracleShape), p, p, p, p, p, p, p, p]
         L.oracle_max_threads.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -219,6 +225,31 @@ def decode_step(pb, tokens=None, threads: int = 1) -> dict:
     if Hi == 1:
         bs, sel = bs[:, 0], sel[:, 0]
     return {"block_scores": bs, "selected": sel, "out": out, "lse": lse, "tokens": tokens}
+
+
+def encode_e4m3(x) -> int:
+    return int(lib().oracle_encode_e4m3(float(x)))
+
+
+def encode_e2m1(x) -> int:
+    return int(lib().oracle_encode_e2m1(float(x)))
+
+
+def kv_update(pb, k_new, v_new, idxk_new) -> dict:
+    """The pools after writing this step's new tokens (copies; pb is unchanged).
+
+    k_new, v_new: bf16 bits [T, Hkv, D]; idxk_new: bf16 bits [T, Hi, Di].
+    Returns kv_pool, idxk_pool, idxk_scales (None for bf16 index keys).
+    """
+    s = shape_of(pb)
+    kv = np.array(pb.kv_pool, copy=True, order="C")
+    ik = np.array(pb.idxk_pool, copy=True, order="C")
+    sc = None if pb.idxk_scales is None else np.array(pb.idxk_scales, copy=True, order="C")
+    arrs = [_c(np.asarray(k_new, dtype=np.uint16)), _c(np.asarray(v_new, dtype=np.uint16)),
+            _c(np.asarray(idxk_new, dtype=np.uint16)), _c(pb.block_table), _c(pb.seq_lens)]
+    _check(lib().oracle_kv_update(ctypes.byref(s), *[_ptr(a) for a in arrs], _ptr(kv), _ptr(ik),
+                                  _ptr(sc)))
+    return {"kv_pool": kv, "idxk_pool": ik, "idxk_scales": sc}
 
 
 def max_threads() -> int:

@@ -131,6 +131,40 @@ double oracle_e2m1(uint8_t nibble)
     return sign ? -v : v;
 }
 
+/* ---- element encoders (the KV / index-key update) ----------------------- */
+
+/* Nearest code of a non-negative magnitude among the codes 0..top (whose
+ * values increase with the code), ties to the even code; values above the
+ * largest one saturate to it.  Round to nearest, ties to even, saturating:
+ * the rounding NVIDIA's FP8 / FP4 conversions name (satfinite). */
+static int nearest_code(double mag, double (*decode)(uint8_t), int top)
+{
+    if (!(mag < decode((uint8_t)top)))
+        return top;
+    int best = 0;
+    for (int c = 1; c <= top; ++c) {
+        double d_best = fabs(decode((uint8_t)best) - mag), d = fabs(decode((uint8_t)c) - mag);
+        if (d < d_best || (d == d_best && (c & 1) == 0 && (best & 1) == 1))
+            best = c;
+    }
+    return best;
+}
+
+/* E4M3 code of x (largest finite magnitude 448 = code 0x7E).  A value that
+ * rounds to zero is stored as +0. */
+uint8_t oracle_encode_e4m3(double x)
+{
+    int c = nearest_code(fabs(x), oracle_e4m3, 0x7E);
+    return (uint8_t)(c == 0 ? 0 : (signbit(x) ? 0x80 | c : c));
+}
+
+/* E2M1 code of x (largest magnitude 6 = code 7); zero is stored as +0. */
+uint8_t oracle_encode_e2m1(double x)
+{
+    int c = nearest_code(fabs(x), oracle_e2m1, 7);
+    return (uint8_t)(c == 0 ? 0 : (signbit(x) ? 8 | c : c));
+}
+
 /* ---- paged gather ------------------------------------------------------- */
 
 /* Page holding logical block b of request r, or -1 if the table entry is out
@@ -423,6 +457,88 @@ int oracle_attend(const oracle_shape *s, const uint16_t *q, const void *kv_pool,
     free(pos_page);
     free(pos_tok);
     free(z);
+    return ORACLE_OK;
+}
+
+/* ---- (d) KV / index-key update ------------------------------------------ */
+
+/* Writes this step's keys, values and index keys into their pages, in place.
+ * [M3-DECODE] "The TP4 decode target": the attention megakernels carry "the
+ * KV update"; [M31-RUBIN] q8kv4 indexer commit: the NVFP4 index-K copy is
+ * "refreshed from this step's slots".  READING (the pages give neither the
+ * slot nor the quantiser):
+ *   - new token j of request r sits at position pos = seq_lens[r] - 1 + j
+ *     (the last position it sees), row pos % P of page
+ *     block_table[r][pos / P];
+ *   - bf16 pools take the bf16 inputs as they are;
+ *   - FP8 pools: code = e4m3(x / k_scale) for K and e4m3(x / v_scale) for V,
+ *     the quotient in binary32 (the pages fix no precision; binary32 is the
+ *     kernel's, so both sides take the rounding decision alike);
+ *   - NVFP4 index keys, per group of 16 consecutive dimensions: scale code
+ *     c = e4m3(amax / 6) with amax the largest |x| of the group and 6 the
+ *     largest e2m1 magnitude, S its value, element codes e2m1(x / S) (0 when
+ *     S = 0), quotients in binary32; no second-level scale, as for the
+ *     decoder above.
+ * Inputs (bf16 bits): k_new, v_new [T][Hkv][D], idxk_new [T][Hi][Di]. */
+int oracle_kv_update(const oracle_shape *s, const uint16_t *k_new, const uint16_t *v_new,
+                     const uint16_t *idxk_new, const int32_t *block_table,
+                     const int32_t *seq_lens, void *kv_pool, void *idxk_pool,
+                     uint8_t *idxk_scales)
+{
+    int T = s->num_requests * s->q_per_req;
+    int Hkv = s->num_kv_heads, Hi = s->num_index_heads, D = s->head_dim, Di = s->index_dim;
+    int P = s->page_size;
+    for (int t = 0; t < T; ++t) {
+        int r = t / s->q_per_req, j = t % s->q_per_req;
+        int rc = check_request(s, seq_lens, r);
+        if (rc)
+            return rc;
+        int64_t pos = (int64_t)seq_lens[r] - 1 + j;
+        int64_t page = page_of(s, block_table, r, pos / P);
+        if (page < 0)
+            return ORACLE_BAD_PAGE;
+        int row = (int)(pos % P);
+        for (int kv = 0; kv < 2; ++kv) {
+            const uint16_t *src = kv ? v_new : k_new;
+            float scale = (float)(kv ? s->v_scale : s->k_scale);
+            for (int g = 0; g < Hkv; ++g)
+                for (int d = 0; d < D; ++d) {
+                    uint16_t bits = src[((int64_t)t * Hkv + g) * D + d];
+                    int64_t idx = (((page * 2 + kv) * Hkv + g) * (int64_t)P + row) * D + d;
+                    if (!s->kv_fp8)
+                        ((uint16_t *)kv_pool)[idx] = bits;
+                    else
+                        ((uint8_t *)kv_pool)[idx] =
+                            oracle_encode_e4m3((double)((float)oracle_bf16(bits) / scale));
+                }
+        }
+        for (int i = 0; i < Hi; ++i) {
+            const uint16_t *src = idxk_new + ((int64_t)t * Hi + i) * Di;
+            int64_t prow = (page * Hi + i) * (int64_t)P + row;
+            if (!s->index_nvfp4) {
+                for (int d = 0; d < Di; ++d)
+                    ((uint16_t *)idxk_pool)[prow * Di + d] = src[d];
+                continue;
+            }
+            uint8_t *codes = (uint8_t *)idxk_pool + prow * (Di / 2);
+            for (int grp = 0; grp < Di / 16; ++grp) {
+                float amax = 0.0f;
+                for (int d = 16 * grp; d < 16 * grp + 16; ++d) {
+                    float a = fabsf((float)oracle_bf16(src[d]));
+                    if (a > amax)
+                        amax = a;
+                }
+                uint8_t sc = oracle_encode_e4m3((double)(amax / 6.0f));
+                idxk_scales[prow * (Di / 16) + grp] = sc;
+                float S = (float)oracle_e4m3(sc);
+                for (int d = 16 * grp; d < 16 * grp + 16; d += 2) {
+                    uint8_t lo = S > 0.0f ? oracle_encode_e2m1((double)((float)oracle_bf16(src[d]) / S)) : 0;
+                    uint8_t hi = S > 0.0f ? oracle_encode_e2m1((double)((float)oracle_bf16(src[d + 1]) / S)) : 0;
+                    codes[d / 2] = (uint8_t)(lo | (hi << 4)); /* dimension 2i: low nibble */
+                }
+            }
+        }
+    }
     return ORACLE_OK;
 }
 

@@ -380,3 +380,44 @@ def make_small_workload(idx: int, seed: Optional[int] = None) -> Problem:
                             num_kv_heads=4, topk=32, index_dtype=NVFP4, index_range=(-4, 4),
                             guard_page=True, seed=seed)
     raise ValueError(idx)
+
+
+# ---------------------------------------------------------------------------
+# this step's new tokens (the KV / index-key update)
+
+# magnitudes of the sixteen e2m1 codes (sign in bit 3)
+_E2M1_MAGNITUDES = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def make_update(pb: Problem, seed: Optional[int] = None, exact_nvfp4: bool = False,
+                index_range=(-8, 8)) -> dict:
+    """Seeded new-token inputs of one step for problem pb (bf16 bits):
+
+        k_new, v_new  [T, Hkv, 128]  N(0, 1)
+        idxk_new      [T, Hi, 128]   bf16 index keys: integers in index_range, as the
+                                     workloads' pools hold; NVFP4 index keys: N(0, 1) times 2^e with e
+                                     uniform in [-4, 4] per group of 16 dimensions, or with
+                                     exact_nvfp4 e2m1 magnitudes times 2^e with a +-6 in
+                                     every group (values the NVFP4 format holds exactly)
+    """
+    rng = np.random.default_rng(pb.seed + 1000 if seed is None else seed)
+    T, Hkv, Hi = pb.num_tokens, pb.num_kv_heads, pb.num_index_heads
+    k_new = normal_bf16(rng, (T, Hkv, HEAD_DIM))
+    v_new = normal_bf16(rng, (T, Hkv, HEAD_DIM))
+    groups = (T, Hi, INDEX_DIM // 16, 16)
+    if pb.index_dtype == BF16:
+        idxk_new = ints_bf16(rng, (T, Hi, INDEX_DIM), *index_range)
+    elif not exact_nvfp4:
+        x = bf16_bits_to_f32(normal_bf16(rng, groups)).astype(np.float64)
+        e = rng.integers(-4, 5, size=groups[:3] + (1,))
+        idxk_new = f32_to_bf16_bits((x * np.exp2(e)).astype(np.float32)).reshape(T, Hi, INDEX_DIM)
+    else:
+        mag = _E2M1_MAGNITUDES[rng.integers(0, 8, size=groups)]
+        mag[..., 0] = 6.0                      # the group's largest magnitude
+        sign = np.where(rng.integers(0, 2, size=groups) == 1, -1.0, 1.0)
+        e = rng.integers(-4, 5, size=groups[:3] + (1,))
+        x = (sign * mag * np.exp2(e)).astype(np.float32)
+        perm = np.argsort(rng.random(groups), axis=-1)   # the 6 at a random place
+        x = np.take_along_axis(x, perm, axis=-1)
+        idxk_new = f32_to_bf16_bits(x).reshape(T, Hi, INDEX_DIM)
+    return {"k_new": k_new, "v_new": v_new, "idxk_new": idxk_new}
