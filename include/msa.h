@@ -196,6 +196,31 @@ msa_status msa_decode_step(const msa_shape *shape, const void *q_idx, const void
                            float *block_scores, int32_t *selected, void *out, float *lse,
                            void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* The KV / index-key update: writes this step's new tokens into their pages
+ * through the block table, to run before msa_index_score / msa_decode_step
+ * on the same stream.  ("MiniMax-M3 NVFP4 low-latency decode megakernel
+ * ...", "The TP4 decode target": the attention megakernels carry "the KV
+ * update"; q8kv4 indexer commit of "Add Rubin (sm_107) ...": the NVFP4
+ * index-K copy is "refreshed from this step's slots".)
+ *   k_new, v_new  bf16 [T][Hkv][D]   this step's keys and values
+ *   idxk_new      bf16 [T][Hi][Di]   this step's index keys
+ *   kv_pool, idxk_pool, idxk_scales  the pools of the layouts above (written)
+ * New token j of request r goes to position seq_lens[r] - 1 + j (the last
+ * position it sees): row (pos % 128) of page block_table[r][pos / 128].
+ * Only those rows are written.  Encodings: bf16 pools take the inputs as
+ * they are; MSA_FP8_E4M3 pools store E4M3(x / k_scale) for K and
+ * E4M3(x / v_scale) for V; MSA_NVFP4 index keys store, per 16 consecutive
+ * dimensions, the E4M3 scale c = E4M3(max |x| / 6) and the e2m1 codes of
+ * x / value(c) (0 when c is 0), dimension 2i in the low nibble.  Every
+ * rounding is to nearest even and saturating, quotients in fp32, and a code
+ * that rounds to zero is stored as +0.  A bad seq_len or page id is
+ * reported through the workspace error word (that row is skipped). */
+msa_status msa_kv_update(const msa_shape *shape, const void *k_new, const void *v_new,
+                         const void *idxk_new, const int32_t *block_table,
+                         const int32_t *seq_lens, void *kv_pool, void *idxk_pool,
+                         void *idxk_scales, void *workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
+
 /* Size of the fixed device scratch used by msa_sparse_decode_noalloc. */
 #define MSA_NOALLOC_SCRATCH_BYTES (8u << 20)
 

@@ -67,6 +67,8 @@ _SIGNATURES = {
                                          ctypes.c_size_t, _p]),
     "msa_decode_step": (ctypes.c_int, [ctypes.POINTER(MsaShape), _p, _p, _p, _p, _p, _p, _p, _p, _p,
                                        _p, _p, _p, ctypes.c_size_t, _p]),
+    "msa_kv_update": (ctypes.c_int, [ctypes.POINTER(MsaShape), _p, _p, _p, _p, _p, _p, _p, _p, _p,
+                                     ctypes.c_size_t, _p]),
     "msa_check_device_status": (ctypes.c_int, [_p, _p]),
     "msa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -183,6 +185,14 @@ def msa_decode_step(shape, q_idx, idxk_pool, idxk_scales, q, kv_pool, block_tabl
                                   _ptr(seq_lens), _ptr(block_scores), _ptr(selected), _ptr(out),
                                   _ptr(lse), _ptr(workspace), int(workspace_bytes),
                                   _stream(stream)), "msa_decode_step")
+
+
+def msa_kv_update(shape, k_new, v_new, idxk_new, block_table, seq_lens, kv_pool, idxk_pool,
+                  idxk_scales, workspace, workspace_bytes, stream=None):
+    _check(load().msa_kv_update(ctypes.byref(shape), _ptr(k_new), _ptr(v_new), _ptr(idxk_new),
+                                _ptr(block_table), _ptr(seq_lens), _ptr(kv_pool), _ptr(idxk_pool),
+                                _ptr(idxk_scales), _ptr(workspace), int(workspace_bytes),
+                                _stream(stream)), "msa_kv_update")
 
 
 def msa_check_device_status(workspace, stream=None) -> int:

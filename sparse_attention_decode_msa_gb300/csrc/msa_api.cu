@@ -335,6 +335,52 @@ msa_status msa_decode_step(const msa_shape *shape, const void *q_idx, const void
                        stream, true);
 }
 
+msa_status msa_kv_update(const msa_shape *shape, const void *k_new, const void *v_new,
+                         const void *idxk_new, const int32_t *block_table,
+                         const int32_t *seq_lens, void *kv_pool, void *idxk_pool,
+                         void *idxk_scales, void *workspace, size_t workspace_bytes,
+                         cudaStream_t stream)
+{
+    msa_status st = check_shape(shape);
+    if (st != MSA_OK)
+        return st;
+    if ((st = check_workspace(shape, workspace, workspace_bytes)) != MSA_OK)
+        return st;
+    const bool nvfp4 = shape->index_dtype == MSA_NVFP4;
+    if (!k_new || !v_new || !idxk_new || !block_table || !seq_lens || !kv_pool || !idxk_pool ||
+        (nvfp4 && !idxk_scales))
+        return MSA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(idxk_new) ||
+        !aligned16(block_table) || !aligned16(seq_lens) || !aligned16(kv_pool) ||
+        !aligned16(idxk_pool) || (nvfp4 && !aligned16(idxk_scales)))
+        return MSA_ERR_INVALID_ARGUMENT;
+    if (tokens_of(shape) == 0)
+        return MSA_OK;
+    UpdateParams p;
+    p.k_new = static_cast<const uint16_t *>(k_new);
+    p.v_new = static_cast<const uint16_t *>(v_new);
+    p.idxk_new = static_cast<const uint16_t *>(idxk_new);
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.kv_pool = static_cast<uint8_t *>(kv_pool);
+    p.idxk_pool = static_cast<uint8_t *>(idxk_pool);
+    p.idxk_scales = static_cast<uint8_t *>(idxk_scales);
+    p.err = static_cast<uint32_t *>(workspace);
+    p.R = shape->num_requests;
+    p.nq = shape->q_per_req;
+    p.Hkv = shape->num_kv_heads;
+    p.Hi = shape->num_index_heads;
+    p.maxB = shape->max_blocks_per_seq;
+    p.num_pages = shape->num_pages;
+    p.kv_fp8 = shape->kv_dtype == MSA_FP8_E4M3;
+    p.idx_nvfp4 = nvfp4;
+    p.k_scale = shape->k_scale;
+    p.v_scale = shape->v_scale;
+    if (p.kv_fp8 && !(shape->k_scale > 0.f && shape->v_scale > 0.f))
+        return MSA_ERR_INVALID_ARGUMENT;
+    return cuda_status(launch_kv_update(p, stream));
+}
+
 msa_status msa_check_device_status(void *workspace, cudaStream_t stream)
 {
     if (!workspace || !aligned16(workspace))

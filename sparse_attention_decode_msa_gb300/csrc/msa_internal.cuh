@@ -90,6 +90,22 @@ struct DecodeParams {
     float v_scale;    // 1 for bf16 values
 };
 
+// This step's new tokens written into their pages (the KV / index-key update).
+struct UpdateParams {
+    const uint16_t *k_new;    // bf16 bits [T][Hkv][D]
+    const uint16_t *v_new;    // bf16 bits [T][Hkv][D]
+    const uint16_t *idxk_new; // bf16 bits [T][Hi][Di]
+    const int32_t *block_table;
+    const int32_t *seq_lens;
+    uint8_t *kv_pool;         // [pages][2][Hkv][P][D] bf16 or E4M3
+    uint8_t *idxk_pool;       // [pages][Hi][P][Di] bf16, or [pages][Hi][P][Di/2] e2m1 pairs
+    uint8_t *idxk_scales;     // NVFP4: E4M3 [pages][Hi][P][Di/16]
+    uint32_t *err;
+    int R, nq, Hkv, Hi, maxB, num_pages;
+    bool kv_fp8, idx_nvfp4;
+    float k_scale, v_scale;
+};
+
 // Host launchers (return the first CUDA error of the launch sequence).  With
 // `pdl` the kernel is launched as a programmatic dependent of the previous
 // kernel in the stream (it runs its prologue early and waits on the grid
@@ -100,6 +116,7 @@ cudaError_t launch_index_score(const ScoreParams &p, int index_dtype, int num_sm
 cudaError_t launch_select(const SelectParams &p, cudaStream_t stream, bool pdl);
 cudaError_t launch_sparse_decode(const DecodeParams &p, const void *kv_pool, int kv_dtype,
                                  int ctas, cudaStream_t stream, bool pdl);
+cudaError_t launch_kv_update(const UpdateParams &p, cudaStream_t stream);
 
 __host__ __device__ constexpr size_t align_to(size_t v, size_t a)
 {

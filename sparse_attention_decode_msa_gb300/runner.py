@@ -8,8 +8,8 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import (make_shape, msa_decode_step, msa_index_score, msa_select_topk, msa_sparse_decode,
-               msa_workspace_bytes, msa_workspace_init)
+from . import (make_shape, msa_decode_step, msa_index_score, msa_kv_update, msa_select_topk,
+               msa_sparse_decode, msa_workspace_bytes, msa_workspace_init)
 
 
 def _dev(a, device):
@@ -103,6 +103,29 @@ class DeviceProblem:
                         self.block_scores if keep_intermediates else None,
                         self.selected if keep_intermediates else None,
                         self.out, self.lse, self.ws, self.ws_bytes, stream)
+
+    def kv_update(self, update: dict, stream=None):
+        """Write this step's new tokens (synth.make_update arrays) into the pools."""
+        self.k_new = _dev(update["k_new"], self.device)
+        self.v_new = _dev(update["v_new"], self.device)
+        self.idxk_new = _dev(update["idxk_new"], self.device)
+        msa_kv_update(self.shape, self.k_new, self.v_new, self.idxk_new, self.block_table,
+                      self.seq_lens, self.kv, self.idxk, self.idxk_scales, self.ws, self.ws_bytes,
+                      stream)
+
+    def pools(self) -> dict:
+        """The pools as numpy arrays (the byte layouts of the synthetic module)."""
+        import torch
+
+        torch.cuda.synchronize()
+
+        def host(t, like):
+            a = t.cpu().numpy()
+            return a.view(np.uint16) if like.dtype == np.uint16 else a
+
+        return {"kv_pool": host(self.kv, self.pb.kv_pool),
+                "idxk_pool": host(self.idxk, self.pb.idxk_pool),
+                "idxk_scales": None if self.idxk_scales is None else self.idxk_scales.cpu().numpy()}
 
     # ---- results as numpy ----
     def results(self) -> dict:
