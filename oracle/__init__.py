@@ -103,6 +103,9 @@ def lib():
         L.oracle_encode_e2m1.argtypes = [ctypes.c_double]
         L.oracle_kv_update.restype = ctypes.c_int
         L.oracle_kv_update.argtypes = [ctypes.POINTER(OracleShape), p, p, p, p, p, p, p, p]
+        L.oracle_select_rows.restype = ctypes.c_int
+        L.oracle_select_rows.argtypes = [p, ctypes.c_int, ctypes.c_int, ctypes.c_int, p, ctypes.c_int,
+                                         ctypes.c_int, ctypes.c_int, p]
         L.oracle_max_threads.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -250,6 +253,17 @@ def kv_update(pb, k_new, v_new, idxk_new) -> dict:
     _check(lib().oracle_kv_update(ctypes.byref(s), *[_ptr(a) for a in arrs], _ptr(kv), _ptr(ik),
                                   _ptr(sc)))
     return {"kv_pool": kv, "idxk_pool": ik, "idxk_scales": sc}
+
+
+def select_rows(scores_hbt, n_visible, k: int, init: int = 0, local: int = 0) -> np.ndarray:
+    """int32 [n_rows, Hs, k] tables of the rows of a [Hs, max_blocks, n_rows] score buffer."""
+    sc = np.ascontiguousarray(scores_hbt, dtype=np.float64)
+    hs, maxb, n = sc.shape
+    nv = np.ascontiguousarray(n_visible, dtype=np.int32)
+    sel = np.empty((n, hs, k), dtype=np.int32)
+    _check(lib().oracle_select_rows(_ptr(sc), hs, maxb, n, _ptr(nv), int(k), int(init), int(local),
+                                    _ptr(sel)))
+    return sel
 
 
 def max_threads() -> int:

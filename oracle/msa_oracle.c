@@ -366,6 +366,36 @@ void oracle_reduce_heads(const oracle_shape *s, const double *scores_by_head, in
     }
 }
 
+/* Block selection of many query rows from a head-major score buffer
+ * scores[Hs][max_blocks][n_rows] (the row index innermost): row t of
+ * selection head gs sees blocks 0 .. n_visible[t] - 1, and its table
+ * sel[t][gs][0..k) is what oracle_select_forced gives for that row.
+ * [M31-RUBIN] prefill-select commit: context rows take a tile select over a
+ * [heads, max_k_tiles, tokens] max-score block, with the "same table bit
+ * for bit, including tie order and init / local forcing" as the per-token
+ * select. */
+int oracle_select_rows(const double *scores, int hs, int max_blocks, int n_rows,
+                       const int32_t *n_visible, int k, int init, int local, int32_t *sel)
+{
+    double *row = (double *)malloc(sizeof(double) * (size_t)(max_blocks > 0 ? max_blocks : 1));
+    if (!row)
+        return ORACLE_NO_MEMORY;
+    int rc = ORACLE_OK;
+    for (int t = 0; t < n_rows && !rc; ++t)
+        for (int gs = 0; gs < hs && !rc; ++gs) {
+            int n = n_visible[t];
+            if (n < 0 || n > max_blocks) {
+                rc = ORACLE_BAD_SHAPE;
+                break;
+            }
+            for (int b = 0; b < n; ++b)
+                row[b] = scores[((int64_t)gs * max_blocks + b) * n_rows + t];
+            rc = oracle_select_forced(row, n, k, init, local, sel + ((int64_t)t * hs + gs) * k);
+        }
+    free(row);
+    return rc;
+}
+
 /* ---- (c) attention over the selected pages ------------------------------ */
 
 /* For every query head h (KV head g = h / (Hq/Hkv); READING: consecutive
