@@ -221,6 +221,27 @@ msa_status msa_kv_update(const msa_shape *shape, const void *k_new, const void *
                          void *idxk_scales, void *workspace, size_t workspace_bytes,
                          cudaStream_t stream);
 
+/* Block tables of many query rows (a prefill's context rows) from a
+ * head-major max-score buffer, one table per row and selection head, the
+ * same table bit for bit as msa_select_topk gives each row (ties to the
+ * smaller block, init / local forcing).  ("Add Rubin (sm_107) ...",
+ * prefill-select commit: context rows take a tile select, one CTA per KV
+ * head and 8 queries over a [heads, max_k_tiles, tokens] max-score block,
+ * each score sector read once.)
+ *   scores_hbt  fp32 [Hs][max_blocks_per_seq][T], the row index innermost:
+ *               the selection heads' block scores (already reduced over
+ *               index heads); entry b of row t is read for
+ *               b < ceil((seq_lens[r] + j) / 128), t = r * q_per_req + j
+ *   selected    int32 [T][Hs][topk], ascending, -1 padded
+ * q_per_req may exceed the decode's 64 here (a prefill of C tokens is one
+ * request with q_per_req = C and seq_lens = 1).  max_blocks_per_seq above
+ * 2048 returns MSA_ERR_UNSUPPORTED (msa_select_topk covers longer rows in
+ * the token-major layout).  Only the workspace's error word is used: a
+ * workspace of 256 bytes suffices. */
+msa_status msa_select_rows(const msa_shape *shape, const float *scores_hbt,
+                           const int32_t *seq_lens, int32_t *selected, void *workspace,
+                           size_t workspace_bytes, cudaStream_t stream);
+
 /* Size of the fixed device scratch used by msa_sparse_decode_noalloc. */
 #define MSA_NOALLOC_SCRATCH_BYTES (8u << 20)
 

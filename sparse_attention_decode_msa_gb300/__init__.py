@@ -69,6 +69,8 @@ _SIGNATURES = {
                                        _p, _p, _p, ctypes.c_size_t, _p]),
     "msa_kv_update": (ctypes.c_int, [ctypes.POINTER(MsaShape), _p, _p, _p, _p, _p, _p, _p, _p, _p,
                                      ctypes.c_size_t, _p]),
+    "msa_select_rows": (ctypes.c_int, [ctypes.POINTER(MsaShape), _p, _p, _p, _p, ctypes.c_size_t,
+                                       _p]),
     "msa_check_device_status": (ctypes.c_int, [_p, _p]),
     "msa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -193,6 +195,13 @@ def msa_kv_update(shape, k_new, v_new, idxk_new, block_table, seq_lens, kv_pool,
                                 _ptr(block_table), _ptr(seq_lens), _ptr(kv_pool), _ptr(idxk_pool),
                                 _ptr(idxk_scales), _ptr(workspace), int(workspace_bytes),
                                 _stream(stream)), "msa_kv_update")
+
+
+def msa_select_rows(shape, scores_hbt, seq_lens, selected, workspace, workspace_bytes,
+                    stream=None):
+    _check(load().msa_select_rows(ctypes.byref(shape), _ptr(scores_hbt), _ptr(seq_lens),
+                                  _ptr(selected), _ptr(workspace), int(workspace_bytes),
+                                  _stream(stream)), "msa_select_rows")
 
 
 def msa_check_device_status(workspace, stream=None) -> int:

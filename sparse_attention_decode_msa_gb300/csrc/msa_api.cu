@@ -22,8 +22,9 @@ bool aligned16(const void *p)
     return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
 }
 
-// Shape checks shared by every entry point.
-msa_status check_shape(const msa_shape *s)
+// Shape checks shared by every entry point.  many_rows: the row select, whose
+// rows per request are not limited by the decode's and scorer's tiles.
+msa_status check_shape(const msa_shape *s, bool many_rows = false)
 {
     if (!s)
         return MSA_ERR_INVALID_ARGUMENT;
@@ -43,9 +44,12 @@ msa_status check_shape(const msa_shape *s)
     if (s->num_index_heads > kMaxIndexHeads ||
         (s->num_index_heads > 1 && s->num_index_heads % s->num_kv_heads != 0))
         return MSA_ERR_UNSUPPORTED;
-    if (s->q_per_req > kMaxQPerReq || s->topk > kMaxTopk || s->max_blocks_per_seq > kMaxBlocks ||
-        s->num_requests > kMaxRequests ||
-        (long long)s->num_requests * s->q_per_req > kMaxTokens)
+    if (!many_rows && (s->q_per_req > kMaxQPerReq ||
+                       (long long)s->num_requests * s->q_per_req > kMaxTokens))
+        return MSA_ERR_UNSUPPORTED;
+    if (many_rows && (long long)s->num_requests * s->q_per_req > kMaxRows)
+        return MSA_ERR_UNSUPPORTED;
+    if (s->topk > kMaxTopk || s->max_blocks_per_seq > kMaxBlocks || s->num_requests > kMaxRequests)
         return MSA_ERR_UNSUPPORTED;
     if (s->kv_dtype != MSA_BF16 && s->kv_dtype != MSA_FP8_E4M3)
         return MSA_ERR_UNSUPPORTED;
@@ -379,6 +383,39 @@ msa_status msa_kv_update(const msa_shape *shape, const void *k_new, const void *
     if (p.kv_fp8 && !(shape->k_scale > 0.f && shape->v_scale > 0.f))
         return MSA_ERR_INVALID_ARGUMENT;
     return cuda_status(launch_kv_update(p, stream));
+}
+
+msa_status msa_select_rows(const msa_shape *shape, const float *scores_hbt,
+                           const int32_t *seq_lens, int32_t *selected, void *workspace,
+                           size_t workspace_bytes, cudaStream_t stream)
+{
+    msa_status st = check_shape(shape, true);
+    if (st != MSA_OK)
+        return st;
+    if (shape->max_blocks_per_seq > kMaxRowSelectBlocks)
+        return MSA_ERR_UNSUPPORTED;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < kAlign)
+        return MSA_ERR_INVALID_ARGUMENT;
+    if (!scores_hbt || !seq_lens || !selected)
+        return MSA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(scores_hbt) || !aligned16(seq_lens) || !aligned16(selected))
+        return MSA_ERR_INVALID_ARGUMENT;
+    if (tokens_of(shape) == 0)
+        return MSA_OK;
+    SelectParams p;
+    p.block_scores = scores_hbt;
+    p.seq_lens = seq_lens;
+    p.selected = selected;
+    p.err = static_cast<uint32_t *>(workspace);
+    p.R = shape->num_requests;
+    p.nq = shape->q_per_req;
+    p.maxB = shape->max_blocks_per_seq;
+    p.k = shape->topk;
+    p.Hs = selection_heads(shape);
+    p.Hi = p.Hs; // the buffer holds the selection heads' scores already
+    p.init = shape->init_blocks;
+    p.local = shape->local_blocks;
+    return cuda_status(launch_select_rows(p, stream));
 }
 
 msa_status msa_check_device_status(void *workspace, cudaStream_t stream)

@@ -25,6 +25,7 @@ constexpr int kMaxTopk = 256;
 constexpr int kMaxQPerReq = 64;
 constexpr int kMaxRequests = 8192;
 constexpr int kMaxIndexHeads = 64;
+constexpr int kMaxRows = 1 << 22;      // rows of one msa_select_rows call
 constexpr int kDefaultCtaBound = 1024; // workspace bound on default persistent decode CTAs
 
 // Bits of the workspace error word.
@@ -117,6 +118,9 @@ cudaError_t launch_select(const SelectParams &p, cudaStream_t stream, bool pdl);
 cudaError_t launch_sparse_decode(const DecodeParams &p, const void *kv_pool, int kv_dtype,
                                  int ctas, cudaStream_t stream, bool pdl);
 cudaError_t launch_kv_update(const UpdateParams &p, cudaStream_t stream);
+// Tables of many rows from a head-major score buffer [Hs][maxB][T] (maxB <= 2048).
+constexpr int kMaxRowSelectBlocks = 2048;
+cudaError_t launch_select_rows(const SelectParams &p, cudaStream_t stream);
 
 __host__ __device__ constexpr size_t align_to(size_t v, size_t a)
 {

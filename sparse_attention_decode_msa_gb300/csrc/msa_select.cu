@@ -212,6 +212,47 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(const SelectPa
 constexpr int kWarpSelWarps = 4;
 constexpr int kWarpSelMaxN = 2048;
 
+// The k largest of a warp's row of keys (lane holds keys of blocks lane,
+// lane + 32, ...; 0 below every candidate), ties to the smaller block:
+// out[0..k) ascending.  Requires more than k candidate blocks.
+template <int S>
+__device__ __forceinline__ void warp_select_keys(const uint32_t (&key)[S], int k, int32_t *out)
+{
+    const int lane = threadIdx.x & 31;
+    uint32_t theta = 0;
+#pragma unroll 1
+    for (int bit = 31; bit >= 0; --bit) {
+        const uint32_t cand = theta | (1u << bit);
+        int c0 = 0, c1 = 0;
+#pragma unroll
+        for (int s = 0; s < S; s += 2) {
+            c0 += key[s] >= cand;
+            c1 += key[s + 1] >= cand;
+        }
+        if ((int)__reduce_add_sync(0xffffffffu, (unsigned)(c0 + c1)) >= k)
+            theta = cand;
+    }
+    int gt = 0;
+#pragma unroll
+    for (int s = 0; s < S; ++s)
+        gt += key[s] > theta;
+    // blocks equal to theta still needed, taken in index order
+    const int need = k - (int)__reduce_add_sync(0xffffffffu, (unsigned)gt);
+    const uint32_t below = (1u << lane) - 1u;
+    int ties = 0, slot = 0;
+#pragma unroll
+    for (int s = 0; s < S; ++s) {
+        const bool eq = key[s] == theta;
+        const uint32_t em = __ballot_sync(0xffffffffu, eq);
+        const bool sel = key[s] > theta || (eq && ties + __popc(em & below) < need);
+        ties += __popc(em);
+        const uint32_t sm = __ballot_sync(0xffffffffu, sel);
+        if (sel)
+            out[slot + __popc(sm & below)] = lane + 32 * s;
+        slot += __popc(sm);
+    }
+}
+
 template <int S> // key slots per lane: rows of up to 32 * S blocks
 __global__ void __launch_bounds__(32 * kWarpSelWarps) select_topk_warp_kernel(const SelectParams p)
 {
@@ -248,38 +289,113 @@ __global__ void __launch_bounds__(32 * kWarpSelWarps) select_topk_warp_kernel(co
         // blocks past n take key 0, below every candidate tried (all >= 1)
         key[s] = b < n ? row_key(p, row, b, n) : 0u;
     }
-    uint32_t theta = 0;
-#pragma unroll 1
-    for (int bit = 31; bit >= 0; --bit) {
-        const uint32_t cand = theta | (1u << bit);
-        int c0 = 0, c1 = 0;
-#pragma unroll
-        for (int s = 0; s < S; s += 2) {
-            c0 += key[s] >= cand;
-            c1 += key[s + 1] >= cand;
+    warp_select_keys<S>(key, p.k, out);
+}
+
+// ---- many query rows from a head-major score buffer -------------------------
+//
+// "Add Rubin (sm_107) MiniMax-M3.1 low-latency decode targets", prefill-select
+// commit: context rows take a tile select, one CTA per KV head and 8 queries
+// over a [heads, max_k_tiles, tokens] max-score block, each score sector read
+// once, with the same table bit for bit as the per-token select (tie order,
+// init / local forcing).  Here: block_scores is [Hs][maxB][T] (row index
+// innermost), row t = r * nq + j sees ceil((seq_len + j) / 128) blocks.  The
+// CTA's threads read the 32-byte sector of block b (8 rows' scores) once,
+// transpose the keys into shared memory, and each warp selects its row.
+constexpr int kTileRows = 8;
+
+template <int S>
+__global__ void __launch_bounds__(32 * kTileRows) select_tile_kernel(const SelectParams p)
+{
+    extern __shared__ uint32_t tkeys[]; // [kTileRows][32 * S]
+    __shared__ int s_n[kTileRows];
+    constexpr int W = 32 * S;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int T = p.R * p.nq;
+    const int t0 = blockIdx.x * kTileRows, gs = blockIdx.y;
+    if (threadIdx.x < kTileRows) {
+        const int t = t0 + threadIdx.x;
+        int n = 0; // rows past T: none
+        if (t < T) {
+            const int r = t / p.nq, j = t - r * p.nq;
+            const int seq_len = p.seq_lens[r];
+            const long long nb_req = ((long long)seq_len + p.nq - 1 + kPage - 1) / kPage;
+            n = (seq_len < 1 || nb_req > p.maxB) ? -1 : ceil_div(seq_len + j, kPage);
         }
-        if ((int)__reduce_add_sync(0xffffffffu, (unsigned)(c0 + c1)) >= p.k)
-            theta = cand;
+        s_n[threadIdx.x] = n;
     }
-    int gt = 0;
+    __syncthreads();
+    int n_max = 0;
 #pragma unroll
-    for (int s = 0; s < S; ++s)
-        gt += key[s] > theta;
-    // blocks equal to theta still needed, taken in index order
-    const int need = p.k - (int)__reduce_add_sync(0xffffffffu, (unsigned)gt);
-    const uint32_t below = (1u << lane) - 1u;
-    int ties = 0, slot = 0;
+    for (int i = 0; i < kTileRows; ++i)
+        n_max = max(n_max, s_n[i]);
+    const float *tile = p.block_scores + (size_t)gs * p.maxB * T + t0;
+    const bool full = t0 + kTileRows <= T && (T & 3) == 0; // two aligned float4 per sector
+    for (int b = threadIdx.x; b < n_max; b += 32 * kTileRows) {
+        const float *src = tile + (size_t)b * T;
+        float v[kTileRows];
+        if (full) {
+            const float4 a = __ldg(reinterpret_cast<const float4 *>(src));
+            const float4 c = __ldg(reinterpret_cast<const float4 *>(src) + 1);
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+            v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < kTileRows; ++i)
+                v[i] = t0 + i < T ? __ldg(src + i) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < kTileRows; ++i) {
+            const int n = s_n[i];
+            uint32_t k = 0u; // past the row's visible blocks: below every candidate
+            if (b < n)
+                k = (b < p.init || b >= n - p.local) ? 0xFFFFFFFFu : order_key(v[i]);
+            tkeys[i * W + b] = k;
+        }
+    }
+    __syncthreads();
+    const int t = t0 + w;
+    if (t >= T)
+        return;
+    int32_t *out = p.selected + ((size_t)t * p.Hs + gs) * p.k;
+    const int n = s_n[w];
+    if (n < 0) {
+        if (lane == 0)
+            set_error(p.err, kErrSeqLen);
+        for (int i = lane; i < p.k; i += 32)
+            out[i] = -1;
+        return;
+    }
+    if (n <= p.k) {
+        for (int i = lane; i < p.k; i += 32)
+            out[i] = i < n ? i : -1;
+        return;
+    }
+    uint32_t key[S];
 #pragma unroll
     for (int s = 0; s < S; ++s) {
-        const bool eq = key[s] == theta;
-        const uint32_t em = __ballot_sync(0xffffffffu, eq);
-        const bool sel = key[s] > theta || (eq && ties + __popc(em & below) < need);
-        ties += __popc(em);
-        const uint32_t sm = __ballot_sync(0xffffffffu, sel);
-        if (sel)
-            out[slot + __popc(sm & below)] = lane + 32 * s;
-        slot += __popc(sm);
+        const int b = lane + 32 * s;
+        key[s] = b < n ? tkeys[w * W + b] : 0u;
     }
+    warp_select_keys<S>(key, p.k, out);
+}
+
+template <int S>
+cudaError_t launch_tile_t(const SelectParams &p, cudaStream_t stream)
+{
+    const size_t smem = sizeof(uint32_t) * kTileRows * 32 * S;
+    if (smem > 48 * 1024) {
+        const cudaError_t e = cudaFuncSetAttribute(select_tile_kernel<S>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess)
+            return e;
+    }
+    const int T = p.R * p.nq;
+    const dim3 grid((T + kTileRows - 1) / kTileRows, p.Hs), block(32 * kTileRows);
+    const cudaError_t e = launch_kernel(select_tile_kernel<S>, grid, block, smem, stream, false, p);
+    if (e != cudaSuccess)
+        return e;
+    return cudaGetLastError();
 }
 
 } // namespace
@@ -313,6 +429,21 @@ cudaError_t launch_select(const SelectParams &p, cudaStream_t stream, bool pdl)
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();
+}
+
+} // namespace msa
+
+namespace msa {
+
+cudaError_t launch_select_rows(const SelectParams &p, cudaStream_t stream)
+{
+    if (p.maxB <= 256)
+        return launch_tile_t<8>(p, stream);
+    if (p.maxB <= 512)
+        return launch_tile_t<16>(p, stream);
+    if (p.maxB <= 1024)
+        return launch_tile_t<32>(p, stream);
+    return launch_tile_t<64>(p, stream);
 }
 
 } // namespace msa

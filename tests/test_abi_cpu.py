@@ -140,3 +140,13 @@ def test_index_heads_per_kv_head_grow_the_score_and_table_buffers(lib):
     T, maxB, k = 32, 256, 16
     assert per_kv >= one + 3 * T * maxB * 4 + 3 * T * k * 4 - 2 * 256
     assert two_per_kv >= per_kv + 4 * T * maxB * 4 - 256
+
+
+def test_row_select_validation(lib):
+    ok = shape(num_requests=1, q_per_req=5000, max_blocks_per_seq=2048)
+    assert msa.msa_workspace_bytes(ok) == 0          # too many rows for the decode's tiles
+    st = lib.msa_select_rows(msa.ctypes.byref(ok), None, None, None, None, 0, None)
+    assert st == msa.MSA_ERR_INVALID_ARGUMENT        # the shape passes; the pointers do not
+    wide = shape(num_requests=1, q_per_req=5000, max_blocks_per_seq=2049)
+    st = lib.msa_select_rows(msa.ctypes.byref(wide), None, None, None, None, 0, None)
+    assert st == msa.MSA_ERR_UNSUPPORTED
