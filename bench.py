@@ -195,7 +195,8 @@ def algorithmic_bytes(pb, selected: np.ndarray) -> dict:
     ctx = pb.contexts
     per_tok = 256 if pb.index_dtype == "bf16" else 64 + 8
     index = int(ctx.sum()) * per_tok
-    page_head = 2 * 128 * 128 * (2 if pb.kv_dtype == "bf16" else 1)
+    page_head = {"bf16": 2 * 128 * 128 * 2, "fp8": 2 * 128 * 128,
+                 "nvfp4": 2 * (128 * 64 + 128 * 8)}[pb.kv_dtype]
     union_pages = 0
     for r in range(pb.num_requests):
         rows = selected[r * pb.q_per_req:(r + 1) * pb.q_per_req].ravel()

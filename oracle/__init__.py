@@ -120,8 +120,9 @@ def shape_of(pb) -> OracleShape:
     return OracleShape(
         num_requests=pb.num_requests, q_per_req=pb.q_per_req, num_q_heads=pb.num_q_heads,
         num_kv_heads=pb.num_kv_heads, head_dim=pb.q.shape[-1], index_dim=pb.q_idx.shape[-1],
-        page_size=pb.kv_pool.shape[3], num_pages=pb.num_pages, max_blocks=pb.max_blocks,
-        topk=pb.topk, kv_fp8=int(pb.kv_dtype == "fp8"), index_nvfp4=int(pb.index_dtype == "nvfp4"),
+        page_size=128, num_pages=pb.num_pages, max_blocks=pb.max_blocks,
+        topk=pb.topk, kv_fp8={"bf16": 0, "fp8": 1, "nvfp4": 2}[pb.kv_dtype],
+        index_nvfp4=int(pb.index_dtype == "nvfp4"),
         softmax_scale=pb.softmax_scale, k_scale=pb.k_scale, v_scale=pb.v_scale,
         num_index_heads=pb.num_index_heads, init_blocks=pb.init_blocks,
         local_blocks=pb.local_blocks,

@@ -55,7 +55,7 @@ typedef struct oracle_shape {
     int32_t num_pages;
     int32_t max_blocks;
     int32_t topk;
-    int32_t kv_fp8;      /* 0: bf16 K/V; 1: E4M3 K/V with per-tensor scales */
+    int32_t kv_fp8;      /* 0: bf16 K/V; 1: E4M3 K/V with per-tensor scales; 2: NVFP4 K/V */
     int32_t index_nvfp4; /* 0: bf16 index keys; 1: NVFP4 codes + E4M3 scales */
     double softmax_scale;
     double k_scale;
@@ -196,11 +196,31 @@ static double index_key(const oracle_shape *s, const void *pool, const uint8_t *
     return oracle_e2m1(code) * scale;
 }
 
+/* Bytes of one NVFP4 K or V tile (one page, one KV head): e2m1 codes
+ * [P][D/2] then E4M3 scales [P][D/16]. */
+static int64_t nvfp4_tile_bytes(const oracle_shape *s)
+{
+    return (int64_t)s->page_size * (s->head_dim / 2 + s->head_dim / 16);
+}
+
+/* Element d of token tok of the K (kv = 0) or V (kv = 1) page of KV head g.
+ * READING for NVFP4 K/V (the pages name the dtype, "Q8KV4", and give no
+ * layout): the K tile of (page, g) then the V tiles, as for bf16 / FP8, each
+ * tile [P][D/2] e2m1 pairs (dimension 2i in the low nibble) followed by
+ * [P][D/16] E4M3 scales, one per 16 consecutive dimensions; k_scale and
+ * v_scale are the second-level (per-tensor) scales. */
 static double kv_elem(const oracle_shape *s, const void *kv_pool, int64_t page, int kv, int g,
                       int tok, int d)
 {
-    int64_t idx = (((page * 2 + kv) * s->num_kv_heads + g) * (int64_t)s->page_size + tok)
-                      * s->head_dim + d;
+    int64_t tile = (page * 2 + kv) * s->num_kv_heads + g;
+    if (s->kv_fp8 == 2) {
+        const uint8_t *t = (const uint8_t *)kv_pool + tile * nvfp4_tile_bytes(s);
+        uint8_t byte = t[(int64_t)tok * (s->head_dim / 2) + d / 2];
+        uint8_t code = (d & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
+        uint8_t sc = t[(int64_t)s->page_size * (s->head_dim / 2) + (int64_t)tok * (s->head_dim / 16) + d / 16];
+        return oracle_e2m1(code) * oracle_e4m3(sc) * (kv ? s->v_scale : s->k_scale);
+    }
+    int64_t idx = (tile * (int64_t)s->page_size + tok) * s->head_dim + d;
     if (!s->kv_fp8)
         return oracle_bf16(((const uint16_t *)kv_pool)[idx]);
     return oracle_e4m3(((const uint8_t *)kv_pool)[idx]) * (kv ? s->v_scale : s->k_scale);
@@ -492,6 +512,30 @@ int oracle_attend(const oracle_shape *s, const uint16_t *q, const void *kv_pool,
 
 /* ---- (d) KV / index-key update ------------------------------------------ */
 
+/* One row of n bf16 values x (each divided by `scale` first, in binary32)
+ * as NVFP4: per group of 16, scale code c = e4m3(amax / 6), codes
+ * e2m1(y / value(c)) (0 when value(c) = 0), quotients in binary32,
+ * dimension 2i in the low nibble of codes[i]. */
+static void nvfp4_group_row(const uint16_t *x, int n, float scale, uint8_t *codes, uint8_t *scales)
+{
+    for (int grp = 0; grp < n / 16; ++grp) {
+        float y[16], amax = 0.0f;
+        for (int i = 0; i < 16; ++i) {
+            y[i] = (float)oracle_bf16(x[16 * grp + i]) / scale;
+            if (fabsf(y[i]) > amax)
+                amax = fabsf(y[i]);
+        }
+        uint8_t sc = oracle_encode_e4m3((double)(amax / 6.0f));
+        scales[grp] = sc;
+        float S = (float)oracle_e4m3(sc);
+        for (int i = 0; i < 16; i += 2) {
+            uint8_t lo = S > 0.0f ? oracle_encode_e2m1((double)(y[i] / S)) : 0;
+            uint8_t hi = S > 0.0f ? oracle_encode_e2m1((double)(y[i + 1] / S)) : 0;
+            codes[8 * grp + i / 2] = (uint8_t)(lo | (hi << 4));
+        }
+    }
+}
+
 /* Writes this step's keys, values and index keys into their pages, in place.
  * [M3-DECODE] "The TP4 decode target": the attention megakernels carry "the
  * KV update"; [M31-RUBIN] q8kv4 indexer commit: the NVFP4 index-K copy is
@@ -504,6 +548,8 @@ int oracle_attend(const oracle_shape *s, const uint16_t *q, const void *kv_pool,
  *   - FP8 pools: code = e4m3(x / k_scale) for K and e4m3(x / v_scale) for V,
  *     the quotient in binary32 (the pages fix no precision; binary32 is the
  *     kernel's, so both sides take the rounding decision alike);
+ *   - NVFP4 K / V pools: y = x / k_scale (x / v_scale) in binary32, then the
+ *     index keys' group recipe below on y;
  *   - NVFP4 index keys, per group of 16 consecutive dimensions: scale code
  *     c = e4m3(amax / 6) with amax the largest |x| of the group and 6 the
  *     largest e2m1 magnitude, S its value, element codes e2m1(x / S) (0 when
@@ -531,6 +577,17 @@ int oracle_kv_update(const oracle_shape *s, const uint16_t *k_new, const uint16_
         for (int kv = 0; kv < 2; ++kv) {
             const uint16_t *src = kv ? v_new : k_new;
             float scale = (float)(kv ? s->v_scale : s->k_scale);
+            if (s->kv_fp8 == 2) {
+                /* NVFP4 K / V: the group recipe of the index keys below on
+                 * y = x / scale (binary32) */
+                for (int g = 0; g < Hkv; ++g) {
+                    uint8_t *tile = (uint8_t *)kv_pool + ((page * 2 + kv) * Hkv + g) * nvfp4_tile_bytes(s);
+                    const uint16_t *x = src + ((int64_t)t * Hkv + g) * D;
+                    nvfp4_group_row(x, D, scale, tile + (int64_t)row * (D / 2),
+                                    tile + (int64_t)P * (D / 2) + (int64_t)row * (D / 16));
+                }
+                continue;
+            }
             for (int g = 0; g < Hkv; ++g)
                 for (int d = 0; d < D; ++d) {
                     uint16_t bits = src[((int64_t)t * Hkv + g) * D + d];
@@ -550,23 +607,8 @@ int oracle_kv_update(const oracle_shape *s, const uint16_t *k_new, const uint16_
                     ((uint16_t *)idxk_pool)[prow * Di + d] = src[d];
                 continue;
             }
-            uint8_t *codes = (uint8_t *)idxk_pool + prow * (Di / 2);
-            for (int grp = 0; grp < Di / 16; ++grp) {
-                float amax = 0.0f;
-                for (int d = 16 * grp; d < 16 * grp + 16; ++d) {
-                    float a = fabsf((float)oracle_bf16(src[d]));
-                    if (a > amax)
-                        amax = a;
-                }
-                uint8_t sc = oracle_encode_e4m3((double)(amax / 6.0f));
-                idxk_scales[prow * (Di / 16) + grp] = sc;
-                float S = (float)oracle_e4m3(sc);
-                for (int d = 16 * grp; d < 16 * grp + 16; d += 2) {
-                    uint8_t lo = S > 0.0f ? oracle_encode_e2m1((double)((float)oracle_bf16(src[d]) / S)) : 0;
-                    uint8_t hi = S > 0.0f ? oracle_encode_e2m1((double)((float)oracle_bf16(src[d + 1]) / S)) : 0;
-                    codes[d / 2] = (uint8_t)(lo | (hi << 4)); /* dimension 2i: low nibble */
-                }
-            }
+            nvfp4_group_row(src, Di, 1.0f, (uint8_t *)idxk_pool + prow * (Di / 2),
+                            idxk_scales + prow * (Di / 16));
         }
     }
     return ORACLE_OK;

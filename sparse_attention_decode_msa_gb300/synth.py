@@ -16,6 +16,10 @@ Layouts (all C-contiguous, element types as stored):
     q            uint16 (bf16 bits)  [T, Hq, 128]
     kv_pool      bf16: uint16 / fp8: uint8 (E4M3)
                                      [num_pages, 2 (K then V), Hkv, 128 tokens, 128 dims]
+                 nvfp4: uint8        [num_pages, 2, Hkv, 9216]: per (page, K/V, KV head) a
+                                     tile of e2m1 pairs [128 tokens][64] (dimension 2i in
+                                     the low nibble) then E4M3 scales [128 tokens][8], one
+                                     per 16 dimensions; k_scale / v_scale are the tensor scales
     block_table  int32               [R, max_blocks]; entries past a request's last
                                      cached block are -1 and are never read
     seq_lens     int32               [R]; query token j of request r sees positions
@@ -274,6 +278,20 @@ def make_problem(
         k_scale = v_scale = s
         _fill_chunked(kv, lambda n: codes[_u16(rng, n * per_page)].reshape((n,) + kv_shape[1:]),
                       256)
+    elif kv_dtype == NVFP4:
+        tile = PAGE * HEAD_DIM // 2 + PAGE * HEAD_DIM // 16
+        kv = np.empty((num_pages, 2, Hkv, tile), dtype=np.uint8)
+
+        def nvfp4_tiles(n):
+            # e2m1 codes uniform over the 16 codes; scales 2^e, e uniform in [-4, 0]
+            t = np.empty((n, 2, Hkv, tile), dtype=np.uint8)
+            t[..., : PAGE * HEAD_DIM // 2] = rng.integers(0, 256, size=(n, 2, Hkv, PAGE * HEAD_DIM // 2),
+                                                          dtype=np.uint8)
+            e = rng.integers(-4, 1, size=(n, 2, Hkv, PAGE * HEAD_DIM // 16))
+            t[..., PAGE * HEAD_DIM // 2:] = ((e + 7) << 3).astype(np.uint8)
+            return t
+
+        _fill_chunked(kv, nvfp4_tiles, 256)
     else:
         raise ValueError(kv_dtype)
 

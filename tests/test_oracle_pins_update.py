@@ -171,3 +171,62 @@ def test_nvfp4_update_of_representable_values_is_lossless():
         mask[page, :, row] = False
     assert np.array_equal(res["idxk_pool"][mask], pb.idxk_pool[mask])
     assert np.array_equal(res["idxk_scales"][mask], pb.idxk_scales[mask])
+
+
+# ---------------------------------------------------------------------------
+# NVFP4 K / V (decode and update)
+
+def nvfp4_kv_f64(pb, page, kv, g):
+    """[128, 128] float64 values of one NVFP4 K or V tile, decoded with the
+    OCP e2m1 table and torch's E4M3 decode, times the tensor scale."""
+    table = e2m1_table()
+    tile = pb.kv_pool[page, kv, g]
+    by = tile[: P * 64].reshape(P, 64).astype(int)
+    codes = np.empty((P, 128), dtype=int)
+    codes[:, 0::2], codes[:, 1::2] = by & 15, by >> 4
+    sc = torch_e4m3_values(tile[P * 64:].reshape(P, 8))
+    vals = np.vectorize(table.get)(codes).astype(np.float64) * np.repeat(sc, 16, axis=1)
+    return vals * (pb.v_scale if kv else pb.k_scale)
+
+
+def test_nvfp4_kv_dense_attention_equals_sdpa():
+    # k >= visible blocks: dense causal attention over torch-decoded K and V
+    pb = synth.make_problem(name="f4kv", contexts=[700, 300], q_per_req=2, num_kv_heads=2,
+                            topk=8, kv_dtype=synth.NVFP4, seed=15)
+    pb.k_scale, pb.v_scale = 0.5, 2.0
+    res = oracle.decode_step(pb)
+    for t in range(pb.num_tokens):
+        r = t // pb.q_per_req
+        L = pb.visible(t)
+        nb = (L + P - 1) // P
+        for h in range(pb.num_q_heads):
+            g = h // 16
+            K = np.concatenate([nvfp4_kv_f64(pb, pb.block_table[r, b], 0, g) for b in range(nb)])[:L]
+            V = np.concatenate([nvfp4_kv_f64(pb, pb.block_table[r, b], 1, g) for b in range(nb)])[:L]
+            q = torch.from_numpy(synth.bf16_bits_to_f32(pb.q[t, h]).astype(np.float64))
+            o = torch.nn.functional.scaled_dot_product_attention(
+                q[None, None, None], torch.from_numpy(K)[None, None], torch.from_numpy(V)[None, None],
+                scale=pb.softmax_scale)[0, 0, 0].numpy()
+            assert np.allclose(res["out"][t, h], o, rtol=0, atol=1e-12), (t, h)
+
+
+def test_nvfp4_kv_update_of_representable_values_is_lossless():
+    pb = synth.make_problem(name="f4upd", contexts=[500, 129], q_per_req=2, num_kv_heads=2,
+                            topk=2, kv_dtype=synth.NVFP4, seed=16)
+    pb.k_scale, pb.v_scale = 0.25, 4.0
+    upd = synth.make_update(pb, exact_nvfp4=True)
+    # K / V inputs the format holds exactly after division by the tensor scale
+    rng = np.random.default_rng(3)
+    for name, scale in (("k_new", pb.k_scale), ("v_new", pb.v_scale)):
+        groups = upd[name].shape[:-1] + (8, 16)
+        mag = synth._E2M1_MAGNITUDES[rng.integers(0, 8, size=groups)]
+        mag[..., 0] = 6.0
+        x = mag * np.exp2(rng.integers(-4, 5, size=groups[:-1] + (1,))) * scale
+        upd[name] = synth.f32_to_bf16_bits(x.reshape(upd[name].shape).astype(np.float32))
+    new = oracle.kv_update(pb, upd["k_new"], upd["v_new"], upd["idxk_new"])
+    after = synth.Problem(**{**pb.__dict__, "kv_pool": new["kv_pool"]})
+    for t, page, row in new_positions(pb):
+        for kv, name in ((0, "k_new"), (1, "v_new")):
+            for g in range(pb.num_kv_heads):
+                got = nvfp4_kv_f64(after, page, kv, g)[row]
+                assert np.array_equal(got, synth.bf16_bits_to_f32(upd[name][t, g])), (t, kv, g)
