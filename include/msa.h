@@ -46,7 +46,8 @@
  *     other places go to the best block scores as above;
  *   - logits are softmax_scale * q . k (FP8 keys times k_scale), the output
  *     is the softmax-weighted mean of V (FP8 values times v_scale), and
- *     lse = ln(sum exp(logit)) (natural log);
+ *     lse = ln(sum exp(logit)) (natural log); NVFP4 keys and values are
+ *     e2m1 x E4M3 scale x the tensor scale (k_scale, v_scale);
  *   - NVFP4 index keys: dimension 2i is the low nibble of byte i, one E4M3
  *     scale per 16 consecutive dimensions, no global scale.
  *
@@ -75,7 +76,11 @@
  *   idxk_scales  MSA_NVFP4 only: E4M3 [num_pages][Hi][P][Di/16], else NULL
  *   q            bf16 [T][Hq][D]
  *   kv_pool      MSA_BF16 or MSA_FP8_E4M3 [num_pages][2][Hkv][P][D]: the K
- *                page of KV head g of page p, then the V pages after all K
+ *                page of KV head g of page p, then the V pages after all K;
+ *                MSA_NVFP4 [num_pages][2][Hkv] tiles of 9216 bytes: e2m1
+ *                pairs [P][D/2] (dimension 2i in the low nibble) then E4M3
+ *                scales [P][D/16], one per 16 dimensions; k_scale and
+ *                v_scale are the tensor (second-level) scales
  *   block_table  int32 [num_requests][max_blocks_per_seq]; entry b of row r
  *                is the page of logical block b of request r.  Only blocks
  *                b < ceil((seq_lens[r] + q_per_req - 1) / P) are read.
@@ -118,7 +123,7 @@ typedef enum msa_dtype {
  * page_size = 128, num_q_heads = 16 * num_kv_heads, num_index_heads = 1 or
  * a multiple of num_kv_heads up to 64, 1 <= q_per_req <= 64,
  * 1 <= topk <= 256, max_blocks_per_seq <= 16384,
- * num_requests * q_per_req <= 8192, kv_dtype in {BF16, FP8_E4M3},
+ * num_requests * q_per_req <= 8192, kv_dtype in {BF16, FP8_E4M3, NVFP4},
  * index_dtype in {BF16, NVFP4}. */
 typedef struct msa_shape {
     int32_t num_requests;       /* R */
@@ -209,7 +214,8 @@ msa_status msa_decode_step(const msa_shape *shape, const void *q_idx, const void
  * position it sees): row (pos % 128) of page block_table[r][pos / 128].
  * Only those rows are written.  Encodings: bf16 pools take the inputs as
  * they are; MSA_FP8_E4M3 pools store E4M3(x / k_scale) for K and
- * E4M3(x / v_scale) for V; MSA_NVFP4 index keys store, per 16 consecutive
+ * E4M3(x / v_scale) for V; MSA_NVFP4 K / V pools store y = x / k_scale
+ * (x / v_scale) by the index keys' recipe; MSA_NVFP4 index keys store, per 16 consecutive
  * dimensions, the E4M3 scale c = E4M3(max |x| / 6) and the e2m1 codes of
  * x / value(c) (0 when c is 0), dimension 2i in the low nibble.  Every
  * rounding is to nearest even and saturating, quotients in fp32, and a code

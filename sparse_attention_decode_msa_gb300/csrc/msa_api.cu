@@ -51,7 +51,7 @@ msa_status check_shape(const msa_shape *s, bool many_rows = false)
         return MSA_ERR_UNSUPPORTED;
     if (s->topk > kMaxTopk || s->max_blocks_per_seq > kMaxBlocks || s->num_requests > kMaxRequests)
         return MSA_ERR_UNSUPPORTED;
-    if (s->kv_dtype != MSA_BF16 && s->kv_dtype != MSA_FP8_E4M3)
+    if (s->kv_dtype != MSA_BF16 && s->kv_dtype != MSA_FP8_E4M3 && s->kv_dtype != MSA_NVFP4)
         return MSA_ERR_UNSUPPORTED;
     if (s->index_dtype != MSA_BF16 && s->index_dtype != MSA_NVFP4)
         return MSA_ERR_UNSUPPORTED;
@@ -202,9 +202,9 @@ msa_status decode_impl(const msa_shape *s, const void *q, const void *kv_pool,
     p.k = s->topk;
     p.num_pages = s->num_pages;
     p.Hs = selection_heads(s);
-    const bool fp8 = s->kv_dtype == MSA_FP8_E4M3;
-    p.scale_log2 = s->softmax_scale * 1.4426950408889634f * (fp8 ? s->k_scale : 1.f);
-    p.v_scale = fp8 ? s->v_scale : 1.f;
+    const bool scaled = s->kv_dtype != MSA_BF16; // E4M3 and NVFP4 carry tensor scales
+    p.scale_log2 = s->softmax_scale * 1.4426950408889634f * (scaled ? s->k_scale : 1.f);
+    p.v_scale = scaled ? s->v_scale : 1.f;
     int ctas = s->decode_ctas;
     if (ctas == 0) {
         const int sms = num_sms_current();
@@ -377,10 +377,11 @@ msa_status msa_kv_update(const msa_shape *shape, const void *k_new, const void *
     p.maxB = shape->max_blocks_per_seq;
     p.num_pages = shape->num_pages;
     p.kv_fp8 = shape->kv_dtype == MSA_FP8_E4M3;
+    p.kv_nvfp4 = shape->kv_dtype == MSA_NVFP4;
     p.idx_nvfp4 = nvfp4;
     p.k_scale = shape->k_scale;
     p.v_scale = shape->v_scale;
-    if (p.kv_fp8 && !(shape->k_scale > 0.f && shape->v_scale > 0.f))
+    if ((p.kv_fp8 || p.kv_nvfp4) && !(shape->k_scale > 0.f && shape->v_scale > 0.f))
         return MSA_ERR_INVALID_ARGUMENT;
     return cuda_status(launch_kv_update(p, stream));
 }

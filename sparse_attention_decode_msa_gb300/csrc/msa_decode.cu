@@ -36,6 +36,7 @@
 //   flag that ends every other wait, and the producer waits (bounded) for its
 //   copies in flight before the CTA exits.
 #include <cmath>
+#include <cstring>
 
 #include "msa_internal.cuh"
 
@@ -157,7 +158,12 @@ __device__ int4 make_entry(const DecodeParams &p, long long x, const int *qt)
 
 constexpr int kUSmxWarps = 8;              // softmax warps: two per TMEM lane quarter
 constexpr int kUSoftmax = 32 * kUSmxWarps; // softmax threads
-constexpr int kUThreads = 32 * (2 + kUSmxWarps); // producer, MMA, softmax
+constexpr int kUCvtWarps = 4;              // NVFP4 only: e2m1 x E4M3 -> bf16 converter warps
+// KV formats of the kernel instances
+constexpr int kKvBf16 = 0, kKvFp8 = 1, kKvNvfp4 = 2;
+template <int KVF>
+constexpr int kUThreadsT = 32 * (2 + kUSmxWarps + (KVF == kKvNvfp4 ? kUCvtWarps : 0)); // producer, MMA, softmax[, converters]
+constexpr int kF4Tile = kPage * kDim / 2 + kPage * kDim / 16; // NVFP4 K or V tile: codes then scales
 constexpr int kUQScales = 16;              // FP8: ring of per-unit query scales (> units in flight)
 constexpr float kPScale = 256.f;           // FP8: P^T is stored as 256 * P (E4M3 hi + lo)
 constexpr int kUHeads = 8;                 // heads per softmax thread (half of the group)
@@ -167,25 +173,33 @@ constexpr int kUQTile = 4096;              // 16 query rows of one unit: bf16 (t
 constexpr int kUPTile = 4096;              // P^T of one page, [16 heads][128 tokens]: bf16, or E4M3 hi + lo
 
 struct USmem {
-    size_t ring, qbuf, pbuf, bars, table, xbuf, lbuf, qsc, misc, qt, total;
+    size_t ring, stage, qbuf, pbuf, bars, table, xbuf, lbuf, qsc, misc, qt, total;
 };
 
-// The ring holds the MMA operands as loaded: bf16 tiles (32 KiB) or E4M3
-// tiles (16 KiB, read by the FP8 MMA as they are).
-__host__ __device__ inline USmem umma_layout(int T, int stages, bool fp8)
+// Bytes of one ring tile: bf16 (32 KiB) and E4M3 (16 KiB) tiles are the MMA
+// operands as loaded; NVFP4 tiles (9 KiB) are widened to bf16 staging tiles.
+__host__ __device__ constexpr int ring_tile_bytes(int kvf)
+{
+    return kvf == kKvBf16 ? kUTile : kvf == kKvFp8 ? kUTile / 2 : kF4Tile;
+}
+
+__host__ __device__ inline USmem umma_layout(int T, int stages, int kvf)
 {
     USmem L{};
     size_t off = 0;
     L.ring = off;                          // 1024-aligned tiles
-    off += (size_t)stages * (fp8 ? kUTile / 2 : kUTile);
+    off += (size_t)stages * ring_tile_bytes(kvf);
+    L.stage = off = align_to(off, 1024);   // NVFP4: bf16 K[2], V[2]
+    off += kvf == kKvNvfp4 ? 4 * (size_t)kUTile : 0;
     L.qbuf = off = align_to(off, 1024);    // [2] query tiles (swizzle atoms: 1024-aligned)
     off += 2 * kUQTile;
     L.pbuf = off = align_to(off, 1024);    // [2] P^T tiles
     off += 2 * kUPTile;
     // full[S], empty[S], qfull[2], qempty[2], s_full[2], s_free[2], p_full[2],
-    // p_free[2], o_full[2], o_free[2], softmax sync, done
+    // p_free[2], o_full[2], o_free[2], softmax sync, done, then NVFP4 only:
+    // kst_full[2], kst_empty[2], vst_full[2], vst_empty[2]
     L.bars = off = align_to(off, 8);
-    off += (size_t)(2 * stages + 16 + 2) * 8;
+    off += (size_t)(2 * stages + 16 + 2 + 8) * 8;
     L.table = off = align_to(off, 16);     // [2][kWin] int4
     off += (size_t)2 * kWin * 16;
     L.xbuf = off = align_to(off, 16);      // [2][4 quarters][16] page maxima
@@ -237,17 +251,21 @@ __device__ __forceinline__ void split_e4m3x2(float x0, float x1, uint32_t &hi, u
     lo = f32x2_to_e4m3x2(x1 - h1, x0 - h0);
 }
 
-template <bool FP8, int STAGES>
-__global__ void __launch_bounds__(kUThreads, 1)
+template <int KVF, int STAGES>
+__global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
     sparse_decode_umma_kernel(const __grid_constant__ CUtensorMap kv_map,
                               const __grid_constant__ CUtensorMap q_map, const DecodeParams p)
 {
-    constexpr int kRaw = FP8 ? kUTile / 2 : kUTile; // bytes of one ring tile
+    constexpr bool FP8 = KVF == kKvFp8;
+    constexpr bool F4 = KVF == kKvNvfp4;
+    constexpr int kRaw = ring_tile_bytes(KVF); // bytes of one ring tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const USmem lay = umma_layout(p.T, STAGES, FP8);
+    const USmem lay = umma_layout(p.T, STAGES, KVF);
     uint8_t *ring = base + lay.ring;
+    uint8_t *kst = base + lay.stage;   // NVFP4: [2] bf16 K tiles
+    uint8_t *vst = kst + 2 * kUTile;   // NVFP4: [2] bf16 V tiles
     uint8_t *qbuf = base + lay.qbuf;
     uint8_t *pbuf = base + lay.pbuf;
     uint64_t *full = reinterpret_cast<uint64_t *>(base + lay.bars);
@@ -262,6 +280,10 @@ __global__ void __launch_bounds__(kUThreads, 1)
     uint64_t *o_free = o_full + 2;
     uint64_t *smx_bar = o_free + 2;    // softmax-warps barrier (kUSmxWarps arrivals)
     uint64_t *done_bar = smx_bar + 1;  // softmax warps finished with TMEM (kUSmxWarps arrivals)
+    uint64_t *kst_full = done_bar + 1; // NVFP4: [2] staging K written (kUCvtWarps arrivals)
+    uint64_t *kst_empty = kst_full + 2; // NVFP4: [2] staging K read by the MMA (commit)
+    uint64_t *vst_full = kst_empty + 2; // NVFP4: [2] staging V written
+    uint64_t *vst_empty = vst_full + 2; // NVFP4: [2] staging V read by the MMA
     float *qscale = reinterpret_cast<float *>(base + lay.qsc);
     int4 *table = reinterpret_cast<int4 *>(base + lay.table);
     float *xbuf = reinterpret_cast<float *>(base + lay.xbuf);
@@ -274,11 +296,18 @@ __global__ void __launch_bounds__(kUThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        prefetch_tensormap(&kv_map);
+        if (!F4)
+            prefetch_tensormap(&kv_map);
         prefetch_tensormap(&q_map);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&empty[s]), 1);
+            mbar_init(smem_u32(&empty[s]), F4 ? kUCvtWarps : 1); // NVFP4: freed by the converters
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&kst_full[b]), kUCvtWarps);
+            mbar_init(smem_u32(&kst_empty[b]), 1);
+            mbar_init(smem_u32(&vst_full[b]), kUCvtWarps);
+            mbar_init(smem_u32(&vst_empty[b]), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&qfull[b]), 1);
@@ -342,9 +371,11 @@ __global__ void __launch_bounds__(kUThreads, 1)
             if (!ok)
                 break;
             // The softmax warps trail the MMA warp by up to two tasks and the MMA
-            // warp trails this one by up to kAhead: only kAhead + 3 tasks into
-            // a window has every reader left the window before it.
-            if (l % kWin == kAhead + 3 && l >= kWin && (l / kWin + 1) * kWin < ntasks)
+            // warp trails this one by up to kAhead (kAhead + 2 with the NVFP4
+            // converters and their two staging tiles between them): only
+            // kAhead + 3 (+ 2) tasks into a window has every reader left the
+            // window before it.
+            if (l % kWin == kAhead + 3 + (F4 ? 2 : 0) && l >= kWin && (l / kWin + 1) * kWin < ntasks)
                 fill_window(l / kWin + 1);
             const int4 e = entry(l);
             const int u = unit_of(e);
@@ -435,9 +466,14 @@ __global__ void __launch_bounds__(kUThreads, 1)
                     const uint32_t dst = smem_u32(ring + (size_t)st * kRaw);
                     const int krow = e.x + kv * p.Hkv * kPage;
                     mbar_arrive_expect_tx(bar, kRaw);
-                    tma_load_2d_hint(dst, &kv_map, 0, krow, bar, kv_policy);
-                    if (!FP8)
-                        tma_load_2d_hint(dst + kUTile / 2, &kv_map, 64, krow, bar, kv_policy);
+                    if (F4) { // one contiguous tile: codes then scales
+                        bulk_load_hint(dst, p.kv_raw + (size_t)(krow / kPage) * kF4Tile, kF4Tile, bar,
+                                       kv_policy);
+                    } else {
+                        tma_load_2d_hint(dst, &kv_map, 0, krow, bar, kv_policy);
+                        if (!FP8)
+                            tma_load_2d_hint(dst + kUTile / 2, &kv_map, 64, krow, bar, kv_policy);
+                    }
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -468,7 +504,9 @@ __global__ void __launch_bounds__(kUThreads, 1)
             int s_units = 0, s_unit = -1;
             auto issue_s = [&](int l) -> bool {
                 const int zk = 2 * l, b = l & 1;
-                if (!mbar_wait_or_abort(smem_u32(&full[zk % STAGES]), (zk / STAGES) & 1, abort_flag))
+                // NVFP4: K(l) widened into staging tile b; else the ring tile landed
+                if (F4 ? !mbar_wait_or_abort(smem_u32(&kst_full[b]), (l >> 1) & 1, abort_flag)
+                       : !mbar_wait_or_abort(smem_u32(&full[zk % STAGES]), (zk / STAGES) & 1, abort_flag))
                     return false;
                 const int4 e = entry(l);
                 const int u = unit_of(e);
@@ -483,7 +521,8 @@ __global__ void __launch_bounds__(kUThreads, 1)
                     return false;
                 tcgen05_after_sync();
                 if (e.x >= 0) {
-                    const uint32_t tileK = smem_u32(ring + (size_t)(zk % STAGES) * kRaw);
+                    const uint32_t tileK = F4 ? smem_u32(kst + b * kUTile)
+                                              : smem_u32(ring + (size_t)(zk % STAGES) * kRaw);
                     const uint32_t qtile = smem_u32(qbuf + qb * kUQTile);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
@@ -499,7 +538,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
                     }
                 }
                 umma_commit(smem_u32(&s_full[b]));
-                umma_commit(smem_u32(&empty[zk % STAGES])); // K tile read
+                umma_commit(F4 ? smem_u32(&kst_empty[b]) : smem_u32(&empty[zk % STAGES])); // K tile read
                 // last task of its unit: the query tile can be replaced
                 if (l + 1 == ntasks || unit_of(entry(l + 1)) != u)
                     umma_commit(smem_u32(&qempty[qb]));
@@ -507,7 +546,8 @@ __global__ void __launch_bounds__(kUThreads, 1)
             };
             auto issue_pv = [&](int l) -> bool {
                 const int zv = 2 * l + 1, b = l & 1;
-                if (!mbar_wait_or_abort(smem_u32(&full[zv % STAGES]), (zv / STAGES) & 1, abort_flag))
+                if (F4 ? !mbar_wait_or_abort(smem_u32(&vst_full[b]), (l >> 1) & 1, abort_flag)
+                       : !mbar_wait_or_abort(smem_u32(&full[zv % STAGES]), (zv / STAGES) & 1, abort_flag))
                     return false;
                 if (!mbar_wait_or_abort(smem_u32(&p_full[b]), (l >> 1) & 1, abort_flag))
                     return false;
@@ -515,7 +555,8 @@ __global__ void __launch_bounds__(kUThreads, 1)
                     return false;
                 tcgen05_after_sync();
                 if (entry(l).x >= 0) {
-                    const uint32_t tileV = smem_u32(ring + (size_t)(zv % STAGES) * kRaw);
+                    const uint32_t tileV = F4 ? smem_u32(vst + b * kUTile)
+                                              : smem_u32(ring + (size_t)(zv % STAGES) * kRaw);
                     const uint32_t ptile = smem_u32(pbuf + b * kUPTile);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
@@ -536,7 +577,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
                 }
                 umma_commit(smem_u32(&o_full[b]));
                 umma_commit(smem_u32(&p_free[b]));
-                umma_commit(smem_u32(&empty[zv % STAGES])); // V tile read
+                umma_commit(F4 ? smem_u32(&vst_empty[b]) : smem_u32(&empty[zv % STAGES])); // V tile read
                 return true;
             };
             if (ntasks > 0)
@@ -560,6 +601,81 @@ __global__ void __launch_bounds__(kUThreads, 1)
         __syncwarp();
         tcgen05_after_sync();
         tmem_dealloc(tmem, kUTmemCols);
+        return;
+    }
+
+    if (F4 && warp >= 2 + kUSmxWarps) {
+        // =================== converter warps (NVFP4) ===================
+        // K and V tiles from the ring (e2m1 pairs [128 tok][64 B], then E4M3
+        // scales [128 tok][8]) into the bf16 staging tiles, in the
+        // two-64-dim-box, 128-byte-swizzled layout the MMA descriptors read.
+        // e2m1 x E4M3 has at most 6 significant bits: exact in bf16.  The
+        // tensor scales are folded into the logit scale and the output.
+        const int ct = threadIdx.x - 32 * (2 + kUSmxWarps); // 0..127
+        bool ok = true;
+        // Thread ct widens the 16 dimensions gch = ct % 8 of rows ct / 8 + 16 i,
+        // i < 8; all loads before the first convert.
+        const int gch = ct & 7, r0 = ct >> 3, sw = r0 & 7; // r & 7 == sw for every row of the thread
+        const int box = gch >> 2, c0 = 2 * (gch & 3);      // 64-dim box and its first 16-byte chunk
+        auto convert = [&](const uint8_t *raw, uint8_t *dst) {
+            uint2 cw[8];
+            uint32_t sc[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = r0 + 16 * i;
+                cw[i] = *reinterpret_cast<const uint2 *>(raw + r * 64 + gch * 8);
+                sc[i] = raw[kPage * 64 + r * 8 + gch];
+            }
+            uint8_t *lo_dst = dst + box * (kUTile / 2) + ((c0 ^ sw) << 4);
+            uint8_t *hi_dst = dst + box * (kUTile / 2) + (((c0 + 1) ^ sw) << 4);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float s, unused;
+                f16x2_to_f32x2(e4m3x2_to_f16x2(sc[i]), s, unused);
+                uint32_t w[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) { // byte k: dimensions 2k (low nibble), 2k + 1
+                    const uint32_t word = k < 4 ? cw[i].x : cw[i].y;
+                    float a, b;
+                    f16x2_to_f32x2(e2m1x2_to_f16x2((word >> (8 * (k & 3))) & 0xFFu), a, b);
+                    w[k] = pack_bf16(a * s, b * s);
+                }
+                const int r = r0 + 16 * i;
+                *reinterpret_cast<uint4 *>(lo_dst + r * 128) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4 *>(hi_dst + r * 128) = make_uint4(w[4], w[5], w[6], w[7]);
+            }
+            fence_async_smem();
+        };
+        // K(l + 1) is widened before V(l): the MMA warp issues S(l + 1)
+        // before O(l).
+        auto do_kv = [&](int l, int kv) -> bool {
+            const int z = 2 * l + kv, b = l & 1;
+            uint64_t *st_full = kv ? vst_full : kst_full, *st_empty = kv ? vst_empty : kst_empty;
+            if (!mbar_wait_or_abort(smem_u32(&full[z % STAGES]), (z / STAGES) & 1, abort_flag))
+                return false;
+            if (l >= 2 && !mbar_wait_or_abort(smem_u32(&st_empty[b]), ((l >> 1) - 1) & 1, abort_flag))
+                return false;
+            if (entry(l).x >= 0)
+                convert(ring + (size_t)(z % STAGES) * kRaw, (kv ? vst : kst) + b * kUTile);
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(smem_u32(&st_full[b]));
+                mbar_arrive(smem_u32(&empty[z % STAGES]));
+            }
+            return true;
+        };
+        if (ntasks > 0)
+            ok = do_kv(0, 0);
+        for (int l = 0; l < ntasks && ok; ++l) {
+            if (l + 1 < ntasks)
+                ok = do_kv(l + 1, 0);
+            if (ok)
+                ok = do_kv(l, 1);
+        }
+        if (!ok) {
+            set_error(p.err, kErrTimeout);
+            *abort_flag = 1;
+        }
         return;
     }
 
@@ -961,16 +1077,16 @@ bool encode_q_map(CUtensorMap *map, const void *q, int T, int Hkv)
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool FP8, int STAGES>
+template <int KVF, int STAGES>
 cudaError_t launch_umma_t(const DecodeParams &p, const CUtensorMap &kv, const CUtensorMap &qm,
                           int ctas, cudaStream_t stream, bool pdl)
 {
-    const size_t smem = umma_layout(p.T, STAGES, FP8).total;
-    cudaError_t e = cudaFuncSetAttribute(sparse_decode_umma_kernel<FP8, STAGES>,
+    const size_t smem = umma_layout(p.T, STAGES, KVF).total;
+    cudaError_t e = cudaFuncSetAttribute(sparse_decode_umma_kernel<KVF, STAGES>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
-    e = launch_kernel(sparse_decode_umma_kernel<FP8, STAGES>, dim3(ctas), dim3(kUThreads), smem,
+    e = launch_kernel(sparse_decode_umma_kernel<KVF, STAGES>, dim3(ctas), dim3(kUThreadsT<KVF>), smem,
                       stream, pdl, kv, qm, p);
     if (e != cudaSuccess)
         return e;
@@ -998,19 +1114,27 @@ cudaError_t launch_sparse_decode(const DecodeParams &p, const void *kv_pool, int
                                  cudaStream_t stream, bool pdl)
 {
     CUtensorMap map;
-    if (!encode_kv_map(&map, kv_pool, kv_dtype, p.num_pages, p.Hkv))
+    std::memset(&map, 0, sizeof(map)); // NVFP4 tiles move by bulk copies: no KV tensor map
+    if (kv_dtype != MSA_NVFP4 && !encode_kv_map(&map, kv_pool, kv_dtype, p.num_pages, p.Hkv))
         return cudaErrorInvalidValue;
     CUtensorMap qmap;
     if (!encode_q_map(&qmap, p.q, p.T, p.Hkv))
         return cudaErrorInvalidValue;
-    if (kv_dtype == MSA_FP8_E4M3) {
-        if (umma_layout(p.T, 12, true).total <= (size_t)kMaxSmem)
-            return launch_umma_t<true, 12>(p, map, qmap, ctas, stream, pdl);
-        return launch_umma_t<true, 6>(p, map, qmap, ctas, stream, pdl);
+    DecodeParams q = p;
+    q.kv_raw = static_cast<const uint8_t *>(kv_pool);
+    if (kv_dtype == MSA_NVFP4) {
+        if (umma_layout(p.T, 8, kKvNvfp4).total <= (size_t)kMaxSmem)
+            return launch_umma_t<kKvNvfp4, 8>(q, map, qmap, ctas, stream, pdl);
+        return launch_umma_t<kKvNvfp4, 4>(q, map, qmap, ctas, stream, pdl);
     }
-    if (umma_layout(p.T, 6, false).total <= (size_t)kMaxSmem)
-        return launch_umma_t<false, 6>(p, map, qmap, ctas, stream, pdl);
-    return launch_umma_t<false, 4>(p, map, qmap, ctas, stream, pdl);
+    if (kv_dtype == MSA_FP8_E4M3) {
+        if (umma_layout(p.T, 12, kKvFp8).total <= (size_t)kMaxSmem)
+            return launch_umma_t<kKvFp8, 12>(q, map, qmap, ctas, stream, pdl);
+        return launch_umma_t<kKvFp8, 6>(q, map, qmap, ctas, stream, pdl);
+    }
+    if (umma_layout(p.T, 6, kKvBf16).total <= (size_t)kMaxSmem)
+        return launch_umma_t<kKvBf16, 6>(q, map, qmap, ctas, stream, pdl);
+    return launch_umma_t<kKvBf16, 4>(q, map, qmap, ctas, stream, pdl);
 }
 
 } // namespace msa

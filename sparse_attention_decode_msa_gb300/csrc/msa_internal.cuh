@@ -81,6 +81,7 @@ struct DecodeParams {
     const int32_t *block_table;
     const int32_t *seq_lens;
     const int32_t *selected; // [T][Hs][k]: one table per token (Hs = 1) or per KV head (Hs = Hkv)
+    const uint8_t *kv_raw;   // the KV pool (read by bulk copies for NVFP4 tiles)
     uint16_t *out;           // bf16 bits [T][Hq][D]
     float *lse;              // [T][Hq]
     float *partial;          // slots of kPartialFloats
@@ -98,12 +99,12 @@ struct UpdateParams {
     const uint16_t *idxk_new; // bf16 bits [T][Hi][Di]
     const int32_t *block_table;
     const int32_t *seq_lens;
-    uint8_t *kv_pool;         // [pages][2][Hkv][P][D] bf16 or E4M3
+    uint8_t *kv_pool;         // [pages][2][Hkv][P][D] bf16 or E4M3, or NVFP4 tiles [pages][2][Hkv][9216]
     uint8_t *idxk_pool;       // [pages][Hi][P][Di] bf16, or [pages][Hi][P][Di/2] e2m1 pairs
     uint8_t *idxk_scales;     // NVFP4: E4M3 [pages][Hi][P][Di/16]
     uint32_t *err;
     int R, nq, Hkv, Hi, maxB, num_pages;
-    bool kv_fp8, idx_nvfp4;
+    bool kv_fp8, kv_nvfp4, idx_nvfp4;
     float k_scale, v_scale;
 };
 

@@ -128,9 +128,9 @@ extern "C" msa_status msa_sparse_decode_noalloc(const msa_shape *shape, const vo
     p.k = shape->topk;
     p.num_pages = shape->num_pages;
     p.Hs = shape->num_index_heads == 1 ? 1 : shape->num_kv_heads; // tables per token
-    const bool fp8 = shape->kv_dtype == MSA_FP8_E4M3;
-    p.scale_log2 = shape->softmax_scale * 1.4426950408889634f * (fp8 ? shape->k_scale : 1.f);
-    p.v_scale = fp8 ? shape->v_scale : 1.f;
+    const bool scaled = shape->kv_dtype != MSA_BF16; // E4M3 and NVFP4 carry tensor scales
+    p.scale_log2 = shape->softmax_scale * 1.4426950408889634f * (scaled ? shape->k_scale : 1.f);
+    p.v_scale = scaled ? shape->v_scale : 1.f;
     return launch_sparse_decode(p, kv_pool, shape->kv_dtype, ctas, stream, false) == cudaSuccess
                ? MSA_OK
                : MSA_ERR_CUDA;

@@ -63,6 +63,33 @@ __device__ __forceinline__ uint32_t e2m1x4_rn_sat(float x0, float x1, float x2, 
     return out;
 }
 
+constexpr int kF4KvTile = kPage * kDim / 2 + kPage * kDim / 16; // NVFP4 K or V tile
+
+// One row of 128 bf16 values as NVFP4, warp-wide: lane holds elements
+// 4 lane .. + 3 (v), divides them by `scale`, and writes its 4 codes (2
+// bytes at codes + 2 lane); the group of 16 = lanes 4 q .. 4 q + 3 shares
+// one E4M3 scale, written by lane 4 q at scales[q].
+__device__ __forceinline__ void nvfp4_quad(uint2 v, float scale, uint8_t *codes, uint8_t *scales)
+{
+    const int lane = threadIdx.x & 31;
+    const float x0 = __fdiv_rn(__uint_as_float(v.x << 16), scale);
+    const float x1 = __fdiv_rn(__uint_as_float(v.x & 0xFFFF0000u), scale);
+    const float x2 = __fdiv_rn(__uint_as_float(v.y << 16), scale);
+    const float x3 = __fdiv_rn(__uint_as_float(v.y & 0xFFFF0000u), scale);
+    float amax = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const uint32_t sc = e4m3x2_rn_sat(0.f, __fdiv_rn(amax, 6.f)) & 0xFFu;
+    float S, unused;
+    f16x2_to_f32x2(e4m3x2_to_f16x2(sc), S, unused);
+    uint32_t c = 0;
+    if (S > 0.f)
+        c = e2m1x4_rn_sat(__fdiv_rn(x0, S), __fdiv_rn(x1, S), __fdiv_rn(x2, S), __fdiv_rn(x3, S));
+    *reinterpret_cast<uint16_t *>(codes + 2 * lane) = (uint16_t)c;
+    if ((lane & 3) == 0)
+        scales[lane >> 2] = (uint8_t)sc;
+}
+
 __global__ void __launch_bounds__(32 * kUpdWarps) kv_update_kernel(const UpdateParams p)
 {
     const int lane = threadIdx.x & 31;
@@ -93,6 +120,13 @@ __global__ void __launch_bounds__(32 * kUpdWarps) kv_update_kernel(const UpdateP
         const int kv = kind / p.Hkv, g = kind - kv * p.Hkv;
         const uint16_t *src = (kv ? p.v_new : p.k_new) + ((size_t)t * p.Hkv + g) * kDim;
         const uint2 v = reinterpret_cast<const uint2 *>(src)[lane]; // elements 4 lane .. + 3
+        if (p.kv_nvfp4) { // the tile of (page, K/V, head g): codes [P][64], then scales [P][8]
+            uint8_t *tile = p.kv_pool + (((size_t)page * 2 + kv) * p.Hkv + g) * kF4KvTile;
+            const float s = kv ? p.v_scale : p.k_scale;
+            nvfp4_quad(v, s, tile + (size_t)row * (kDim / 2), tile + (size_t)kPage * (kDim / 2) +
+                                                                  (size_t)row * (kDim / 16));
+            return;
+        }
         const size_t elem = (((size_t)page * 2 + kv) * p.Hkv + g) * (size_t)kPage * kDim +
                             (size_t)row * kDim + 4 * lane;
         if (!p.kv_fp8) {
@@ -116,21 +150,7 @@ __global__ void __launch_bounds__(32 * kUpdWarps) kv_update_kernel(const UpdateP
         *reinterpret_cast<uint2 *>(p.idxk_pool + prow * (kDim * 2) + 8 * lane) = v;
         return;
     }
-    const float x0 = __uint_as_float(v.x << 16), x1 = __uint_as_float(v.x & 0xFFFF0000u);
-    const float x2 = __uint_as_float(v.y << 16), x3 = __uint_as_float(v.y & 0xFFFF0000u);
-    // amax of the group of 16 = lanes 4 q .. 4 q + 3
-    float amax = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    const uint32_t sc = e4m3x2_rn_sat(0.f, __fdiv_rn(amax, 6.f)) & 0xFFu;
-    float S, unused;
-    f16x2_to_f32x2(e4m3x2_to_f16x2(sc), S, unused);
-    uint32_t codes = 0;
-    if (S > 0.f)
-        codes = e2m1x4_rn_sat(__fdiv_rn(x0, S), __fdiv_rn(x1, S), __fdiv_rn(x2, S), __fdiv_rn(x3, S));
-    *reinterpret_cast<uint16_t *>(p.idxk_pool + prow * (kDim / 2) + 2 * lane) = (uint16_t)codes;
-    if ((lane & 3) == 0)
-        p.idxk_scales[prow * (kDim / 16) + (lane >> 2)] = (uint8_t)sc;
+    nvfp4_quad(v, 1.f, p.idxk_pool + prow * (kDim / 2), p.idxk_scales + prow * (kDim / 16));
 }
 
 } // namespace

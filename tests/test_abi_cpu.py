@@ -74,7 +74,7 @@ def test_workspace_bytes_cover_the_layout(lib):
 @pytest.mark.parametrize("field,value", [
     ("head_dim", 64), ("index_dim", 64), ("page_size", 64), ("num_q_heads", 32),
     ("num_index_heads", 2), ("num_index_heads", 6), ("num_index_heads", 128),
-    ("kv_dtype", 2), ("index_dtype", 1), ("q_per_req", 65),
+    ("kv_dtype", 3), ("index_dtype", 1), ("q_per_req", 65),
     ("topk", 257), ("max_blocks_per_seq", 16385),
 ])
 def test_unsupported_shapes_are_rejected(lib, field, value):
