@@ -231,7 +231,7 @@ def run_ours(args, rank, world, local):
     msa.load()
 
     idx = args.config
-    pb = synth.make_workload(idx, seed=idx + 1000 * rank)
+    pb = synth.make_workload(idx, seed=idx + 1000 * rank, kv_dtype=args.kv_dtype)
     base = DeviceProblem(pb, device=f"cuda:{local}")
     base.decode_step()
     torch.cuda.synchronize()
@@ -412,7 +412,7 @@ def run_ours(args, rank, world, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "fp8-e4m3 KV / bf16 Q" if pb.kv_dtype == "fp8" else "bf16",
+        "dtype": {"fp8": "fp8-e4m3 KV / bf16 Q", "nvfp4": "nvfp4 KV / bf16 Q"}.get(pb.kv_dtype, "bf16"),
         "data": "synthetic (seeded; see config.recipe)",
         "config": {
             "workload": f"{pb.name} (workload {idx})",
@@ -500,7 +500,7 @@ def run_reference(args, rank, world, local):
 
     oracle.build()
     idx = args.config
-    pb = synth.make_workload(idx)
+    pb = synth.make_workload(idx, kv_dtype=args.kv_dtype)
     threads = max(1, os.cpu_count() or 1)
     rng = np.random.default_rng(0)
     # size the per-step sample so the whole run stays within ~3 minutes
@@ -540,6 +540,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=1, help="workload 0..4 (default 1: spec-verify)")
+    ap.add_argument("--kv-dtype", choices=["bf16", "fp8", "nvfp4"], default=None,
+                    help="replace the workload's KV dtype (same shapes)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

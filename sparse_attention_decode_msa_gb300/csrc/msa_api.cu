@@ -173,6 +173,7 @@ msa_status select_impl(const msa_shape *s, const float *block_scores, const int3
     p.k = s->topk;
     p.Hi = s->num_index_heads;
     p.Hs = selection_heads(s);
+    p.r = p.Hi / p.Hs;
     p.init = s->init_blocks;
     p.local = s->local_blocks;
     return cuda_status(launch_select(p, stream, pdl));
@@ -414,6 +415,7 @@ msa_status msa_select_rows(const msa_shape *shape, const float *scores_hbt,
     p.k = shape->topk;
     p.Hs = selection_heads(shape);
     p.Hi = p.Hs; // the buffer holds the selection heads' scores already
+    p.r = 1;
     p.init = shape->init_blocks;
     p.local = shape->local_blocks;
     return cuda_status(launch_select_rows(p, stream));

@@ -197,9 +197,9 @@ __host__ __device__ inline USmem umma_layout(int T, int stages, int kvf)
     off += 2 * kUPTile;
     // full[S], empty[S], qfull[2], qempty[2], s_full[2], s_free[2], p_full[2],
     // p_free[2], o_full[2], o_free[2], softmax sync, done, then NVFP4 only:
-    // kst_full[2], kst_empty[2], vst_full[2], vst_empty[2]
+    // kst_full[2], kst_empty[2], vst_full[2], vst_empty[2], qconv[2]
     L.bars = off = align_to(off, 8);
-    off += (size_t)(2 * stages + 16 + 2 + 8) * 8;
+    off += (size_t)(2 * stages + 16 + 2 + 10) * 8;
     L.table = off = align_to(off, 16);     // [2][kWin] int4
     off += (size_t)2 * kWin * 16;
     L.xbuf = off = align_to(off, 16);      // [2][4 quarters][16] page maxima
@@ -284,6 +284,7 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
     uint64_t *kst_empty = kst_full + 2; // NVFP4: [2] staging K read by the MMA (commit)
     uint64_t *vst_full = kst_empty + 2; // NVFP4: [2] staging V written
     uint64_t *vst_empty = vst_full + 2; // NVFP4: [2] staging V read by the MMA
+    uint64_t *qconv = vst_empty + 2;    // NVFP4: [2] query tile widened to f16 (kUCvtWarps)
     float *qscale = reinterpret_cast<float *>(base + lay.qsc);
     int4 *table = reinterpret_cast<int4 *>(base + lay.table);
     float *xbuf = reinterpret_cast<float *>(base + lay.xbuf);
@@ -308,6 +309,7 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
             mbar_init(smem_u32(&kst_empty[b]), 1);
             mbar_init(smem_u32(&vst_full[b]), kUCvtWarps);
             mbar_init(smem_u32(&vst_empty[b]), 1);
+            mbar_init(smem_u32(&qconv[b]), kUCvtWarps);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&qfull[b]), 1);
@@ -496,7 +498,8 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
         // bf16: kind::f16, 8 steps of K = 16.  FP8: kind::f8f6f4 on the E4M3
         // tiles as loaded, 4 steps of K = 32 for each of the hi and lo parts
         // of Q (in S^T) and of P (in O^T); operand types E4M3 = 0.
-        constexpr uint32_t kE4M3 = FP8 ? ~((7u << 7) | (7u << 10)) : ~0u;
+        // NVFP4: kind::f16 with f16 operands (format 0), widened in shared memory
+        constexpr uint32_t kE4M3 = (FP8 || F4) ? ~((7u << 7) | (7u << 10)) : ~0u;
         constexpr uint32_t kIdescS = umma_idesc_bf16(128, 16, 0, 0) & kE4M3; // K and Q^T both K-major
         constexpr uint32_t kIdescO = umma_idesc_bf16(128, 16, 1, 0) & kE4M3; // V^T MN-major, P^T K-major
         bool ok = true;
@@ -511,7 +514,9 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
                 const int4 e = entry(l);
                 const int u = unit_of(e);
                 if (u != s_unit) {
-                    if (!mbar_wait_or_abort(smem_u32(&qfull[s_units & 1]), (s_units >> 1) & 1, abort_flag))
+                    // NVFP4: the converter warps widen the query tile to f16 in place
+                    uint64_t *qready = F4 ? qconv : qfull;
+                    if (!mbar_wait_or_abort(smem_u32(&qready[s_units & 1]), (s_units >> 1) & 1, abort_flag))
                         return false;
                     s_unit = u;
                     ++s_units;
@@ -607,12 +612,16 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
     if (F4 && warp >= 2 + kUSmxWarps) {
         // =================== converter warps (NVFP4) ===================
         // K and V tiles from the ring (e2m1 pairs [128 tok][64 B], then E4M3
-        // scales [128 tok][8]) into the bf16 staging tiles, in the
-        // two-64-dim-box, 128-byte-swizzled layout the MMA descriptors read.
-        // e2m1 x E4M3 has at most 6 significant bits: exact in bf16.  The
-        // tensor scales are folded into the logit scale and the output.
+        // scales [128 tok][8]) into the f16 staging tiles, in the
+        // two-64-dim-box, 128-byte-swizzled layout the MMA descriptors read:
+        // one cvt.f16x2.e2m1x2 and one f16x2 multiply by the scale per two
+        // values.  e2m1 x E4M3 has at most 6 significant bits: exact in f16.
+        // The query tile of each new unit is widened from bf16 to f16 in
+        // place.  The tensor scales are folded into the logit scale and the
+        // output.
         const int ct = threadIdx.x - 32 * (2 + kUSmxWarps); // 0..127
         bool ok = true;
+        int units = 0, cur = -1;
         // Thread ct widens the 16 dimensions gch = ct % 8 of rows ct / 8 + 16 i,
         // i < 8; all loads before the first convert.
         const int gch = ct & 7, r0 = ct >> 3, sw = r0 & 7; // r & 7 == sw for every row of the thread
@@ -630,19 +639,13 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
             uint8_t *hi_dst = dst + box * (kUTile / 2) + (((c0 + 1) ^ sw) << 4);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                float s, unused;
-                f16x2_to_f32x2(e4m3x2_to_f16x2(sc[i]), s, unused);
-                uint32_t w[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) { // byte k: dimensions 2k (low nibble), 2k + 1
-                    const uint32_t word = k < 4 ? cw[i].x : cw[i].y;
-                    float a, b;
-                    f16x2_to_f32x2(e2m1x2_to_f16x2((word >> (8 * (k & 3))) & 0xFFu), a, b);
-                    w[k] = pack_bf16(a * s, b * s);
-                }
+                const uint32_t s2 = e4m3x2_to_f16x2(sc[i] | (sc[i] << 8)); // (scale, scale)
+                uint32_t lo[4], hi[4]; // dimensions 0..7 and 8..15 of the group
+                e2m1x8_scaled_f16x2(cw[i].x, s2, lo);
+                e2m1x8_scaled_f16x2(cw[i].y, s2, hi);
                 const int r = r0 + 16 * i;
-                *reinterpret_cast<uint4 *>(lo_dst + r * 128) = make_uint4(w[0], w[1], w[2], w[3]);
-                *reinterpret_cast<uint4 *>(hi_dst + r * 128) = make_uint4(w[4], w[5], w[6], w[7]);
+                *reinterpret_cast<uint4 *>(lo_dst + r * 128) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                *reinterpret_cast<uint4 *>(hi_dst + r * 128) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
             }
             fence_async_smem();
         };
@@ -653,9 +656,30 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
             uint64_t *st_full = kv ? vst_full : kst_full, *st_empty = kv ? vst_empty : kst_empty;
             if (!mbar_wait_or_abort(smem_u32(&full[z % STAGES]), (z / STAGES) & 1, abort_flag))
                 return false;
+            const int4 e = entry(l);
+            if (kv == 0 && unit_of(e) != cur) {
+                const int qb = units & 1;
+                if (!mbar_wait_or_abort(smem_u32(&qfull[qb]), (units >> 1) & 1, abort_flag))
+                    return false;
+                uint8_t *q = qbuf + qb * kUQTile;
+                for (int i = ct; i < kUQTile / 16; i += 32 * kUCvtWarps) {
+                    uint4 v = reinterpret_cast<uint4 *>(q)[i];
+                    v.x = bf16x2_to_f16x2(v.x);
+                    v.y = bf16x2_to_f16x2(v.y);
+                    v.z = bf16x2_to_f16x2(v.z);
+                    v.w = bf16x2_to_f16x2(v.w);
+                    reinterpret_cast<uint4 *>(q)[i] = v;
+                }
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_u32(&qconv[qb]));
+                cur = unit_of(e);
+                ++units;
+            }
             if (l >= 2 && !mbar_wait_or_abort(smem_u32(&st_empty[b]), ((l >> 1) - 1) & 1, abort_flag))
                 return false;
-            if (entry(l).x >= 0)
+            if (e.x >= 0)
                 convert(ring + (size_t)(z % STAGES) * kRaw, (kv ? vst : kst) + b * kUTile);
             __syncwarp();
             if (lane == 0) {
@@ -966,7 +990,8 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
             for (int h = 0; h < kUHeads; ++h) {
                 const int hh = h0 + h;
                 const uint32_t off = hh * 128 + ((((col >> 3) ^ (hh & 7))) << 4) + (col & 7) * 2;
-                *reinterpret_cast<uint16_t *>(pt + off) = (uint16_t)(pack_bf16(pv[h], 0.f) & 0xFFFFu);
+                *reinterpret_cast<uint16_t *>(pt + off) =
+                    (uint16_t)((F4 ? pack_f16(pv[h], 0.f) : pack_bf16(pv[h], 0.f)) & 0xFFFFu);
             }
             fence_async_smem();
         } else if (live) {

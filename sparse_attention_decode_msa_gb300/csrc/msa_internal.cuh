@@ -74,6 +74,7 @@ struct SelectParams {
     uint32_t *err;
     int R, nq, maxB, k;
     int Hi, Hs, init, local;
+    int r; // index heads per selection head: Hi / Hs
 };
 
 struct DecodeParams {
@@ -552,6 +553,21 @@ __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte)
         : "=r"(out)
         : "r"(byte));
     return out;
+}
+
+// Eight e2m1 codes (one 32-bit word, byte k = codes 2k (low nibble) and
+// 2k + 1) times an f16x2 scale pair: out[k] = f16x2 of the two codes of byte
+// k, each multiplied by s2.  Exact when the products fit f16.
+__device__ __forceinline__ void e2m1x8_scaled_f16x2(uint32_t word, uint32_t s2, uint32_t (&out)[4])
+{
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n .reg .b32 h0, h1, h2, h3;\n"
+        " mov.b32 {b0, b1, b2, b3}, %4;\n"
+        " cvt.rn.f16x2.e2m1x2 h0, b0;\n cvt.rn.f16x2.e2m1x2 h1, b1;\n"
+        " cvt.rn.f16x2.e2m1x2 h2, b2;\n cvt.rn.f16x2.e2m1x2 h3, b3;\n"
+        " mul.rn.f16x2 %0, h0, %5;\n mul.rn.f16x2 %1, h1, %5;\n"
+        " mul.rn.f16x2 %2, h2, %5;\n mul.rn.f16x2 %3, h3, %5;\n}\n"
+        : "=r"(out[0]), "=r"(out[1]), "=r"(out[2]), "=r"(out[3])
+        : "r"(word), "r"(s2));
 }
 
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b)

@@ -70,9 +70,8 @@ __device__ __forceinline__ uint32_t row_key(const SelectParams &p, const float *
 {
     if (b < p.init || b >= n - p.local)
         return 0xFFFFFFFFu;
-    const int r = p.Hi / p.Hs;
     uint32_t k = order_key(row[b]);
-    for (int i = 1; i < r; ++i) {
+    for (int i = 1; i < p.r; ++i) {
         const uint32_t v = order_key(row[(size_t)i * p.maxB + b]);
         k = v > k ? v : k;
     }
@@ -110,7 +109,7 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(const SelectPa
 
     // block_scores come from the previous kernel of the step
     grid_dependency_wait();
-    const float *row = p.block_scores + ((size_t)t * p.Hi + (size_t)gs * (p.Hi / p.Hs)) * p.maxB;
+    const float *row = p.block_scores + ((size_t)t * p.Hi + (size_t)gs * p.r) * p.maxB;
     for (int b = threadIdx.x; b < n; b += kSelThreads)
         keys[b] = row_key(p, row, b, n);
     if (threadIdx.x == 0) {
@@ -281,13 +280,41 @@ __global__ void __launch_bounds__(32 * kWarpSelWarps) select_topk_warp_kernel(co
         return;
     }
     grid_dependency_wait(); // block_scores come from the previous kernel of the step
-    const float *row = p.block_scores + ((size_t)t * p.Hi + (size_t)gs * (p.Hi / p.Hs)) * p.maxB;
+    const float *row = p.block_scores + ((size_t)t * p.Hi + (size_t)gs * p.r) * p.maxB;
+    // every load of the row first, then the group maximum, then the forcing
+    float v[S];
+#pragma unroll
+    for (int s = 0; s < S; ++s) {
+        const int b = lane + 32 * s;
+        v[s] = b < n ? row[b] : 0.f;
+    }
     uint32_t key[S];
 #pragma unroll
     for (int s = 0; s < S; ++s) {
         const int b = lane + 32 * s;
         // blocks past n take key 0, below every candidate tried (all >= 1)
-        key[s] = b < n ? row_key(p, row, b, n) : 0u;
+        key[s] = b < n ? order_key(v[s]) : 0u;
+    }
+    for (int i = 1; i < p.r; ++i) { // the KV head's other index heads
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            const int b = lane + 32 * s;
+            v[s] = b < n ? row[(size_t)i * p.maxB + b] : 0.f;
+        }
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            const int b = lane + 32 * s;
+            const uint32_t k2 = b < n ? order_key(v[s]) : 0u;
+            key[s] = k2 > key[s] ? k2 : key[s];
+        }
+    }
+    if (p.init > 0 || p.local > 0) {
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            const int b = lane + 32 * s;
+            if (b < n && (b < p.init || b >= n - p.local))
+                key[s] = 0xFFFFFFFFu; // forced: above every score
+        }
     }
     warp_select_keys<S>(key, p.k, out);
 }

@@ -346,29 +346,35 @@ RECIPES = {
 }
 
 
-def make_workload(idx: int, seed: Optional[int] = None) -> Problem:
-    """The full-size workload number idx (0..4), seeded with seed (default idx)."""
+def make_workload(idx: int, seed: Optional[int] = None, kv_dtype: Optional[str] = None) -> Problem:
+    """The full-size workload number idx (0..4), seeded with seed (default idx).
+    kv_dtype replaces the workload's KV dtype (same shapes; e.g. NVFP4 KV)."""
     seed = idx if seed is None else seed
     ctx = workload_contexts(idx, np.random.default_rng(10_000 + seed))
     name = WORKLOADS[idx]
     rec = RECIPES[idx]
+    if kv_dtype is not None:
+        name += f"-{kv_dtype}-kv"
+        rec += f"; KV replaced by {kv_dtype}"
+    kv = kv_dtype or BF16
     if idx == 0:
         return make_problem(name=name, contexts=ctx, q_per_req=1, num_kv_heads=1, topk=8,
-                            num_pages=64, max_blocks=32, seed=seed, recipe=rec)
+                            num_pages=64, max_blocks=32, seed=seed, recipe=rec, kv_dtype=kv)
     if idx == 1:
         return make_problem(name=name, contexts=ctx, q_per_req=4, num_kv_heads=4, topk=16,
-                            num_pages=4096, max_blocks=256, seed=seed, recipe=rec)
+                            num_pages=4096, max_blocks=256, seed=seed, recipe=rec, kv_dtype=kv)
     if idx == 2:
         return make_problem(name=name, contexts=ctx, q_per_req=48, num_kv_heads=4, topk=16,
                             index_range=(-1, 1), num_pages=2049, guard_page=True, max_blocks=1024,
-                            seed=seed, recipe=rec)
+                            seed=seed, recipe=rec, kv_dtype=kv)
     if idx == 3:
         return make_problem(name=name, contexts=ctx, q_per_req=1, num_kv_heads=4, topk=16,
-                            kv_dtype=FP8, guard_page=True, max_blocks=512, seed=seed, recipe=rec)
+                            kv_dtype=kv_dtype or FP8, guard_page=True, max_blocks=512, seed=seed,
+                            recipe=rec)
     if idx == 4:
         return make_problem(name=name, contexts=ctx, q_per_req=2, num_kv_heads=4, topk=32,
                             index_dtype=NVFP4, index_range=(-4, 4), num_pages=16385,
-                            guard_page=True, max_blocks=512, seed=seed, recipe=rec)
+                            guard_page=True, max_blocks=512, seed=seed, recipe=rec, kv_dtype=kv)
     raise ValueError(idx)
 
 
