@@ -158,7 +158,7 @@ __device__ int4 make_entry(const DecodeParams &p, long long x, const int *qt)
 
 constexpr int kUSmxWarps = 8;              // softmax warps: two per TMEM lane quarter
 constexpr int kUSoftmax = 32 * kUSmxWarps; // softmax threads
-constexpr int kUCvtWarps = 4;              // NVFP4 only: e2m1 x E4M3 -> bf16 converter warps
+constexpr int kUCvtWarps = 4;              // NVFP4 only: e2m1 x E4M3 -> f16 converter warps
 // KV formats of the kernel instances
 constexpr int kKvBf16 = 0, kKvFp8 = 1, kKvNvfp4 = 2;
 template <int KVF>
