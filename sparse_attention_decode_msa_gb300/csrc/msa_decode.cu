@@ -177,7 +177,7 @@ struct USmem {
 };
 
 // Bytes of one ring tile: bf16 (32 KiB) and E4M3 (16 KiB) tiles are the MMA
-// operands as loaded; NVFP4 tiles (9 KiB) are widened to bf16 staging tiles.
+// operands as loaded; NVFP4 tiles (9 KiB) are widened to f16 staging tiles.
 __host__ __device__ constexpr int ring_tile_bytes(int kvf)
 {
     return kvf == kKvBf16 ? kUTile : kvf == kKvFp8 ? kUTile / 2 : kF4Tile;
