@@ -759,31 +759,41 @@ __global__ void __launch_bounds__(kF4Threads, 1) index_score_fp4_kernel(const Sc
             const uint4 c1 = *reinterpret_cast<const uint4 *>(codes + (row0 + 8) * 64 + 16 * q);
             const uint32_t s0 = *reinterpret_cast<const uint16_t *>(scl + row0 * 8 + 2 * q);
             const uint32_t s1 = *reinterpret_cast<const uint16_t *>(scl + (row0 + 8) * 8 + 2 * q);
+            // the two scales of each row (dims 32q .. +15 and +16 .. +31), as f16 pairs
+            const uint32_t f0[2] = {e4m3x2_to_f16x2((s0 & 0xFFu) * 0x101u), e4m3x2_to_f16x2((s0 >> 8) * 0x101u)};
+            const uint32_t f1[2] = {e4m3x2_to_f16x2((s1 & 0xFFu) * 0x101u), e4m3x2_to_f16x2((s1 >> 8) * 0x101u)};
             uint32_t a[8][4];
 #pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                // bytes 2s, 2s+1 of the 16: dims 32q + 4s .. + 3; scale byte s / 4
-                const uint32_t w0 = (&c0.x)[s >> 1], w1 = (&c1.x)[s >> 1];
-                const int sh = (s & 1) * 16, ssh = (s >> 2) * 8;
-                const uint32_t e0 = (s0 >> ssh) & 0xFFu, e1 = (s1 >> ssh) & 0xFFu;
-                const uint32_t f0 = e4m3x2_to_f16x2(e0 | (e0 << 8));
-                const uint32_t f1 = e4m3x2_to_f16x2(e1 | (e1 << 8));
-                a[s][0] = hmul2_u32(e2m1x2_to_f16x2((w0 >> sh) & 0xFFu), f0);
-                a[s][1] = hmul2_u32(e2m1x2_to_f16x2((w1 >> sh) & 0xFFu), f1);
-                a[s][2] = hmul2_u32(e2m1x2_to_f16x2((w0 >> (sh + 8)) & 0xFFu), f0);
-                a[s][3] = hmul2_u32(e2m1x2_to_f16x2((w1 >> (sh + 8)) & 0xFFu), f1);
+            for (int w = 0; w < 4; ++w) {
+                // word w of the 16 bytes: k-steps 2w (bytes 0, 1) and 2w + 1 (bytes 2, 3),
+                // dims 32q + 8w .. + 7; scale byte w / 2
+                uint32_t r0[4], r1[4];
+                e2m1x8_scaled_f16x2((&c0.x)[w], f0[w >> 1], r0);
+                e2m1x8_scaled_f16x2((&c1.x)[w], f1[w >> 1], r1);
+                a[2 * w][0] = r0[0];
+                a[2 * w][2] = r0[1];
+                a[2 * w + 1][0] = r0[2];
+                a[2 * w + 1][2] = r0[3];
+                a[2 * w][1] = r1[0];
+                a[2 * w][3] = r1[1];
+                a[2 * w + 1][1] = r1[2];
+                a[2 * w + 1][3] = r1[3];
             }
             const int pos_g = b * kPage + row0;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                // two accumulators (even and odd k-steps) halve the dependent
+                // chain; the scores are exact in fp32 in any order
+                float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int s = 0; s < 8; ++s)
+                for (int s = 0; s < 8; s += 2) {
                     mma_f16(acc, a[s], bq[nt][s][0], bq[nt][s][1]);
+                    mma_f16(acc2, a[s + 1], bq[nt][s + 1][0], bq[nt][s + 1][1]);
+                }
                 // acc: (row g, cols 2q, 2q+1), (row g + 8, cols 2q, 2q+1); col = query token
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
-                    float v0 = acc[c], v1 = acc[2 + c];
+                    float v0 = acc[c] + acc2[c], v1 = acc[2 + c] + acc2[2 + c];
                     if (need_mask) {
                         const int L = seq_len + nt * 8 + 2 * q + c;
                         if (pos_g >= L)
