@@ -606,29 +606,39 @@ cudaError_t launch_umma_fit(const ScoreParams &p, const CUtensorMap &kmap, const
 // ---------------------------------------------------------------------------
 // NVFP4 scorer with a bulk-copy page ring (up to 16 query tokens a request).
 // One persistent CTA per SM takes a contiguous range of the call's pages
-// (request-major).  Warp 0 streams each page's packed E2M1 codes (8 KiB) and
-// E4M3 scales (1 KiB) into a ring of shared-memory stages with two 1-D bulk
-// copies; consumer warp w scores pages w, w + 8, ... of the range on its own:
+// (request-major).  Two producer warps stream the pages' packed E2M1 codes
+// (8 KiB) and E4M3 scales (1 KiB) into a ring of shared-memory stages with
+// two 1-D bulk copies each, warp w the pages w, w + 2, ... (one warp alone
+// issues bulk copies of this size at about one per 340 ns, 4 TB/s over the
+// GPU; two reach the HBM rate); consumer warp c scores pages c, c + 12, ... of
+// the range on its own:
 // 16-byte loads of 32 codes per row and thread, widened in registers
 // (cvt.rn.f16x2.e2m1x2 times the power-of-two f16 scale: exact), mma.sync
 // m16n8k16 against the request's query tokens kept as f16 fragments in
 // registers, causal mask, maximum over the page's 128 rows in registers and
 // shuffles, one write per (query token, block).  No global load waits in the
 // consumers' path and no cross-warp reduction.
-constexpr int kF4Consumers = 8;
-constexpr int kF4Threads = 32 * (1 + kF4Consumers);
+constexpr int kF4Producers = 2;
+constexpr int kF4Consumers = 12;
+constexpr int kF4Threads = 32 * (kF4Producers + kF4Consumers);
 constexpr int kF4Codes = kPage * kDim / 2;      // 8 KiB
 constexpr int kF4Scales = kPage * kDim / 16;    // 1 KiB
 constexpr int kF4Stage = kF4Codes + kF4Scales;  // 9 KiB
-constexpr int kF4Stages = 16;
+// ring depths: 24 stages, or 12 when the request prefix of a call with many
+// requests leaves no room for 24
+constexpr int kF4StagesDeep = 24, kF4StagesShallow = 12;
+// a slot's successive pages belong to one producer warp and one consumer warp
+static_assert(kF4StagesDeep % kF4Producers == 0 && kF4StagesDeep % kF4Consumers == 0 &&
+                  kF4StagesShallow % kF4Producers == 0 && kF4StagesShallow % kF4Consumers == 0,
+              "ring / warp split");
 
-__host__ __device__ inline size_t fp4_smem_bytes(int R)
+__host__ __device__ inline size_t fp4_smem_bytes(int R, int stages)
 {
     // ring, full[S], empty[S], abort flag, request prefix [R + 1]
-    return align_to((size_t)kF4Stages * kF4Stage, 16) + 2 * kF4Stages * 8 + 16 + (size_t)(R + 1) * 4 + 128;
+    return align_to((size_t)stages * kF4Stage, 16) + 2 * (size_t)stages * 8 + 16 + (size_t)(R + 1) * 4 + 128;
 }
 
-template <int NT>
+template <int NT, int kF4Stages>
 __global__ void __launch_bounds__(kF4Threads, 1) index_score_fp4_kernel(const ScoreParams p)
 {
     extern __shared__ __align__(128) uint8_t smem_f4[];
@@ -665,15 +675,15 @@ __global__ void __launch_bounds__(kF4Threads, 1) index_score_fp4_kernel(const Sc
         return lo;
     };
 
-    if (warp == 0) {
-        // =================== producer ===================
+    if (warp < kF4Producers) {
+        // =================== producers: pages warp, warp + kF4Producers, ... ===================
         const uint64_t k_policy = l2_evict_first_policy(); // index-key pages are streamed
         bool ok = true;
-        int issued = 0;
-        for (int l0 = 0; l0 < n && ok; l0 += 32) {
+        int issued = 0; // one past this warp's last issued page
+        for (int l0 = warp; l0 < n && ok; l0 += 32 * kF4Producers) {
             int page = 0;
-            if (l0 + lane < n) {
-                const int x = x_begin + l0 + lane;
+            if (l0 + kF4Producers * lane < n) {
+                const int x = x_begin + l0 + kF4Producers * lane;
                 const int rr = request_of(x);
                 page = p.block_table[(size_t)rr * p.maxB + (x - prefix[rr])];
                 if (page < 0 || page >= p.num_pages) {
@@ -681,9 +691,10 @@ __global__ void __launch_bounds__(kF4Threads, 1) index_score_fp4_kernel(const Sc
                     page = 0; // stay in bounds; the call's outputs are void
                 }
             }
-            const int cnt = n - l0 < 32 ? n - l0 : 32;
+            const int left = (n - l0 + kF4Producers - 1) / kF4Producers; // this warp's pages from l0 on
+            const int cnt = left < 32 ? left : 32;
             for (int i = 0; i < cnt; ++i) {
-                const int l = l0 + i;
+                const int l = l0 + kF4Producers * i;
                 const int pg = __shfl_sync(0xffffffffu, page, i);
                 if (lane == 0) {
                     const int slot = l % kF4Stages;
@@ -707,14 +718,17 @@ __global__ void __launch_bounds__(kF4Threads, 1) index_score_fp4_kernel(const Sc
         if (!ok && lane == 0) {
             set_error(p.err, kErrTimeout);
             *abort_flag = 1;
+            // this warp's copies that may still be in flight: its pages among
+            // the last kF4Stages before its next one (older ones were consumed)
             for (int z = issued - kF4Stages < 0 ? 0 : issued - kF4Stages; z < issued; ++z)
-                (void)mbar_wait_bounded(smem_u32(&full[z % kF4Stages]), (z / kF4Stages) & 1);
+                if (z % kF4Producers == warp)
+                    (void)mbar_wait_bounded(smem_u32(&full[z % kF4Stages]), (z / kF4Stages) & 1);
         }
         return;
     }
 
-    // =================== consumer warps 1..8 ===================
-    const int cw = warp - 1;
+    // =================== consumer warps ===================
+    const int cw = warp - kF4Producers;
     const int g = lane >> 2, q = lane & 3;
     uint32_t bq[NT][8][2]; // query fragments of the current request, f16
     int frag_r = -1, seq_len = 0;
@@ -827,11 +841,11 @@ __global__ void __launch_bounds__(kF4Threads, 1) index_score_fp4_kernel(const Sc
     }
 }
 
-template <int NT>
+template <int NT, int STAGES>
 cudaError_t launch_fp4_t(const ScoreParams &p, int num_sms, cudaStream_t stream)
 {
-    const size_t smem = fp4_smem_bytes(p.R);
-    cudaError_t e = cudaFuncSetAttribute(index_score_fp4_kernel<NT>,
+    const size_t smem = fp4_smem_bytes(p.R, STAGES);
+    cudaError_t e = cudaFuncSetAttribute(index_score_fp4_kernel<NT, STAGES>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
@@ -841,8 +855,16 @@ cudaError_t launch_fp4_t(const ScoreParams &p, int num_sms, cudaStream_t stream)
         grid = max_pages;
     if (grid < 1)
         grid = 1;
-    index_score_fp4_kernel<NT><<<(unsigned)grid, kF4Threads, smem, stream>>>(p);
+    index_score_fp4_kernel<NT, STAGES><<<(unsigned)grid, kF4Threads, smem, stream>>>(p);
     return cudaGetLastError();
+}
+
+template <int NT>
+cudaError_t launch_fp4_fit(const ScoreParams &p, int num_sms, cudaStream_t stream)
+{
+    if (fp4_smem_bytes(p.R, kF4StagesDeep) <= (size_t)kSMaxSmem)
+        return launch_fp4_t<NT, kF4StagesDeep>(p, num_sms, stream);
+    return launch_fp4_t<NT, kF4StagesShallow>(p, num_sms, stream);
 }
 
 template <bool NVFP4, int NT, int PPI>
@@ -896,8 +918,8 @@ cudaError_t launch_index_score(const ScoreParams &p, int index_dtype, int num_sm
         }
     }
     const int nt = (p.nq + 7) / 8;
-    if (index_dtype == MSA_NVFP4 && nt <= 2 && fp4_smem_bytes(p.R) <= (size_t)kSMaxSmem)
-        return nt == 1 ? launch_fp4_t<1>(p, num_sms, stream) : launch_fp4_t<2>(p, num_sms, stream);
+    if (index_dtype == MSA_NVFP4 && nt <= 2 && fp4_smem_bytes(p.R, kF4StagesShallow) <= (size_t)kSMaxSmem)
+        return nt == 1 ? launch_fp4_fit<1>(p, num_sms, stream) : launch_fp4_fit<2>(p, num_sms, stream);
     if (index_dtype == MSA_NVFP4) {
         switch (nt) {
         case 1: return launch_t<true, 1, 4>(p, num_sms, stream);

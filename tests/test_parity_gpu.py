@@ -106,6 +106,28 @@ def test_index_score_across_query_counts(torch_cuda, nq, index_dtype):
     check_device_ok(dp)
 
 
+@pytest.mark.parametrize("nq", [1, 2])
+def test_nvfp4_index_score_with_many_requests(torch_cuda, nq):
+    # 3000 requests: the per-request page offsets leave no room for the deep
+    # page ring of the NVFP4 scorer, which then runs with the shallow one
+    rng = np.random.default_rng(40 + nq)
+    ctx = rng.integers(nq, 600, size=3000)
+    pb = synth.make_problem(name=f"many{nq}", contexts=ctx, q_per_req=nq, num_kv_heads=1, topk=2,
+                            index_dtype=synth.NVFP4, index_range=(-4, 4), guard_page=True,
+                            seed=500 + nq)
+    dp = device_problem(pb)
+    dp.index_score()
+    res = dp.results()
+    tokens = sorted(set(rng.choice(pb.num_tokens, size=40, replace=False).tolist())
+                    | {0, pb.num_tokens - 1})
+    nb = pb.blocks_per_request()
+    for t in tokens:
+        want = oracle.block_scores(pb, t)
+        n = int(nb[t // pb.q_per_req])
+        assert np.array_equal(res["block_scores"][t, :n], want[:n]), (t, nq)
+    check_device_ok(dp)
+
+
 @pytest.mark.parametrize("idx", range(5))
 def test_select_is_bit_exact_on_oracle_scores(torch_cuda, idx):
     torch = torch_cuda
