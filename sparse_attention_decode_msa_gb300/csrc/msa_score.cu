@@ -867,6 +867,228 @@ cudaError_t launch_fp4_fit(const ScoreParams &p, int num_sms, cudaStream_t strea
     return launch_fp4_t<NT, kF4StagesShallow>(p, num_sms, stream);
 }
 
+// ---------------------------------------------------------------------------
+// bf16 scorer with a TMA page ring (up to 8 query tokens a request).  One
+// persistent CTA per SM takes a contiguous range of the call's pages
+// (request-major).  Two producer warps bring each page's 128 x 128 index-key
+// tile into a 6-stage ring (two 16 KiB TMA boxes, 128-byte swizzle), warp w
+// the pages w, w + 2, ...; consumer warp c scores pages c, c + 6, ... on its
+// own: ldmatrix of the swizzled rows (conflict-free), mma.sync m16n8k16
+// against the request's query tokens kept in registers, causal mask, maximum
+// over the page's 128 rows in registers and shuffles, one write per (query
+// token, block).  With a few pages per SM (a short decode step), nearly a
+// CTA's whole share of pages is in flight from the start.
+constexpr int kRProducers = 2;
+constexpr int kRConsumers = 6;
+constexpr int kRThreads = 32 * (kRProducers + kRConsumers);
+constexpr int kRStages = 6;
+constexpr int kRTile = kPage * kDim * 2; // bf16 page tile, 32 KiB
+// a slot's successive pages belong to one producer warp and one consumer warp
+static_assert(kRStages % kRProducers == 0 && kRStages % kRConsumers == 0, "ring / warp split");
+
+__host__ __device__ inline size_t ring_smem_bytes(int R)
+{
+    // alignment slack (swizzle atoms: 1024 B), ring, full[S], empty[S],
+    // abort flag, request prefix [R + 1]
+    return 1024 + (size_t)kRStages * kRTile + 2 * kRStages * 8 + 16 + (size_t)(R + 1) * 4 + 16;
+}
+
+__global__ void __launch_bounds__(kRThreads, 1)
+    index_score_ring_kernel(const __grid_constant__ CUtensorMap k_map, const ScoreParams p)
+{
+    extern __shared__ uint8_t smem_rg[];
+    uint8_t *ring = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_rg) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(ring + (size_t)kRStages * kRTile);
+    uint64_t *empty = full + kRStages;
+    volatile int *abort_flag = reinterpret_cast<int *>(empty + kRStages);
+    int *prefix = reinterpret_cast<int *>(empty + kRStages) + 4;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    launch_dependents(); // the select may start its prologue while pages are scored
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&k_map);
+        for (int s = 0; s < kRStages; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    build_item_prefix<1>(p, prefix); // ends with __syncthreads
+
+    const int P = prefix[p.R];
+    const int x_begin = (int)((long long)blockIdx.x * P / gridDim.x);
+    const int n = (int)((long long)(blockIdx.x + 1) * P / gridDim.x) - x_begin;
+    auto request_of = [&](int x) { // largest r with prefix[r] <= x (a request with pages)
+        int lo = 0, hi = p.R - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (prefix[mid] <= x)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        return lo;
+    };
+
+    if (warp < kRProducers) {
+        // =================== producers: pages warp, warp + kRProducers, ... ===================
+        const uint64_t k_policy = l2_evict_first_policy(); // index-key pages are streamed
+        bool ok = true;
+        int issued = 0; // one past this warp's last issued page
+        for (int l0 = warp; l0 < n && ok; l0 += 32 * kRProducers) {
+            int page = 0;
+            if (l0 + kRProducers * lane < n) {
+                const int x = x_begin + l0 + kRProducers * lane;
+                const int rr = request_of(x);
+                page = p.block_table[(size_t)rr * p.maxB + (x - prefix[rr])];
+                if (page < 0 || page >= p.num_pages) {
+                    set_error(p.err, kErrPage);
+                    page = 0; // stay in bounds; the call's outputs are void
+                }
+            }
+            const int left = (n - l0 + kRProducers - 1) / kRProducers; // this warp's pages from l0 on
+            const int cnt = left < 32 ? left : 32;
+            for (int i = 0; i < cnt; ++i) {
+                const int l = l0 + kRProducers * i;
+                const int pg = __shfl_sync(0xffffffffu, page, i);
+                if (lane == 0) {
+                    const int slot = l % kRStages;
+                    if (l >= kRStages)
+                        ok = mbar_wait_or_abort(smem_u32(&empty[slot]), ((l / kRStages) - 1) & 1, abort_flag);
+                    if (ok) {
+                        const uint32_t bar = smem_u32(&full[slot]);
+                        const uint32_t dst = smem_u32(ring + (size_t)slot * kRTile);
+                        mbar_arrive_expect_tx(bar, kRTile);
+                        const int krow = (pg * p.heads + p.head) * kPage;
+                        tma_load_2d_hint(dst, &k_map, 0, krow, bar, k_policy);
+                        tma_load_2d_hint(dst + kRTile / 2, &k_map, 64, krow, bar, k_policy);
+                        issued = l + 1;
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok)
+                    break;
+            }
+        }
+        if (!ok && lane == 0) {
+            set_error(p.err, kErrTimeout);
+            *abort_flag = 1;
+            // this warp's copies that may still be in flight: its pages among
+            // the last kRStages before its next one (older ones were consumed)
+            for (int z = issued - kRStages < 0 ? 0 : issued - kRStages; z < issued; ++z)
+                if (z % kRProducers == warp)
+                    (void)mbar_wait_bounded(smem_u32(&full[z % kRStages]), (z / kRStages) & 1);
+        }
+        return;
+    }
+
+    // =================== consumer warps ===================
+    const int cw = warp - kRProducers;
+    const int g = lane >> 2, q = lane & 3;
+    // ldmatrix.x4 of a 16 x 16 A tile: lanes 8i .. 8i + 7 give the rows of
+    // matrix i = (rows +0 / +8 for i even / odd, dims +0 / +8 for i < 2 / >= 2)
+    const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const int lchunk = lane >> 4;
+    uint32_t bq[8][2]; // query fragments of the current request: k-step s, dims 16 s + 2 q (+8)
+    int frag_r = -1, seq_len = 0;
+    bool ok = true;
+    for (int l = cw; l < n && ok; l += kRConsumers) {
+        const int slot = l % kRStages;
+        const int x = x_begin + l;
+        const int r = request_of(x), b = x - prefix[r];
+        if (r != frag_r) {
+            frag_r = r;
+            seq_len = p.seq_lens[r];
+            const uint16_t *qrow = p.q_idx + ((size_t)(r * p.nq + (g < p.nq ? g : 0)) * p.heads + p.head) * kDim;
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                uint32_t v0 = 0, v1 = 0;
+                if (g < p.nq) {
+                    v0 = __ldg(reinterpret_cast<const uint32_t *>(qrow + 16 * s + 2 * q));
+                    v1 = __ldg(reinterpret_cast<const uint32_t *>(qrow + 16 * s + 8 + 2 * q));
+                }
+                bq[s][0] = v0;
+                bq[s][1] = v1;
+            }
+        }
+        if (!mbar_wait_or_abort(smem_u32(&full[slot]), (l / kRStages) & 1, abort_flag)) {
+            ok = false;
+            break;
+        }
+        const uint32_t tile = smem_u32(ring + (size_t)slot * kRTile);
+        float rmax[2] = {-INFINITY, -INFINITY};
+        const bool need_mask = (b + 1) * kPage > seq_len;
+#pragma unroll 2
+        for (int mt = 0; mt < kPage / 16; ++mt) {
+            // rows are 128 B (64 dims) in each half of the tile; 16-byte chunk
+            // c of row w sits at chunk c ^ (w % 8)
+            const int row = 16 * mt + lrow;
+            const uint32_t rbase = tile + row * 128;
+            const int sw = row & 7;
+            // two accumulators (even and odd k-steps) halve the dependent
+            // chain; the scores are exact in fp32 in any order
+            float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int s = 0; s < 8; s += 2) {
+                uint32_t a0[4], a1[4];
+                ldsm_x4(a0, rbase + (s >> 2) * (kRTile / 2) + (((2 * (s & 3) + lchunk) ^ sw) << 4));
+                ldsm_x4(a1, rbase + ((s + 1) >> 2) * (kRTile / 2) + (((2 * ((s + 1) & 3) + lchunk) ^ sw) << 4));
+                mma_bf16(acc, a0, bq[s][0], bq[s][1]);
+                mma_bf16(acc2, a1, bq[s + 1][0], bq[s + 1][1]);
+            }
+            // acc: (row g, cols 2q, 2q+1), (row g + 8, cols 2q, 2q+1); col = query token
+            const int pos_g = b * kPage + 16 * mt + g;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                float v0 = acc[c] + acc2[c], v1 = acc[2 + c] + acc2[2 + c];
+                if (need_mask) {
+                    const int L = seq_len + 2 * q + c;
+                    if (pos_g >= L)
+                        v0 = -INFINITY;
+                    if (pos_g + 8 >= L)
+                        v1 = -INFINITY;
+                }
+                rmax[c] = fmaxf(rmax[c], fmaxf(v0, v1));
+            }
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_u32(&empty[slot])); // the page's rows are read
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            float v = rmax[c];
+            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+            const int jj = 2 * q + c;
+            if (g == 0 && jj < p.nq)
+                p.block_scores[((size_t)(r * p.nq + jj) * p.heads + p.head) * p.maxB + b] = v;
+        }
+    }
+    if (!ok) {
+        set_error(p.err, kErrTimeout);
+        *abort_flag = 1;
+    }
+}
+
+cudaError_t launch_ring(const ScoreParams &p, const CUtensorMap &kmap, int num_sms, cudaStream_t stream)
+{
+    const size_t smem = ring_smem_bytes(p.R);
+    cudaError_t e = cudaFuncSetAttribute(index_score_ring_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    long long grid = num_sms;
+    const long long max_pages = (long long)p.R * p.maxB;
+    if (grid > max_pages)
+        grid = max_pages;
+    if (grid < 1)
+        grid = 1;
+    index_score_ring_kernel<<<(unsigned)grid, kRThreads, smem, stream>>>(kmap, p);
+    return cudaGetLastError();
+}
 template <bool NVFP4, int NT, int PPI>
 cudaError_t launch_t(const ScoreParams &p, int num_sms, cudaStream_t stream)
 {
@@ -916,6 +1138,14 @@ cudaError_t launch_index_score(const ScoreParams &p, int index_dtype, int num_sm
         case 48: return launch_umma_fit<48>(p, kmap, qmap, num_sms, stream);
         default: return launch_umma_fit<64>(p, kmap, qmap, num_sms, stream);
         }
+    }
+    if (index_dtype == MSA_BF16 && ring_smem_bytes(p.R) <= (size_t)kSMaxSmem) {
+        // up to 8 query tokens a request: the TMA-ring mma.sync scorer
+        CUtensorMap kmap;
+        if (!encode_2d_sw128(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.idxk, kDim,
+                             (uint64_t)p.num_pages * p.heads * kPage, kDim * 2, 64, kPage))
+            return cudaErrorInvalidValue;
+        return launch_ring(p, kmap, num_sms, stream);
     }
     const int nt = (p.nq + 7) / 8;
     if (index_dtype == MSA_NVFP4 && nt <= 2 && fp4_smem_bytes(p.R, kF4StagesShallow) <= (size_t)kSMaxSmem)
