@@ -95,7 +95,7 @@ def hbm_peak():
 def score_kernel_name(index_dtype: str, q_per_req: int) -> str:
     """The index scorer the library launches for this shape (its dispatch rule)."""
     if index_dtype == "bf16":
-        return "index_score_umma_kernel" if q_per_req > 8 else "index_score_kernel"
+        return "index_score_umma_kernel" if q_per_req > 8 else "index_score_ring_kernel"
     return "index_score_fp4_kernel" if q_per_req <= 16 else "index_score_kernel"
 
 

@@ -7,19 +7,17 @@
 // the per-token scores never reach memory: each page is scored and reduced to
 // its block max in registers.
 //
-// The dot products run on the tensor cores (mma.sync m16n8k16) with the page's
-// 16-token row tiles as M and the request's query tokens as N.  Inputs are
-// integer-valued (bf16) or NVFP4 with power-of-two scales, so every product
-// and partial sum is exact in fp32 and the result equals the plain dot product
-// bit for bit, whatever the summation order.  Because the K dimension is a
-// pure sum, each thread may take its index-key dimensions in whatever order
-// makes its global loads coalesced, provided the query fragment follows the
-// same order.
+// The dot products run on the tensor cores with the page's 16-token row tiles
+// (or the whole 128-token page) as M and the request's query tokens as N.
+// Inputs are integer-valued (bf16) or NVFP4 with power-of-two scales, so every
+// product and partial sum is exact in fp32 and the result equals the plain
+// dot product bit for bit, whatever the summation order.
 //
-// Work decomposition: one item = PPI consecutive pages of one request, one CTA
-// of 4 warps per item in a grid-stride loop; each warp owns 2 row tiles of
-// every page of the item and issues all of its 16-byte loads before the first
-// mma, so a CTA keeps PPI * 32 KiB (bf16) of index keys in flight.
+// Four scorers, by index-key format and query tokens a request:
+//   bf16, <= 8:   TMA page ring, ldmatrix + mma.sync (index_score_ring_kernel)
+//   bf16, > 8:    TMA page ring, tcgen05 (index_score_umma_kernel)
+//   NVFP4, <= 16: bulk-copy page ring, mma.sync (index_score_fp4_kernel)
+//   NVFP4, > 16:  register-staged grid-stride items (index_score_kernel)
 #include "msa_internal.cuh"
 
 namespace msa {
@@ -66,9 +64,15 @@ __device__ void build_item_prefix(const ScoreParams &p, int *prefix)
     __syncthreads();
 }
 
-// Score kernel.  NVFP4 selects the index-key format; NT = n-tiles of 8 query
-// tokens; PPI = pages per item.
-template <bool NVFP4, int NT, int PPI>
+// Register-staged NVFP4 scorer for many query tokens a request.  NT = n-tiles
+// of 8 query tokens; PPI = pages per item.  One item = PPI consecutive pages
+// of one request, one CTA of 4 warps per item in a grid-stride loop; each
+// warp owns 2 row tiles of every page of the item and issues all of its
+// 16-byte loads before the first mma.  Because the K dimension is a pure sum,
+// each thread takes its index-key dimensions in the order that makes its
+// loads coalesced (32 q + 4 s .. + 3 at k-step s), and the query fragment
+// follows the same order.
+template <int NT, int PPI>
 __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(const ScoreParams p)
 {
     extern __shared__ int item_prefix[]; // [R + 1]
@@ -102,7 +106,7 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(const ScoreP
 
         // ---- issue every load of the item ----
         // row tile i of this warp: mt = i * 4 + warp; page pg = mt / 8; rows (mt % 8) * 16 + g (+8)
-        uint4 raw[MT][2][NVFP4 ? 1 : 4];
+        uint4 raw[MT][2];
         uint32_t sraw[MT][2];
 #pragma unroll
         for (int i = 0; i < MT; ++i) {
@@ -122,18 +126,10 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(const ScoreP
             for (int h = 0; h < 2; ++h) {
                 const int row = (mt & 7) * 16 + g + 8 * h;
                 const size_t grow = ((size_t)page * p.heads + p.head) * kPage + row;
-                if (!NVFP4) {
-                    const uint4 *src = reinterpret_cast<const uint4 *>(p.idxk + grow * (kDim * 2));
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        raw[i][h][c] = live ? __ldg(src + c * 4 + q) : make_uint4(0, 0, 0, 0);
-                } else {
-                    const uint4 *src = reinterpret_cast<const uint4 *>(p.idxk + grow * (kDim / 2));
-                    raw[i][h][0] = live ? __ldg(src + q) : make_uint4(0, 0, 0, 0);
-                    const uint16_t *s16 =
-                        reinterpret_cast<const uint16_t *>(p.scales + grow * (kDim / 16));
-                    sraw[i][h] = live ? (uint32_t)__ldg(s16 + q) : 0u;
-                }
+                const uint4 *src = reinterpret_cast<const uint4 *>(p.idxk + grow * (kDim / 2));
+                raw[i][h] = live ? __ldg(src + q) : make_uint4(0, 0, 0, 0);
+                const uint16_t *s16 = reinterpret_cast<const uint16_t *>(p.scales + grow * (kDim / 16));
+                sraw[i][h] = live ? (uint32_t)__ldg(s16 + q) : 0u;
             }
         }
 
@@ -152,19 +148,12 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(const ScoreP
             const uint16_t *qrow = p.q_idx + ((size_t)(t0 + (j < p.nq ? j : 0)) * p.heads + p.head) * kDim;
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
-                // bf16: k-step s = 2c + hh covers dims 32c + 8q + 4hh .. +3
-                // nvfp4: k-step s covers dims 32q + 4s .. +3
-                const int d0 = NVFP4 ? (32 * q + 4 * s) : (32 * (s >> 1) + 8 * q + 4 * (s & 1));
+                // k-step s covers dims 32q + 4s .. +3
                 uint2 v = make_uint2(0, 0);
                 if (j < p.nq)
-                    v = __ldg(reinterpret_cast<const uint2 *>(qrow + d0));
-                if (NVFP4) {
-                    bq[s][0] = bf16x2_to_f16x2(v.x);
-                    bq[s][1] = bf16x2_to_f16x2(v.y);
-                } else {
-                    bq[s][0] = v.x;
-                    bq[s][1] = v.y;
-                }
+                    v = __ldg(reinterpret_cast<const uint2 *>(qrow + 32 * q + 4 * s));
+                bq[s][0] = bf16x2_to_f16x2(v.x);
+                bq[s][1] = bf16x2_to_f16x2(v.y);
             }
 
 #pragma unroll
@@ -178,31 +167,21 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(const ScoreP
 #pragma unroll
                 for (int s = 0; s < 8; ++s) {
                     uint32_t a[4];
-                    if (!NVFP4) {
-                        const uint4 &r0 = raw[i][0][s >> 1];
-                        const uint4 &r1 = raw[i][1][s >> 1];
-                        a[0] = (s & 1) ? r0.z : r0.x;
-                        a[1] = (s & 1) ? r1.z : r1.x;
-                        a[2] = (s & 1) ? r0.w : r0.y;
-                        a[3] = (s & 1) ? r1.w : r1.y;
-                        mma_bf16(acc, a, bq[s][0], bq[s][1]);
-                    } else {
-                        // byte 2s -> dims 32q+4s, +1; byte 2s+1 -> dims +2, +3
-                        const uint32_t w0 = (&raw[i][0][0].x)[s >> 1];
-                        const uint32_t w1 = (&raw[i][1][0].x)[s >> 1];
-                        const int sh = (s & 1) * 16;
-                        // scale byte: dims 32q..32q+15 -> byte 0, 32q+16.. -> byte 1
-                        const int ssh = (s >> 2) * 8;
-                        const uint32_t sc0 = (sraw[i][0] >> ssh) & 0xFFu;
-                        const uint32_t sc1 = (sraw[i][1] >> ssh) & 0xFFu;
-                        const uint32_t f0 = e4m3x2_to_f16x2(sc0 | (sc0 << 8));
-                        const uint32_t f1 = e4m3x2_to_f16x2(sc1 | (sc1 << 8));
-                        a[0] = hmul2_u32(e2m1x2_to_f16x2((w0 >> sh) & 0xFFu), f0);
-                        a[1] = hmul2_u32(e2m1x2_to_f16x2((w1 >> sh) & 0xFFu), f1);
-                        a[2] = hmul2_u32(e2m1x2_to_f16x2((w0 >> (sh + 8)) & 0xFFu), f0);
-                        a[3] = hmul2_u32(e2m1x2_to_f16x2((w1 >> (sh + 8)) & 0xFFu), f1);
-                        mma_f16(acc, a, bq[s][0], bq[s][1]);
-                    }
+                    // byte 2s -> dims 32q+4s, +1; byte 2s+1 -> dims +2, +3
+                    const uint32_t w0 = (&raw[i][0].x)[s >> 1];
+                    const uint32_t w1 = (&raw[i][1].x)[s >> 1];
+                    const int sh = (s & 1) * 16;
+                    // scale byte: dims 32q..32q+15 -> byte 0, 32q+16.. -> byte 1
+                    const int ssh = (s >> 2) * 8;
+                    const uint32_t sc0 = (sraw[i][0] >> ssh) & 0xFFu;
+                    const uint32_t sc1 = (sraw[i][1] >> ssh) & 0xFFu;
+                    const uint32_t f0 = e4m3x2_to_f16x2(sc0 | (sc0 << 8));
+                    const uint32_t f1 = e4m3x2_to_f16x2(sc1 | (sc1 << 8));
+                    a[0] = hmul2_u32(e2m1x2_to_f16x2((w0 >> sh) & 0xFFu), f0);
+                    a[1] = hmul2_u32(e2m1x2_to_f16x2((w1 >> sh) & 0xFFu), f1);
+                    a[2] = hmul2_u32(e2m1x2_to_f16x2((w0 >> (sh + 8)) & 0xFFu), f0);
+                    a[3] = hmul2_u32(e2m1x2_to_f16x2((w1 >> (sh + 8)) & 0xFFu), f1);
+                    mma_f16(acc, a, bq[s][0], bq[s][1]);
                 }
                 // acc: (row g, cols 2q, 2q+1), (row g+8, cols 2q, 2q+1); col = query token
                 const int pos_g = b * kPage + (mt & 7) * 16 + g;
@@ -632,7 +611,7 @@ static_assert(kF4StagesDeep % kF4Producers == 0 && kF4StagesDeep % kF4Consumers 
                   kF4StagesShallow % kF4Producers == 0 && kF4StagesShallow % kF4Consumers == 0,
               "ring / warp split");
 
-__host__ __device__ inline size_t fp4_smem_bytes(int R, int stages)
+__host__ __device__ constexpr size_t fp4_smem_bytes(int R, int stages)
 {
     // ring, full[S], empty[S], abort flag, request prefix [R + 1]
     return align_to((size_t)stages * kF4Stage, 16) + 2 * (size_t)stages * 8 + 16 + (size_t)(R + 1) * 4 + 128;
@@ -886,7 +865,7 @@ constexpr int kRTile = kPage * kDim * 2; // bf16 page tile, 32 KiB
 // a slot's successive pages belong to one producer warp and one consumer warp
 static_assert(kRStages % kRProducers == 0 && kRStages % kRConsumers == 0, "ring / warp split");
 
-__host__ __device__ inline size_t ring_smem_bytes(int R)
+__host__ __device__ constexpr size_t ring_smem_bytes(int R)
 {
     // alignment slack (swizzle atoms: 1024 B), ring, full[S], empty[S],
     // abort flag, request prefix [R + 1]
@@ -1089,10 +1068,11 @@ cudaError_t launch_ring(const ScoreParams &p, const CUtensorMap &kmap, int num_s
     index_score_ring_kernel<<<(unsigned)grid, kRThreads, smem, stream>>>(kmap, p);
     return cudaGetLastError();
 }
-template <bool NVFP4, int NT, int PPI>
+
+template <int NT, int PPI>
 cudaError_t launch_t(const ScoreParams &p, int num_sms, cudaStream_t stream)
 {
-    auto kern = index_score_kernel<NVFP4, NT, PPI>;
+    auto kern = index_score_kernel<NT, PPI>;
     const size_t smem = sizeof(int) * (size_t)(p.R + 1);
     int per_sm = 0;
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kScoreThreads, smem);
@@ -1116,21 +1096,24 @@ cudaError_t launch_t(const ScoreParams &p, int num_sms, cudaStream_t stream)
 cudaError_t launch_index_score(const ScoreParams &p, int index_dtype, int num_sms,
                                cudaStream_t stream)
 {
-    // Many query tokens per request (bf16 index keys): the tcgen05 scorer, one
-    // MMA per page for all of them.  Otherwise the mma.sync scorer, whose
-    // loads are all in flight from the start of the kernel: for a few query
-    // tokens per page the tensor work is small and the start-up of the
-    // TMA / MMA pipeline dominates, and for NVFP4 keys the in-register
-    // widening avoids the f16 staging traffic in shared memory.
-    if (index_dtype == MSA_BF16 && p.nq > 8) {
+    // The rings leave room for the request prefix of the largest call.
+    static_assert(ring_smem_bytes(kMaxRequests) <= (size_t)kSMaxSmem, "bf16 ring and request prefix");
+    static_assert(fp4_smem_bytes(kMaxRequests, kF4StagesShallow) <= (size_t)kSMaxSmem,
+                  "NVFP4 ring and request prefix");
+    if (index_dtype == MSA_BF16) {
+        CUtensorMap kmap; // every page row of the index-key pool, 64-dim boxes of 128 rows
+        if (!encode_2d_sw128(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.idxk, kDim,
+                             (uint64_t)p.num_pages * p.heads * kPage, kDim * 2, 64, kPage))
+            return cudaErrorInvalidValue;
+        // up to 8 query tokens a request (one n-tile of mma.sync): the
+        // TMA-ring mma.sync scorer; more: tcgen05, one MMA per page for all
+        if (p.nq <= 8)
+            return launch_ring(p, kmap, num_sms, stream);
         const int T = p.R * p.nq;
         const int npad = (p.nq + 15) / 16 * 16;
-        CUtensorMap qmap, kmap;
-        // this head's query rows: T rows, heads * Di apart; keys: every page row
+        CUtensorMap qmap; // this head's query rows: T rows, heads * Di apart
         if (!encode_2d_sw128(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.q_idx + (size_t)p.head * kDim, kDim, T,
-                             (uint64_t)p.heads * kDim * 2, 64, npad) ||
-            !encode_2d_sw128(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.idxk, kDim,
-                             (uint64_t)p.num_pages * p.heads * kPage, kDim * 2, 64, kPage))
+                             (uint64_t)p.heads * kDim * 2, 64, npad))
             return cudaErrorInvalidValue;
         switch (npad) {
         case 16: return launch_umma_fit<16>(p, kmap, qmap, num_sms, stream);
@@ -1139,36 +1122,18 @@ cudaError_t launch_index_score(const ScoreParams &p, int index_dtype, int num_sm
         default: return launch_umma_fit<64>(p, kmap, qmap, num_sms, stream);
         }
     }
-    if (index_dtype == MSA_BF16 && ring_smem_bytes(p.R) <= (size_t)kSMaxSmem) {
-        // up to 8 query tokens a request: the TMA-ring mma.sync scorer
-        CUtensorMap kmap;
-        if (!encode_2d_sw128(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.idxk, kDim,
-                             (uint64_t)p.num_pages * p.heads * kPage, kDim * 2, 64, kPage))
-            return cudaErrorInvalidValue;
-        return launch_ring(p, kmap, num_sms, stream);
-    }
+    // NVFP4: up to 16 query tokens a request, the bulk-copy ring (the
+    // widening of the codes in registers keeps up with HBM there); more, the
+    // register-staged scorer with several n-tiles
     const int nt = (p.nq + 7) / 8;
-    if (index_dtype == MSA_NVFP4 && nt <= 2 && fp4_smem_bytes(p.R, kF4StagesShallow) <= (size_t)kSMaxSmem)
-        return nt == 1 ? launch_fp4_fit<1>(p, num_sms, stream) : launch_fp4_fit<2>(p, num_sms, stream);
-    if (index_dtype == MSA_NVFP4) {
-        switch (nt) {
-        case 1: return launch_t<true, 1, 4>(p, num_sms, stream);
-        case 2: return launch_t<true, 2, 2>(p, num_sms, stream);
-        case 3:
-        case 4: return launch_t<true, 4, 1>(p, num_sms, stream);
-        case 5:
-        case 6: return launch_t<true, 6, 1>(p, num_sms, stream);
-        default: return launch_t<true, 8, 1>(p, num_sms, stream);
-        }
-    }
     switch (nt) {
-    case 1: return launch_t<false, 1, 1>(p, num_sms, stream);
-    case 2: return launch_t<false, 2, 1>(p, num_sms, stream);
+    case 1: return launch_fp4_fit<1>(p, num_sms, stream);
+    case 2: return launch_fp4_fit<2>(p, num_sms, stream);
     case 3:
-    case 4: return launch_t<false, 4, 1>(p, num_sms, stream);
+    case 4: return launch_t<4, 1>(p, num_sms, stream);
     case 5:
-    case 6: return launch_t<false, 6, 1>(p, num_sms, stream);
-    default: return launch_t<false, 8, 1>(p, num_sms, stream);
+    case 6: return launch_t<6, 1>(p, num_sms, stream);
+    default: return launch_t<8, 1>(p, num_sms, stream);
     }
 }
 
