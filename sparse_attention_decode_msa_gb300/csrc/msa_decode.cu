@@ -902,23 +902,31 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
 
     int l_last = -1, sm_units = 0;
     float unit_scale = p.scale_log2; // logits to base 2 (FP8: / the unit's query scale)
-    for (int l = 0; l < ntasks && ok; ++l) {
+    // One pass past the last task (l == ntasks) finishes the last unit, so
+    // that finalize has one call site: its code, run once per unit, is
+    // fetched once per CTA instead of once per copy.
+    for (int l = 0; l <= ntasks && ok; ++l) {
+        const bool end = l == ntasks;
         const int b = l & 1;
-        if (!mbar_wait_or_abort(smem_u32(&s_full[b]), (l >> 1) & 1, abort_flag)) {
-            ok = false;
-            break;
-        }
-        tcgen05_after_sync();
-        const int4 e = entry(l);
-        const int u = unit_of(e);
-        const bool live = e.x >= 0;
+        int4 e = make_int4(-1, 0, 0, 0);
+        int u = -2; // no unit: ends the last one
         float sv[kUHeads];
-        if (live)
-            tmem_ld8(lane_base + 16 * b, sv);
-        tcgen05_before_sync();
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(smem_u32(&s_free[b]));
+        if (!end) {
+            if (!mbar_wait_or_abort(smem_u32(&s_full[b]), (l >> 1) & 1, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tcgen05_after_sync();
+            e = entry(l);
+            u = unit_of(e);
+            if (e.x >= 0)
+                tmem_ld8(lane_base + 16 * b, sv);
+            tcgen05_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_u32(&s_free[b]));
+        }
+        const bool live = e.x >= 0;
 
         if (u != cur_unit) {
             if (cur_unit >= 0) {
@@ -926,10 +934,12 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
                     fold(l_last);
                 if (!ok)
                     break;
-                finalize(cur_t, cur_g, false);
+                finalize(cur_t, cur_g, end);
                 if (!ok)
                     break;
             }
+            if (end)
+                break;
             cur_unit = u;
             cur_t = e.z;
             cur_g = e.w;
@@ -1028,12 +1038,6 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
             alpha_prev[h] = live ? alpha[h] : 1.f;
         pending = live;
         l_last = l;
-    }
-    if (ok && cur_unit >= 0) {
-        if (l_last >= 0)
-            fold(l_last);
-        if (ok)
-            finalize(cur_t, cur_g, true);
     }
     if (!ok) {
         set_error(p.err, kErrTimeout);
