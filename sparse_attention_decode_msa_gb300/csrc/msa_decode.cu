@@ -157,7 +157,6 @@ __device__ int4 make_entry(const DecodeParams &p, long long x, const int *qt)
 // 16 registers (one per head) once the next page's P^T is written.
 
 constexpr int kUSmxWarps = 8;              // softmax warps: two per TMEM lane quarter
-constexpr int kUSoftmax = 32 * kUSmxWarps; // softmax threads
 constexpr int kUCvtWarps = 4;              // NVFP4 only: e2m1 x E4M3 -> f16 converter warps
 // KV formats of the kernel instances
 constexpr int kKvBf16 = 0, kKvFp8 = 1, kKvNvfp4 = 2;
@@ -711,7 +710,7 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
     const int half = (warp - 2) >> 2;      // heads 8*half .. 8*half + 7
     const int h0 = kUHeads * half;
     const int idx = 32 * quarter + lane;   // token of S^T / dimension of O^T
-    const int sidx = threadIdx.x - 64;     // 0 .. kUSoftmax - 1
+    const int sidx = threadIdx.x - 64;     // 0 .. 32 * kUSmxWarps - 1
     const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16) + h0;
     int sync_phase = 0;
     bool ok = true;

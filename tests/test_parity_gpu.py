@@ -300,6 +300,26 @@ def test_max_topk_and_wide_block_table(torch_cuda):
                            strict=False)
 
 
+def test_largest_request_count(torch_cuda):
+    # 8192 requests, the most a call takes: the bf16 scorer's page ring then
+    # shares shared memory with the largest per-request page offsets (its
+    # tightest configuration); every token's scores and selection, attention
+    # on a seeded sample
+    rng = np.random.default_rng(60)
+    ctx = rng.integers(1, 260, size=8192)
+    pb = synth.make_problem(name="maxR", contexts=ctx, q_per_req=1, num_kv_heads=1, topk=1,
+                            seed=61)
+    dp = device_problem(pb)
+    dp.decode_step()
+    res = dp.results()
+    tokens = np.sort(rng.choice(pb.num_tokens, size=256, replace=False))
+    ref = oracle.decode_step(pb, tokens=tokens, threads=THREADS)
+    assert_scores_equal(pb, res["block_scores"], ref["block_scores"], tokens)
+    assert np.array_equal(res["selected"][tokens], ref["selected"])
+    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], tokens, strict=False)
+    check_device_ok(dp)
+
+
 def test_large_speculative_step(torch_cuda):
     pb = synth.make_problem(name="nq64", contexts=[3000], q_per_req=64, num_kv_heads=1, topk=8,
                             index_range=(-2, 2), seed=25)
