@@ -185,6 +185,9 @@ msa_status msa_select_topk(const msa_shape *shape, const float *block_scores,
 /* Stage (c): attention of each token over the visible positions of its
  * selected blocks, split over persistent CTAs and merged in a fixed order
  * with one reciprocal per output row (no atomics).  out: bf16, lse: fp32.
+ * The CTAs' task ranges are cut in 32-bit arithmetic: a call with
+ * T * num_kv_heads * topk * (decode CTAs + 1) >= 2^32 returns
+ * MSA_ERR_UNSUPPORTED (so does msa_decode_step).
  * ("MiniMax-M3 NVFP4 low-latency decode megakernel ...", "The TP4 decode
  * target": long-context sparse decode; "Add Rubin (sm_107) ...", "Items and
  * numerics": the split-K merge.) */

@@ -179,6 +179,23 @@ msa_status select_impl(const msa_shape *s, const float *block_scores, const int3
     return cuda_status(launch_select(p, stream, pdl));
 }
 
+// Persistent CTAs of the decode: the shape's, else one per SM (at most the
+// workspace bound and the number of tasks); -1 if the device cannot be read.
+int decode_ctas(const msa_shape *s)
+{
+    int ctas = s->decode_ctas;
+    if (ctas == 0) {
+        const int sms = num_sms_current();
+        if (sms < 1)
+            return -1;
+        ctas = sms < kDefaultCtaBound ? sms : kDefaultCtaBound;
+        const long long max_tasks = (long long)tokens_of(s) * s->num_kv_heads * s->topk;
+        if (ctas > max_tasks)
+            ctas = (int)max_tasks;
+    }
+    return ctas;
+}
+
 msa_status decode_impl(const msa_shape *s, const void *q, const void *kv_pool,
                        const int32_t *block_table, const int32_t *seq_lens,
                        const int32_t *selected, void *out, float *lse, void *ws,
@@ -206,17 +223,21 @@ msa_status decode_impl(const msa_shape *s, const void *q, const void *kv_pool,
     const bool scaled = s->kv_dtype != MSA_BF16; // E4M3 and NVFP4 carry tensor scales
     p.scale_log2 = s->softmax_scale * 1.4426950408889634f * (scaled ? s->k_scale : 1.f);
     p.v_scale = scaled ? s->v_scale : 1.f;
-    int ctas = s->decode_ctas;
-    if (ctas == 0) {
-        const int sms = num_sms_current();
-        if (sms < 1)
-            return MSA_ERR_CUDA;
-        ctas = sms < kDefaultCtaBound ? sms : kDefaultCtaBound;
-        const long long max_tasks = (long long)p.T * p.Hkv * p.k;
-        if (ctas > max_tasks)
-            ctas = (int)max_tasks;
-    }
+    const int ctas = decode_ctas(s);
+    if (ctas < 1)
+        return MSA_ERR_CUDA;
     return cuda_status(launch_sparse_decode(p, kv_pool, s->kv_dtype, ctas, stream, pdl));
+}
+
+// The decode cuts its P <= T * Hkv * k tasks into G ranges in 32-bit
+// arithmetic: calls with P (G + 1) >= 2^32 are not taken.
+msa_status check_decode_size(const msa_shape *s)
+{
+    const int ctas = decode_ctas(s);
+    if (ctas < 1)
+        return MSA_ERR_CUDA;
+    const long long bound = (long long)tokens_of(s) * s->num_kv_heads * s->topk;
+    return bound * (ctas + 1) < (1ll << 32) ? MSA_OK : MSA_ERR_UNSUPPORTED;
 }
 
 } // namespace
@@ -298,6 +319,8 @@ msa_status msa_sparse_decode(const msa_shape *shape, const void *q, const void *
         return MSA_ERR_INVALID_ARGUMENT;
     if (tokens_of(shape) == 0)
         return MSA_OK;
+    if ((st = check_decode_size(shape)) != MSA_OK)
+        return st;
     return decode_impl(shape, q, kv_pool, block_table, seq_lens, selected, out, lse, workspace,
                        stream, false);
 }
@@ -324,6 +347,8 @@ msa_status msa_decode_step(const msa_shape *shape, const void *q_idx, const void
         return MSA_ERR_INVALID_ARGUMENT;
     if (tokens_of(shape) == 0)
         return MSA_OK;
+    if ((st = check_decode_size(shape)) != MSA_OK)
+        return st;
     const WorkspaceLayout w = layout_of(shape);
     uint8_t *wsb = static_cast<uint8_t *>(workspace);
     if (!block_scores)

@@ -88,7 +88,7 @@ __device__ __forceinline__ Task task_of(long long x, const int *qt, int T)
 {
     const int PT = qt[T];
     Task tk;
-    tk.g = (int)(x / PT);
+    tk.g = (int)((uint32_t)x / (uint32_t)PT); // x < P < 2^32 (see owner_of)
     const int rem = (int)(x - (long long)tk.g * PT);
     int lo = 0, hi = T - 1;
     while (lo < hi) {
@@ -104,15 +104,19 @@ __device__ __forceinline__ Task task_of(long long x, const int *qt, int T)
 }
 
 // CTA that owns task x when P tasks are cut into G equal ranges:
-// range(c) = [floor(c P / G), floor((c+1) P / G)).
+// range(c) = [floor(c P / G), floor((c+1) P / G)).  The host admits only calls
+// with P (G + 1) < 2^32 (it bounds P by T Hkv k), so every product here fits
+// 32 bits.  These run on the unit finalize's path, whose code runs cold once
+// or twice per CTA: 64-bit divisions there (long software sequences) cost
+// 1-2.3 us per launch, even as a branch not taken.
 __device__ __forceinline__ int owner_of(long long x, long long P, int G)
 {
-    return (int)(((x + 1) * G + P - 1) / P) - 1;
+    return (int)((((uint32_t)x + 1u) * (uint32_t)G + ((uint32_t)P - 1u)) / (uint32_t)P) - 1;
 }
 
 __device__ __forceinline__ bool range_empty(int c, long long P, int G)
 {
-    return (long long)c * P / G == (long long)(c + 1) * P / G;
+    return (uint32_t)c * (uint32_t)P / (uint32_t)G == (uint32_t)(c + 1) * (uint32_t)P / (uint32_t)G;
 }
 
 // Table entry of task x: {K-tile row in the KV tensor map or -1, visible
@@ -336,7 +340,8 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
 
     const long long P = (long long)p.Hkv * qt[p.T];
     const int G = gridDim.x, c = blockIdx.x;
-    const long long x_begin = (long long)c * P / G, x_end = (long long)(c + 1) * P / G;
+    const long long x_begin = (uint32_t)c * (uint32_t)P / (uint32_t)G; // 32-bit: see owner_of
+    const long long x_end = (uint32_t)(c + 1) * (uint32_t)P / (uint32_t)G;
     const int ntasks = (int)(x_end - x_begin);
 
     grid_dependency_wait(); // `selected` comes from the previous kernel of the step

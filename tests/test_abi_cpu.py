@@ -121,6 +121,20 @@ def test_null_and_misaligned_pointers_are_rejected_on_the_host(lib):
                                msa.msa_workspace_bytes(s4), None) == 1
 
 
+def test_decode_beyond_32_bit_task_ranges_is_unsupported(lib):
+    # T * Hkv * topk * (decode CTAs + 1) >= 2^32: the decode's cut of its
+    # tasks into CTA ranges would not fit 32-bit arithmetic; refused on the
+    # host before anything is launched (the CTA count given: no device query)
+    s = shape(num_requests=2048, q_per_req=4, topk=256)
+    s.decode_ctas = 1024
+    assert 2048 * 4 * 4 * 256 * 1025 >= 2 ** 32
+    ws_bytes = msa.msa_workspace_bytes(s)
+    assert ws_bytes > 0
+    fake = 0x10000
+    assert lib.msa_sparse_decode(msa.ctypes.byref(s), *([fake] * 7), fake, ws_bytes, None) == 2
+    assert lib.msa_decode_step(msa.ctypes.byref(s), *([fake] * 11), fake, ws_bytes, None) == 2
+
+
 def test_zero_requests_is_a_validated_no_op(lib):
     s = shape(num_requests=0)
     ws_bytes = msa.msa_workspace_bytes(s)
