@@ -101,6 +101,13 @@ extern "C" msa_status msa_sparse_decode_noalloc(const msa_shape *shape, const vo
     const long long slots = (long long)ctas + units;
     if (head + slots * (long long)kPartialBytes > (long long)MSA_NOALLOC_SCRATCH_BYTES)
         return MSA_ERR_UNSUPPORTED; // too big for the fixed scratch: use msa_sparse_decode
+    // The decode cuts its P <= units * topk tasks into ctas ranges in 32-bit
+    // arithmetic (P (ctas + 1) < 2^32); the fixed scratch bounds ctas + units
+    // far below what could break that.
+    static_assert((unsigned long long)(MSA_NOALLOC_SCRATCH_BYTES / kPartialBytes) * kMaxTopk *
+                          (MSA_NOALLOC_SCRATCH_BYTES / kPartialBytes + 1) <
+                      (1ull << 32),
+                  "fixed scratch admits task ranges beyond 32 bits");
 
     unsigned char *scratch = static_cast<unsigned char *>(scratch_address(dev));
     if (!scratch)
