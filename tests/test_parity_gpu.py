@@ -320,6 +320,36 @@ def test_largest_request_count(torch_cuda):
     check_device_ok(dp)
 
 
+@pytest.mark.parametrize("kv_dtype", [synth.BF16, synth.FP8])
+def test_permuting_the_page_pool_changes_nothing(torch_cuda, kv_dtype):
+    # pages are data addressed through the block table: moving every page of
+    # the pools to another slot and renumbering the table leaves every output
+    # bit for bit (no physical page id reaches the arithmetic or the order)
+    import dataclasses
+
+    pb = synth.make_problem(name="perm", contexts=[700, 3000, 129, 9000], q_per_req=3,
+                            num_kv_heads=2, topk=6, kv_dtype=kv_dtype, guard_page=True, seed=77)
+    rng = np.random.default_rng(78)
+    perm = rng.permutation(pb.num_pages)  # old page p -> slot perm[p]
+    def moved(pool):
+        out = np.empty_like(pool)
+        out[perm] = pool
+        return out
+    bt = pb.block_table.copy()
+    bt[bt >= 0] = perm[bt[bt >= 0]]
+    pb2 = dataclasses.replace(pb, kv_pool=moved(pb.kv_pool), idxk_pool=moved(pb.idxk_pool),
+                              block_table=bt)
+    results = []
+    for p in (pb, pb2):
+        dp = device_problem(p)
+        dp.decode_step()
+        results.append(dp.results())
+        check_device_ok(dp)
+    for key in ("block_scores", "selected", "out", "lse"):
+        a, b = results[0][key], results[1][key]
+        assert np.array_equal(a.view(np.uint8), b.view(np.uint8)), key
+
+
 def test_large_speculative_step(torch_cuda):
     pb = synth.make_problem(name="nq64", contexts=[3000], q_per_req=64, num_kv_heads=1, topk=8,
                             index_range=(-2, 2), seed=25)
