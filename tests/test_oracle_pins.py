@@ -409,6 +409,38 @@ def test_attention_causal_limit():
             assert (not np.array_equal(out, base["out"][j])) == changes, (j, pos)
 
 
+@pytest.mark.parametrize("kv_dtype", [synth.BF16, synth.FP8, synth.NVFP4])
+def test_pages_are_reached_only_through_the_block_table(kv_dtype):
+    # moving every page of the pools to another slot and renumbering the
+    # block table changes no result: a page read by its block number, or a
+    # table entry used for the wrong request, breaks this
+    import dataclasses
+
+    pb = synth.make_problem(name="perm", contexts=[300, 1000, 129], q_per_req=2, num_kv_heads=2,
+                            topk=4, kv_dtype=kv_dtype, guard_page=True, seed=91)
+    perm = np.random.default_rng(92).permutation(pb.num_pages)
+
+    def moved(pool):
+        out = np.empty_like(pool)
+        out[perm] = pool
+        return out
+
+    bt = pb.block_table.copy()
+    bt[bt >= 0] = perm[bt[bt >= 0]]
+    assert not np.array_equal(bt, pb.block_table)
+    pb2 = dataclasses.replace(pb, kv_pool=moved(pb.kv_pool), idxk_pool=moved(pb.idxk_pool),
+                              block_table=bt)
+    r1 = oracle.decode_step(pb, threads=2)
+    r2 = oracle.decode_step(pb2, threads=2)
+    for key in ("block_scores", "selected", "out", "lse"):
+        assert np.array_equal(r1[key], r2[key]), key
+    # and a table that points at the wrong pages does change the result
+    bt_bad = pb.block_table.copy()
+    bt_bad[0, :2] = bt_bad[0, 1::-1]
+    r3 = oracle.decode_step(dataclasses.replace(pb, block_table=bt_bad), threads=2)
+    assert not np.array_equal(r3["block_scores"], r1["block_scores"])
+
+
 def test_decode_step_matches_stagewise_calls():
     pb = synth.make_small_workload(4)
     res = oracle.decode_step(pb, threads=3)
