@@ -190,27 +190,36 @@ class ClockSampler:
 def algorithmic_bytes(pb, selected: np.ndarray) -> dict:
     """Bytes the method must move for one step (see the design notes).
 
-    index: the index key of every cached token once per request;
+    index: the index key of every cached token once per request (and index head);
     kv: per (request, KV head) the union over the request's query tokens of
-        the selected pages (K page + V page of that head);
+        the pages selected for that KV head (K page + V page of that head);
+        selected is [T, k] (one table per token) or [T, Hs, k] (one per KV head);
     small: q, q_idx, out, lse, the block-table rows used, seq_lens."""
     ctx = pb.contexts
-    per_tok = 256 if pb.index_dtype == "bf16" else 64 + 8
+    Hi = getattr(pb, "num_index_heads", 1)
+    per_tok = (256 if pb.index_dtype == "bf16" else 64 + 8) * Hi
     index = int(ctx.sum()) * per_tok
     page_head = {"bf16": 2 * 128 * 128 * 2, "fp8": 2 * 128 * 128,
                  "nvfp4": 2 * (128 * 64 + 128 * 8)}[pb.kv_dtype]
-    union_pages = 0
+    sel = selected.reshape(pb.num_tokens, -1, selected.shape[-1])
+    Hs = sel.shape[1]
+    union_pages = 0   # summed over (request, KV head)
     for r in range(pb.num_requests):
-        rows = selected[r * pb.q_per_req:(r + 1) * pb.q_per_req].ravel()
-        union_pages += len(np.unique(rows[rows >= 0]))
-    kv = union_pages * pb.num_kv_heads * page_head
+        rows = sel[r * pb.q_per_req:(r + 1) * pb.q_per_req]
+        for g in range(Hs):
+            hr = rows[:, g].ravel()
+            union_pages += len(np.unique(hr[hr >= 0]))
+    if Hs == 1:
+        union_pages *= pb.num_kv_heads   # one table serves every KV head
+    kv = union_pages * page_head
     T, Hq = pb.num_tokens, pb.num_q_heads
     nb = pb.blocks_per_request()
-    small = T * Hq * 128 * 2 * 2 + T * 128 * 2 + T * Hq * 4 + int(nb.sum()) * 4 + pb.num_requests * 4
-    scores_io = int(nb.sum()) * pb.q_per_req * 4  # block scores written once
+    small = (T * Hq * 128 * 2 * 2 + T * Hi * 128 * 2 + T * Hq * 4 + int(nb.sum()) * 4
+             + pb.num_requests * 4)
+    scores_io = int(nb.sum()) * pb.q_per_req * Hi * 4  # block scores written once
     return {"index": index, "kv": kv, "small": small, "scores_io": scores_io,
-            "total": index + kv + small, "union_pages": union_pages,
-            "sum_selected_pages": int((selected >= 0).sum())}
+            "total": index + kv + small, "union_page_heads": union_pages,
+            "sum_selected_page_heads": int((sel >= 0).sum()) * (pb.num_kv_heads if Hs == 1 else 1)}
 
 
 # ---------------------------------------------------------------------------
@@ -240,7 +249,7 @@ def run_ours(args, rank, world, local):
     status = msa.msa_check_device_status(base.ws)
     if status != msa.MSA_OK:
         raise RuntimeError(f"device check failed: {msa.status_string(status)}")
-    sel = base.selected[:, 0].cpu().numpy()
+    sel = base.selected.cpu().numpy()
     nbytes = algorithmic_bytes(pb, sel)
 
     # device copies so that no step finds its inputs in L2
@@ -339,6 +348,50 @@ def run_ours(args, rank, world, local):
         t_end2 = time.time()
         soak_label = f"timed region + {t_end2 - ts0:.1f} s of the same replays right after it"
         t_end = t_end2
+
+    # ---- the step's distribution: per-replay CUDA events over >= 50 steps
+    # (graph replays, median per step), then eager C-ABI calls (one event pair
+    # per step) ----
+    def replay_samples(name, fn, k):
+        seq = graphs_for(name, fn, k)
+        counts = [nrep] * (k // nrep) + ([k % nrep] if k % nrep else [])
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(seq) + 1)]
+        with torch.cuda.stream(stream):
+            evs[0].record(stream)
+            for i, g in enumerate(seq):
+                g.replay()
+                evs[i + 1].record(stream)
+        evs[-1].synchronize()
+        per = [evs[i].elapsed_time(evs[i + 1]) / n for i, n in enumerate(counts)]
+        return per, evs[0].elapsed_time(evs[-1]) / k
+
+    k_dist = max(args.steps, 50 * nrep)
+    graph_per, graph_mean = replay_samples("step", step_fn, k_dist)
+
+    def eager_samples(k):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(k + 1)]
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                step_fn(reps[i % nrep], stream)
+            evs[0].record(stream)
+            for i in range(k):
+                step_fn(reps[i % nrep], stream)
+                evs[i + 1].record(stream)
+        evs[-1].synchronize()
+        per = [evs[i].elapsed_time(evs[i + 1]) for i in range(k)]
+        return per, evs[0].elapsed_time(evs[-1]) / k
+
+    eager_per, eager_mean = eager_samples(max(args.steps, 50))
+    step_dist = {
+        "graph_replays": {"steps": k_dist, "mean_us": round(graph_mean * 1e3, 2),
+                          "median_us": round(statistics.median(graph_per) * 1e3, 2),
+                          "min_us": round(min(graph_per) * 1e3, 2),
+                          "per": f"one event pair per replay of {nrep} steps"},
+        "eager": {"steps": len(eager_per), "mean_us": round(eager_mean * 1e3, 2),
+                  "median_us": round(statistics.median(eager_per) * 1e3, 2),
+                  "min_us": round(min(eager_per) * 1e3, 2),
+                  "per": "one event pair per msa_decode_step call, no graph"},
+    }
 
     # ---- per-stage times (same protocol) ----
     k_stage = max(args.steps, 50)
@@ -457,6 +510,7 @@ def run_ours(args, rank, world, local):
         "achieved_gbps": round(nbytes["total"] / (ms_step_max / 1e3) / 1e9, 1),
         "frac_of_8tbs": round(nbytes["total"] / (ms_step_max / 1e3) / 8e12, 4),
         "stages_us": {k: round(v * 1e3, 2) for k, v in stage_ms.items()},
+        "step_distribution": step_dist,
         "roofline": {
             "kernel": kernel_key,
             "bound": "hbm",
@@ -508,15 +562,20 @@ def oracle_tokens_per_second(pb, budget_s: float, threads: int, sample_tokens=No
 
 
 def cpu_baseline(pb, budget_s=15.0):
+    """The oracle on the host cores: OpenMP over tokens on every core (the
+    reported value), and again on one thread."""
     import oracle
 
     threads = max(1, os.cpu_count() or 1)
     oracle.build()
     v, n, el = oracle_tokens_per_second(pb, budget_s, threads)
+    v1, n1, el1 = oracle_tokens_per_second(pb, budget_s * 2 / 3, 1, sample_tokens=1)
+    what = ("query tokens of the same workload drawn at random (whole fused step per token: "
+            "index score of every cached token, select, attention)")
     return {"value": round(v, 2), "unit": "query-tokens/s", "cores": threads, "kind": "oracle",
-            "sample": (f"{n} query tokens of the same workload drawn at random (whole fused step "
-                       f"per token: index score of every cached token, select, attention) in "
-                       f"{el:.1f} s, OpenMP over tokens")}
+            "sample": f"{n} {what} in {el:.1f} s, OpenMP over tokens on {threads} threads",
+            "single_thread": {"value": round(v1, 3), "unit": "query-tokens/s", "cores": 1,
+                              "sample": f"{n1} {what} in {el1:.1f} s on one thread"}}
 
 
 def run_reference(args, rank, world, local):
@@ -567,7 +626,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=1, help="workload 0..4 (default 1: spec-verify)")
+    ap.add_argument("--config", type=int, default=4,
+                    help="workload 0..4 (default 4: NVFP4 index keys, the largest)")
     ap.add_argument("--kv-dtype", choices=["bf16", "fp8", "nvfp4"], default=None,
                     help="replace the workload's KV dtype (same shapes)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")

@@ -62,9 +62,11 @@
  *     MSA_ERR_INVALID_ARGUMENT.  Nothing is launched in either case.
  *   - Values that can only be checked on the device (page ids in the block
  *     table, seq_lens, selected block ids) are bounds-checked by the
- *     kernels before use; a bad one sets a bit in the workspace's error
- *     word, the offending access is skipped, and the outputs of that call
- *     are unspecified.  msa_check_device_status reports and clears it.
+ *     kernels before use (each of msa_index_score, msa_select_topk and
+ *     msa_sparse_decode checks the ones it reads); a bad one sets a bit in
+ *     the workspace's error word, the offending access is skipped, and the
+ *     outputs of that call are unspecified.  msa_check_device_status
+ *     reports and clears it.
  *   - Every device pointer must be 16-byte aligned.
  *
  * Layouts (row-major, element type as stored; T = num_requests * q_per_req,
@@ -259,26 +261,44 @@ msa_status msa_select_rows(const msa_shape *shape, const float *scores_hbt,
  * output tensors by a runtime that owns every device allocation, or code on
  * a path where the allocator may not be called.  It computes exactly what
  * msa_sparse_decode computes, with the same kernels, but keeps the scratch
- * (split partials and the error word) in a fixed array of
- * MSA_NOALLOC_SCRATCH_BYTES compiled into the library, which every GPU that
- * loads the library holds until the process exits.  It allocates nothing.
- *   - The first call on each device looks up that device's copy of the array
- *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ * (split partials, their arrival counters and the error word) in a fixed
+ * array of MSA_NOALLOC_SCRATCH_BYTES compiled into the library, which every
+ * GPU that loads the library holds until the process exits.  It allocates
+ * nothing.
+ *   - Every call asks the CUDA runtime for the address of the array in the
+ *     current device's context (cudaGetSymbolAddress).  The first call on a
+ *     device loads the library's device code there; make that first call
+ *     before any stream capture.
  *   - All calls share the one array: calls whose work overlaps on the GPU
  *     (different streams, or different host threads) race and give wrong
- *     results.  Each call clears the error word it needs; the partial slots
- *     are always written before they are read.
- *   - Device-side bounds failures are not reported (there is no workspace to
- *     read them from); use msa_sparse_decode for that.
+ *     results.  Each call clears the error word and the arrival counters it
+ *     needs; the partial slots are always written before they are read.
+ *   - Device-side failures are not reported (there is no workspace to read
+ *     them from): neither a bounds failure (bad page id, seq_len or block id)
+ *     nor a bounded wait that ran out (MSA_ERR_TIMEOUT elsewhere).  After one
+ *     the call still returns MSA_OK and its outputs are unspecified; callers
+ *     that need to detect them use msa_sparse_decode.
+ *   - Shapes are checked as by every other entry point, with the same
+ *     statuses (MSA_ERR_INVALID_ARGUMENT, MSA_ERR_UNSUPPORTED).
  *   - Returns MSA_ERR_UNSUPPORTED when the scratch it needs exceeds
  *     MSA_NOALLOC_SCRATCH_BYTES: 256 bytes of error word, a 4-byte counter per
  *     (token, KV head) pair rounded up to 256 bytes, and (decode CTAs + pairs)
- *     partial slots of 8320 bytes (with the default CTA count on a 152-SM
- *     GPU: at most 855 (token, KV head) pairs). */
+ *     partial slots of 8320 bytes (with 152 decode CTAs, the default on a
+ *     152-SM GPU: at most 855 (token, KV head) pairs). */
 msa_status msa_sparse_decode_noalloc(const msa_shape *shape, const void *q, const void *kv_pool,
                                      const int32_t *block_table, const int32_t *seq_lens,
                                      const int32_t *selected, void *out, float *lse,
                                      cudaStream_t stream);
+
+/* Test hook, not for production use: the SM-clock limit of the sparse
+ * decode's bounded waits in the calls that follow, for the whole process
+ * (clocks <= 0 restores the default, 2^31).  With a limit of a few clocks a
+ * normal decode gives up at its first wait that is not already complete: its
+ * CTAs stop, wait (with the default limit) for their copies and tensor-core
+ * work in flight, free their tensor memory and exit, and the call reports
+ * MSA_ERR_TIMEOUT through msa_check_device_status.  That is how the timeout
+ * path is tested without a hang or a fault.  Always returns MSA_OK. */
+msa_status msa_set_decode_wait_limit(int64_t clocks);
 
 /* Synchronise `stream`, read the workspace's error word and clear it.
  * Returns MSA_OK, MSA_ERR_DEVICE_CHECK, MSA_ERR_TIMEOUT or MSA_ERR_CUDA. */

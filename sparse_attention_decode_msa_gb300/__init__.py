@@ -71,6 +71,7 @@ _SIGNATURES = {
                                      ctypes.c_size_t, _p]),
     "msa_select_rows": (ctypes.c_int, [ctypes.POINTER(MsaShape), _p, _p, _p, _p, ctypes.c_size_t,
                                        _p]),
+    "msa_set_decode_wait_limit": (ctypes.c_int, [ctypes.c_int64]),
     "msa_check_device_status": (ctypes.c_int, [_p, _p]),
     "msa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -207,3 +208,8 @@ def msa_select_rows(shape, scores_hbt, seq_lens, selected, workspace, workspace_
 def msa_check_device_status(workspace, stream=None) -> int:
     """Synchronise, read and clear the workspace error word; returns the status code."""
     return int(load().msa_check_device_status(_ptr(workspace), _stream(stream)))
+
+
+def msa_set_decode_wait_limit(clocks: int):
+    """Test hook: the clock limit of the decode's bounded waits (<= 0: the default)."""
+    _check(load().msa_set_decode_wait_limit(int(clocks)), "msa_set_decode_wait_limit")

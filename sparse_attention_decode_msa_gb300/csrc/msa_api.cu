@@ -1,6 +1,7 @@
 // msa_api.cu -- the C ABI of include/msa.h: host-side validation, workspace
 // layout and the launch sequence.  No allocation, no global state beyond the
 // per-device SM count and the driver entry point used to encode tensor maps.
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -8,23 +9,19 @@
 #include "msa_internal.cuh"
 
 namespace msa {
-namespace {
 
-constexpr size_t kAlign = 256;
+// Clock limit of the decode's bounded waits (changed only by the test hook
+// msa_set_decode_wait_limit).
+std::atomic<long long> g_decode_wait_limit{kWaitLimit};
 
-size_t align_up(size_t v)
+long long decode_wait_limit()
 {
-    return (v + kAlign - 1) / kAlign * kAlign;
-}
-
-bool aligned16(const void *p)
-{
-    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+    return g_decode_wait_limit.load(std::memory_order_relaxed);
 }
 
 // Shape checks shared by every entry point.  many_rows: the row select, whose
 // rows per request are not limited by the decode's and scorer's tiles.
-msa_status check_shape(const msa_shape *s, bool many_rows = false)
+msa_status check_shape(const msa_shape *s, bool many_rows)
 {
     if (!s)
         return MSA_ERR_INVALID_ARGUMENT;
@@ -60,6 +57,20 @@ msa_status check_shape(const msa_shape *s, bool many_rows = false)
         (long long)s->num_pages * s->num_index_heads * kPage > 0x7FFFFFFFll)
         return MSA_ERR_UNSUPPORTED;
     return MSA_OK;
+}
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v)
+{
+    return (v + kAlign - 1) / kAlign * kAlign;
+}
+
+bool aligned16(const void *p)
+{
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
 }
 
 int tokens_of(const msa_shape *s)
@@ -223,6 +234,8 @@ msa_status decode_impl(const msa_shape *s, const void *q, const void *kv_pool,
     const bool scaled = s->kv_dtype != MSA_BF16; // E4M3 and NVFP4 carry tensor scales
     p.scale_log2 = s->softmax_scale * 1.4426950408889634f * (scaled ? s->k_scale : 1.f);
     p.v_scale = scaled ? s->v_scale : 1.f;
+    p.slots = w.slots;
+    p.wait_limit = decode_wait_limit();
     const int ctas = decode_ctas(s);
     if (ctas < 1)
         return MSA_ERR_CUDA;
@@ -444,6 +457,13 @@ msa_status msa_select_rows(const msa_shape *shape, const float *scores_hbt,
     p.init = shape->init_blocks;
     p.local = shape->local_blocks;
     return cuda_status(launch_select_rows(p, stream));
+}
+
+msa_status msa_set_decode_wait_limit(int64_t clocks)
+{
+    g_decode_wait_limit.store(clocks > 0 ? (long long)clocks : kWaitLimit,
+                              std::memory_order_relaxed);
+    return MSA_OK;
 }
 
 msa_status msa_check_device_status(void *workspace, cudaStream_t stream)

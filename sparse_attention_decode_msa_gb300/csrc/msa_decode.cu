@@ -28,10 +28,11 @@
 //   TMA.  A K stage goes back to the producer as soon as S has read it.
 // * Math.  On the tensor cores (tcgen05.mma, accumulators in TMEM), per page:
 //   S^T = K Q^T and O^T = V^T P^T, M = 128 (tokens, then dimensions), N = 16
-//   query heads; see the section before the kernel.  FP8 keys and values are
-//   widened to f16 in shared memory by four converter warps (exact), with
-//   k_scale folded into the logit scale and v_scale into the output.  Logits
-//   are kept in base 2.
+//   query heads; see the section before the kernel.  E4M3 keys and values are
+//   MMA operands as loaded (kind::f8f6f4, the query and P as E4M3 hi + lo
+//   pairs); NVFP4 keys and values are widened to f16 in shared memory by four
+//   converter warps (exact).  The tensor scales k_scale and v_scale are folded
+//   into the logit scale and the output.  Logits are kept in base 2.
 // * Every wait is bounded; a timeout sets MSA_ERR_TIMEOUT, raises a CTA abort
 //   flag that ends every other wait, and the producer waits (bounded) for its
 //   copies in flight before the CTA exits.
@@ -66,6 +67,8 @@ __device__ void build_token_prefix(const DecodeParams &p, int *qt)
                 if (sl >= 1 && nb <= p.maxB) {
                     n = ceil_div(sl + j, kPage);
                     n = n < p.k ? n : p.k;
+                } else if (blockIdx.x == 0) {
+                    set_error(p.err, kErrSeqLen); // the token gets no tasks: its outputs are not written
                 }
             }
             int incl = n;
@@ -156,7 +159,8 @@ __device__ int4 make_entry(const DecodeParams &p, long long x, const int *qt)
 // written by the softmax warps in the K-major 128-byte-swizzled form.
 // Warps: 0 = TMA producer + task table, 1 = MMA issuer + TMEM owner,
 // 2..9 = softmax (thread = one TMEM lane: a token for S^T, a dimension for
-// O^T; two warps per lane quarter, 8 heads each), 10..13 = FP8 converters.  The softmax warps exchange per-head page maxima through shared memory,
+// O^T; two warps per lane quarter, 8 heads each), 10..13 = NVFP4 converters
+// (NVFP4 K/V only).  The softmax warps exchange per-head page maxima through shared memory,
 // keep the running max / denominator per head, and fold each page's O^T into
 // 16 registers (one per head) once the next page's P^T is written.
 
@@ -173,7 +177,16 @@ constexpr int kUHeads = 8;                 // heads per softmax thread (half of 
 constexpr int kUTmemCols = 64;             // S[2] + O[2], 16 columns each
 constexpr int kUTile = 32768;              // bf16 K or V tile of one (page, KV head)
 constexpr int kUQTile = 4096;              // 16 query rows of one unit: bf16 (two 64-dim boxes) or E4M3 hi + lo
-constexpr int kUPTile = 4096;              // P^T of one page, [16 heads][128 tokens]: bf16, or E4M3 hi + lo
+constexpr int kUPTile = 4096;              // P^T of one page, [16 heads][128 tokens], one part: bf16 / f16, or E4M3 hi + lo
+
+// Bytes of one page's P^T buffer: bf16 values have room for P as a bf16
+// hi + lo pair (two 4 KiB parts, 16 significant bits), used for the page of a
+// unit that has only that page (see the softmax section); E4M3 takes an E4M3
+// hi + lo pair of 256 P, NVFP4 one f16 part.
+__host__ __device__ constexpr int p_tile_bytes(int kvf)
+{
+    return kvf == kKvBf16 ? 2 * kUPTile : kUPTile;
+}
 
 struct USmem {
     size_t ring, stage, qbuf, pbuf, bars, table, xbuf, lbuf, qsc, misc, qt, total;
@@ -197,12 +210,12 @@ __host__ __device__ inline USmem umma_layout(int T, int stages, int kvf)
     L.qbuf = off = align_to(off, 1024);    // [2] query tiles (swizzle atoms: 1024-aligned)
     off += 2 * kUQTile;
     L.pbuf = off = align_to(off, 1024);    // [2] P^T tiles
-    off += 2 * kUPTile;
+    off += 2 * (size_t)p_tile_bytes(kvf);
     // full[S], empty[S], qfull[2], qempty[2], s_full[2], s_free[2], p_full[2],
     // p_free[2], o_full[2], o_free[2], softmax sync, done, then NVFP4 only:
-    // kst_full[2], kst_empty[2], vst_full[2], vst_empty[2], qconv[2]
+    // kst_full[2], kst_empty[2], vst_full[2], vst_empty[2], qconv[2]; MMA drain
     L.bars = off = align_to(off, 8);
-    off += (size_t)(2 * stages + 16 + 2 + 10) * 8;
+    off += (size_t)(2 * stages + 16 + 2 + 10 + 1) * 8;
     L.table = off = align_to(off, 16);     // [2][kWin] int4
     off += (size_t)2 * kWin * 16;
     L.xbuf = off = align_to(off, 16);      // [2][4 quarters][16] page maxima
@@ -288,6 +301,7 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
     uint64_t *vst_full = kst_empty + 2; // NVFP4: [2] staging V written
     uint64_t *vst_empty = vst_full + 2; // NVFP4: [2] staging V read by the MMA
     uint64_t *qconv = vst_empty + 2;    // NVFP4: [2] query tile widened to f16 (kUCvtWarps)
+    uint64_t *mma_drain = qconv + 2;    // the MMAs issued before a timeout have completed (commit)
     float *qscale = reinterpret_cast<float *>(base + lay.qsc);
     int4 *table = reinterpret_cast<int4 *>(base + lay.table);
     float *xbuf = reinterpret_cast<float *>(base + lay.xbuf);
@@ -296,6 +310,13 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
     int *s_flag = reinterpret_cast<int *>(base + lay.misc) + 1; // [0] last arrival, [1] abort
     int *qt = reinterpret_cast<int *>(base + lay.qt);
     volatile int *abort_flag = s_flag + 1;
+    const long long wl = p.wait_limit; // clocks of every wait below but the final drains
+    // A wait made by every lane of a warp, with one outcome for the whole
+    // warp: a lane that saw the phase complete and one that gave up would
+    // otherwise part ways before warp-wide instructions.
+    auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait_or_abort(bar, parity, abort_flag, wl));
+    };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -326,6 +347,7 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
         }
         mbar_init(smem_u32(smx_bar), kUSmxWarps);
         mbar_init(smem_u32(done_bar), kUSmxWarps);
+        mbar_init(smem_u32(mma_drain), 1);
         s_flag[0] = 0;
         s_flag[1] = 0;
         fence_mbar_init();
@@ -372,7 +394,7 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
             const int zk = 2 * l;
             if (lane == 0 && zk >= STAGES)
                 ok = mbar_wait_or_abort(smem_u32(&empty[zk % STAGES]), ((zk / STAGES) - 1) & 1,
-                                        abort_flag);
+                                        abort_flag, wl);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok)
                 break;
@@ -390,7 +412,7 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
                 prod_last = u;
                 const int qb = prod_units & 1;
                 if (lane == 0 && prod_units >= 2)
-                    ok = mbar_wait_or_abort(smem_u32(&qempty[qb]), ((prod_units >> 1) - 1) & 1, abort_flag);
+                    ok = mbar_wait_or_abort(smem_u32(&qempty[qb]), ((prod_units >> 1) - 1) & 1, abort_flag, wl);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok)
                     break;
@@ -460,7 +482,7 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
                     const int st = z % STAGES;
                     if (kv == 1 && z >= STAGES)
                         ok = mbar_wait_or_abort(smem_u32(&empty[st]), ((z / STAGES) - 1) & 1,
-                                                abort_flag);
+                                                abort_flag, wl);
                     if (!ok)
                         break;
                     const uint32_t bar = smem_u32(&full[st]);
@@ -512,21 +534,21 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
             auto issue_s = [&](int l) -> bool {
                 const int zk = 2 * l, b = l & 1;
                 // NVFP4: K(l) widened into staging tile b; else the ring tile landed
-                if (F4 ? !mbar_wait_or_abort(smem_u32(&kst_full[b]), (l >> 1) & 1, abort_flag)
-                       : !mbar_wait_or_abort(smem_u32(&full[zk % STAGES]), (zk / STAGES) & 1, abort_flag))
+                if (F4 ? !mbar_wait_or_abort(smem_u32(&kst_full[b]), (l >> 1) & 1, abort_flag, wl)
+                       : !mbar_wait_or_abort(smem_u32(&full[zk % STAGES]), (zk / STAGES) & 1, abort_flag, wl))
                     return false;
                 const int4 e = entry(l);
                 const int u = unit_of(e);
                 if (u != s_unit) {
                     // NVFP4: the converter warps widen the query tile to f16 in place
                     uint64_t *qready = F4 ? qconv : qfull;
-                    if (!mbar_wait_or_abort(smem_u32(&qready[s_units & 1]), (s_units >> 1) & 1, abort_flag))
+                    if (!mbar_wait_or_abort(smem_u32(&qready[s_units & 1]), (s_units >> 1) & 1, abort_flag, wl))
                         return false;
                     s_unit = u;
                     ++s_units;
                 }
                 const int qb = (s_units - 1) & 1;
-                if (l >= 2 && !mbar_wait_or_abort(smem_u32(&s_free[b]), ((l >> 1) - 1) & 1, abort_flag))
+                if (l >= 2 && !mbar_wait_or_abort(smem_u32(&s_free[b]), ((l >> 1) - 1) & 1, abort_flag, wl))
                     return false;
                 tcgen05_after_sync();
                 if (e.x >= 0) {
@@ -555,25 +577,33 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
             };
             auto issue_pv = [&](int l) -> bool {
                 const int zv = 2 * l + 1, b = l & 1;
-                if (F4 ? !mbar_wait_or_abort(smem_u32(&vst_full[b]), (l >> 1) & 1, abort_flag)
-                       : !mbar_wait_or_abort(smem_u32(&full[zv % STAGES]), (zv / STAGES) & 1, abort_flag))
+                if (F4 ? !mbar_wait_or_abort(smem_u32(&vst_full[b]), (l >> 1) & 1, abort_flag, wl)
+                       : !mbar_wait_or_abort(smem_u32(&full[zv % STAGES]), (zv / STAGES) & 1, abort_flag, wl))
                     return false;
-                if (!mbar_wait_or_abort(smem_u32(&p_full[b]), (l >> 1) & 1, abort_flag))
+                if (!mbar_wait_or_abort(smem_u32(&p_full[b]), (l >> 1) & 1, abort_flag, wl))
                     return false;
-                if (l >= 2 && !mbar_wait_or_abort(smem_u32(&o_free[b]), ((l >> 1) - 1) & 1, abort_flag))
+                if (l >= 2 && !mbar_wait_or_abort(smem_u32(&o_free[b]), ((l >> 1) - 1) & 1, abort_flag, wl))
                     return false;
                 tcgen05_after_sync();
                 if (entry(l).x >= 0) {
                     const uint32_t tileV = F4 ? smem_u32(vst + b * kUTile)
                                               : smem_u32(ring + (size_t)(zv % STAGES) * kRaw);
-                    const uint32_t ptile = smem_u32(pbuf + b * kUPTile);
+                    const uint32_t ptile = smem_u32(pbuf + b * p_tile_bytes(KVF));
+                    // bf16: steps 0..7 take P hi, 8..15 (single-page units) P lo,
+                    // over the same V^T slices
+                    const int e_t = entry(l).z;
+                    const int pv_steps = (KVF == kKvBf16 && qt[e_t + 1] - qt[e_t] == 1) ? 16 : 8;
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
+                    for (int ks = 0; ks < 16; ++ks) {
+                        if (ks >= pv_steps)
+                            break;
                         if (!FP8) {
                             // V^T, MN-major: 16 tokens per k-step = 16 rows of 128 bytes;
                             // the two 64-dim halves of a row are 16 KiB apart (LBO)
-                            const uint64_t a = umma_desc_sw128(tileV + ks * 2048, kUTile / 2, 1024);
-                            const uint64_t bp = umma_desc_sw128(ptile + (ks >> 2) * (kUPTile / 2) + (ks & 3) * 32, 16, 1024);
+                            const int kt = ks & 7;
+                            const uint64_t a = umma_desc_sw128(tileV + kt * 2048, kUTile / 2, 1024);
+                            const uint64_t bp = umma_desc_sw128(
+                                ptile + (ks >> 3) * kUPTile + (kt >> 2) * (kUPTile / 2) + (kt & 3) * 32, 16, 1024);
                             umma_bf16(tmem + 32 + 16 * b, a, bp, kIdescO, ks > 0);
                         } else {
                             // V^T, MN-major: 32 tokens per k-step = 32 rows of 128 bytes
@@ -600,6 +630,9 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
             if (!ok) {
                 set_error(p.err, kErrTimeout);
                 *abort_flag = 1;
+                // the MMAs issued so far finish before TMEM is freed
+                umma_commit(smem_u32(mma_drain));
+                (void)mbar_wait_bounded(smem_u32(mma_drain), 0);
             }
         }
         __syncwarp();
@@ -658,12 +691,12 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
         auto do_kv = [&](int l, int kv) -> bool {
             const int z = 2 * l + kv, b = l & 1;
             uint64_t *st_full = kv ? vst_full : kst_full, *st_empty = kv ? vst_empty : kst_empty;
-            if (!mbar_wait_or_abort(smem_u32(&full[z % STAGES]), (z / STAGES) & 1, abort_flag))
+            if (!wait_all(smem_u32(&full[z % STAGES]), (z / STAGES) & 1))
                 return false;
             const int4 e = entry(l);
             if (kv == 0 && unit_of(e) != cur) {
                 const int qb = units & 1;
-                if (!mbar_wait_or_abort(smem_u32(&qfull[qb]), (units >> 1) & 1, abort_flag))
+                if (!wait_all(smem_u32(&qfull[qb]), (units >> 1) & 1))
                     return false;
                 uint8_t *q = qbuf + qb * kUQTile;
                 for (int i = ct; i < kUQTile / 16; i += 32 * kUCvtWarps) {
@@ -681,7 +714,7 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
                 cur = unit_of(e);
                 ++units;
             }
-            if (l >= 2 && !mbar_wait_or_abort(smem_u32(&st_empty[b]), ((l >> 1) - 1) & 1, abort_flag))
+            if (l >= 2 && !wait_all(smem_u32(&st_empty[b]), ((l >> 1) - 1) & 1))
                 return false;
             if (e.x >= 0)
                 convert(ring + (size_t)(z % STAGES) * kRaw, (kv ? vst : kst) + b * kUTile);
@@ -726,7 +759,7 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
         __syncwarp();
         if (lane == 0)
             mbar_arrive(smem_u32(smx_bar));
-        if (!mbar_wait_or_abort(smem_u32(smx_bar), sync_phase & 1, abort_flag))
+        if (!wait_all(smem_u32(smx_bar), sync_phase & 1))
             ok = false;
         ++sync_phase;
     };
@@ -748,7 +781,7 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
     // fold the previous page's O^T (thread = dimension) into o[]
     auto fold = [&](int l_prev) {
         const int b = l_prev & 1;
-        if (!mbar_wait_or_abort(smem_u32(&o_full[b]), (l_prev >> 1) & 1, abort_flag)) {
+        if (!wait_all(smem_u32(&o_full[b]), (l_prev >> 1) & 1)) {
             ok = false;
             return;
         }
@@ -812,6 +845,11 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
             }
             if (idx < kUHeads)
                 p.lse[hbase + idx] = (Mi == -INFINITY) ? -INFINITY : (Mi + log2f(Li)) * 0.69314718055994531f;
+            return;
+        }
+        if ((long long)c_last + u >= p.slots) { // the caller's scratch is short: no slot is touched
+            if (sidx == 0)
+                set_error(p.err, kErrScratch);
             return;
         }
         int arrivals = 0; // CTAs with tasks of this unit
@@ -916,7 +954,7 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
         int u = -2; // no unit: ends the last one
         float sv[kUHeads];
         if (!end) {
-            if (!mbar_wait_or_abort(smem_u32(&s_full[b]), (l >> 1) & 1, abort_flag)) {
+            if (!wait_all(smem_u32(&s_full[b]), (l >> 1) & 1)) {
                 ok = false;
                 break;
             }
@@ -993,25 +1031,41 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
             }
         }
         // P^T[h][token idx] into the K-major, 128-byte-swizzled B tile
-        if (l >= 2 && !mbar_wait_or_abort(smem_u32(&p_free[b]), ((l >> 1) - 1) & 1, abort_flag)) {
+        if (l >= 2 && !wait_all(smem_u32(&p_free[b]), ((l >> 1) - 1) & 1)) {
             ok = false;
             break;
         }
         if (live && !FP8) {
-            uint8_t *pt = pbuf + b * kUPTile + (idx >> 6) * (kUPTile / 2);
+            // bf16: hi = bf16(p); for the page of a single-page unit also
+            // lo = bf16(p - hi) (p - hi is exact in fp32) in the second part.
+            // There a handful of positions can carry the whole softmax, and
+            // P rounded to bf16 alone would put an error of up to 2^-9 |V| into
+            // O; a unit with two or more pages sees at least 129 positions
+            // (every selected block but the last visible one is full), where
+            // those roundings average out.  NVFP4: f16(p).
+            uint8_t *pt = pbuf + b * p_tile_bytes(KVF) + (idx >> 6) * (kUPTile / 2);
             const int col = idx & 63;
+            const bool hilo = !F4 && qt[e.z + 1] - qt[e.z] == 1;
 #pragma unroll
             for (int h = 0; h < kUHeads; ++h) {
                 const int hh = h0 + h;
                 const uint32_t off = hh * 128 + ((((col >> 3) ^ (hh & 7))) << 4) + (col & 7) * 2;
-                *reinterpret_cast<uint16_t *>(pt + off) =
-                    (uint16_t)((F4 ? pack_f16(pv[h], 0.f) : pack_bf16(pv[h], 0.f)) & 0xFFFFu);
+                if (F4) {
+                    *reinterpret_cast<uint16_t *>(pt + off) = (uint16_t)(pack_f16(pv[h], 0.f) & 0xFFFFu);
+                } else {
+                    const uint32_t hi = pack_bf16(pv[h], 0.f) & 0xFFFFu;
+                    *reinterpret_cast<uint16_t *>(pt + off) = (uint16_t)hi;
+                    if (hilo) {
+                        const uint32_t lo = pack_bf16(pv[h] - __uint_as_float(hi << 16), 0.f) & 0xFFFFu;
+                        *reinterpret_cast<uint16_t *>(pt + kUPTile + off) = (uint16_t)lo;
+                    }
+                }
             }
             fence_async_smem();
         } else if (live) {
             // FP8: 256 P as E4M3 hi + lo, one byte per (head row, token) in
             // each of two K-major tiles of 16 rows x 128 bytes
-            uint8_t *phi = pbuf + b * kUPTile, *plo = phi + kUPTile / 2;
+            uint8_t *phi = pbuf + b * p_tile_bytes(KVF), *plo = phi + kUPTile / 2;
 #pragma unroll
             for (int h = 0; h < kUHeads; h += 2) {
                 uint32_t hi, lo;

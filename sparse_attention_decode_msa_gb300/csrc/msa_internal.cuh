@@ -34,7 +34,11 @@ enum : uint32_t {
     kErrSeqLen = 2u,    // seq_len < 1, or cached blocks > max_blocks_per_seq
     kErrSelection = 4u, // selected block id not a visible block of the token
     kErrTimeout = 8u,   // a bounded wait ran out
+    kErrScratch = 16u,  // a decode partial slot or arrival counter outside the scratch given
 };
+
+// SM clocks after which a bounded wait gives up (about a second).
+constexpr long long kWaitLimit = 1ll << 31;
 
 // Bytes of one decode partial: o[16][128] then m[16], l[16] (fp32).
 constexpr size_t kPartialFloats = size_t(kGroup) * kDim + 2 * kGroup;
@@ -91,7 +95,17 @@ struct DecodeParams {
     int R, nq, T, Hkv, maxB, k, num_pages, Hs;
     float scale_log2; // softmax_scale * log2(e) (* k_scale for FP8 keys)
     float v_scale;    // 1 for bf16 values
+    long long slots;  // partial slots in `partial` (slot c + u of CTA c and unit u is checked)
+    long long wait_limit; // SM clocks of the decode's bounded waits (kWaitLimit unless testing)
 };
+
+// The decode's wait limit for the calls that follow (msa_set_decode_wait_limit).
+long long decode_wait_limit();
+
+// Shape checks of every entry point (MSA_OK, MSA_ERR_INVALID_ARGUMENT or
+// MSA_ERR_UNSUPPORTED); many_rows: the row select, whose rows per request are
+// not limited by the decode's and scorer's tiles.
+msa_status check_shape(const msa_shape *s, bool many_rows = false);
 
 // This step's new tokens written into their pages (the KV / index-key update).
 struct UpdateParams {
@@ -209,29 +223,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 }
 
 // Wait for phase `parity` of the barrier; false if it did not complete
-// within ~2^31 SM clocks (about a second).
+// within kWaitLimit SM clocks (about a second).
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
 {
     if (mbar_try_wait(bar, parity))
         return true;
     const long long start = clock64();
     while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - start > (1ll << 31))
+        if (clock64() - start > kWaitLimit)
             return false;
     }
     return true;
 }
 
 // Like mbar_wait_bounded, but also gives up as soon as *abort_flag is set
-// (another thread of the CTA already timed out).
+// (another thread of the CTA already timed out), and after `limit` clocks.
 __device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity,
-                                                   const volatile int *abort_flag)
+                                                   const volatile int *abort_flag,
+                                                   long long limit = kWaitLimit)
 {
     if (mbar_try_wait(bar, parity))
         return true;
     const long long start = clock64();
     while (!mbar_try_wait(bar, parity)) {
-        if (*abort_flag || clock64() - start > (1ll << 31))
+        if (*abort_flag || clock64() - start > limit)
             return false;
     }
     return true;

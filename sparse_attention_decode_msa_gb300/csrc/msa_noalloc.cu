@@ -13,8 +13,6 @@
 //
 // The kernels are exactly those of msa_sparse_decode; only where their
 // scratch lives differs.
-#include <mutex>
-
 #include "msa_internal.cuh"
 
 namespace msa {
@@ -24,25 +22,17 @@ namespace {
 // (token, KV head) unit, then the decode's partial slots.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[MSA_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-
-// Device address of g_noalloc_scratch per device.  In host code the array's
-// name only stands in for the symbol; the address the kernels need comes from
-// cudaGetSymbolAddress, taken once per device with that device current.
-void *scratch_address(int dev)
+// Device address of g_noalloc_scratch in the current device's context.  In
+// host code the array's name only stands in for the symbol; the address the
+// kernels need comes from cudaGetSymbolAddress, asked on every call (a cheap
+// lookup once the module is loaded) so that it is always the address in the
+// context that is current now, also after a cudaDeviceReset.
+void *scratch_address()
 {
-    static std::mutex mu;
-    static void *addr[kMaxDevices] = {nullptr};
-    if (dev < 0 || dev >= kMaxDevices)
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess)
         return nullptr;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess)
-            return nullptr;
-        addr[dev] = p;
-    }
-    return addr[dev];
+    return p;
 }
 
 int sm_count(int dev)
@@ -68,11 +58,10 @@ extern "C" msa_status msa_sparse_decode_noalloc(const msa_shape *shape, const vo
                                                 const int32_t *seq_lens, const int32_t *selected,
                                                 void *out, float *lse, cudaStream_t stream)
 {
-    if (!shape || shape->num_requests < 0 || shape->decode_ctas < 0)
-        return MSA_ERR_INVALID_ARGUMENT;
-    // the shape rules of every other entry point (0 = invalid or unsupported)
-    if (msa_workspace_bytes(shape) == 0)
-        return MSA_ERR_UNSUPPORTED;
+    // the shape rules of every other entry point, with their status
+    const msa_status st = check_shape(shape);
+    if (st != MSA_OK)
+        return st;
     if (!q || !kv_pool || !block_table || !seq_lens || !selected || !out || !lse)
         return MSA_ERR_INVALID_ARGUMENT;
     if (!aligned16(q) || !aligned16(kv_pool) || !aligned16(block_table) || !aligned16(seq_lens) ||
@@ -109,7 +98,7 @@ extern "C" msa_status msa_sparse_decode_noalloc(const msa_shape *shape, const vo
                       (1ull << 32),
                   "fixed scratch admits task ranges beyond 32 bits");
 
-    unsigned char *scratch = static_cast<unsigned char *>(scratch_address(dev));
+    unsigned char *scratch = static_cast<unsigned char *>(scratch_address());
     if (!scratch)
         return MSA_ERR_CUDA;
     // the error word and the arrival counters must start at zero; the partial
@@ -138,6 +127,10 @@ extern "C" msa_status msa_sparse_decode_noalloc(const msa_shape *shape, const vo
     const bool scaled = shape->kv_dtype != MSA_BF16; // E4M3 and NVFP4 carry tensor scales
     p.scale_log2 = shape->softmax_scale * 1.4426950408889634f * (scaled ? shape->k_scale : 1.f);
     p.v_scale = scaled ? shape->v_scale : 1.f;
+    // slots the array holds after the head (the kernel checks every slot it
+    // touches against it, so no problem can write past the array)
+    p.slots = ((long long)MSA_NOALLOC_SCRATCH_BYTES - head) / (long long)kPartialBytes;
+    p.wait_limit = decode_wait_limit();
     return launch_sparse_decode(p, kv_pool, shape->kv_dtype, ctas, stream, false) == cudaSuccess
                ? MSA_OK
                : MSA_ERR_CUDA;

@@ -98,48 +98,101 @@ def test_invalid_shapes_are_rejected(lib, field, value):
     assert st == msa.MSA_ERR_INVALID_ARGUMENT
 
 
+# Calls with stand-in device addresses run in a child process that sees no
+# GPU: host validation must refuse them before anything is launched, and if it
+# ever stopped doing so the child gets a CUDA error, never a kernel reading
+# memory that is not there.
+CHILD_PRELUDE = """
+import ctypes, json, sys
+sys.path.insert(0, {root!r})
+import sparse_attention_decode_msa_gb300 as msa
+lib = msa.load()
+lib.msa_sparse_decode_noalloc.restype = ctypes.c_int
+lib.msa_sparse_decode_noalloc.argtypes = [ctypes.POINTER(msa.MsaShape)] + [ctypes.c_void_p] * 8
+def shape(**kw):
+    base = dict(num_requests=8, q_per_req=4, num_kv_heads=4, num_pages=4096,
+                max_blocks_per_seq=256, topk=16)
+    base.update(kw)
+    return msa.make_shape(**base)
+fake = 0x10000
+out = []
+"""
+
+
+def statuses_without_a_gpu(body: str) -> list:
+    import json
+    import subprocess
+    import sys
+
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    code = CHILD_PRELUDE.format(root=ROOT) + body + "\nprint(json.dumps(out))\n"
+    res = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                         timeout=300)
+    assert res.returncode == 0, res.stderr
+    return json.loads(res.stdout.strip().splitlines()[-1])
+
+
 def test_null_and_misaligned_pointers_are_rejected_on_the_host(lib):
-    s = shape()
-    ws_bytes = msa.msa_workspace_bytes(s)
-    fake = 0x10000  # never dereferenced: validation fails first
-    args = [fake] * 7
-    # no workspace
-    assert lib.msa_sparse_decode(msa.ctypes.byref(s), *args, None, ws_bytes, None) == 1
-    # workspace too small
-    assert lib.msa_sparse_decode(msa.ctypes.byref(s), *args, fake, ws_bytes - 1, None) == 1
-    # a null input
-    bad = list(args)
-    bad[1] = None
-    assert lib.msa_sparse_decode(msa.ctypes.byref(s), *bad, fake, ws_bytes, None) == 1
-    # a misaligned input
-    bad = list(args)
-    bad[0] = fake + 2
-    assert lib.msa_sparse_decode(msa.ctypes.byref(s), *bad, fake, ws_bytes, None) == 1
-    # NVFP4 index keys need their scales
-    s4 = shape(index_dtype=2)
-    assert lib.msa_index_score(msa.ctypes.byref(s4), fake, fake, None, fake, fake, fake, fake,
-                               msa.msa_workspace_bytes(s4), None) == 1
+    got = statuses_without_a_gpu("""
+s = shape()
+ws_bytes = msa.msa_workspace_bytes(s)
+args = [fake] * 7
+out.append(lib.msa_sparse_decode(ctypes.byref(s), *args, None, ws_bytes, None))       # no workspace
+out.append(lib.msa_sparse_decode(ctypes.byref(s), *args, fake, ws_bytes - 1, None))   # too small
+bad = list(args); bad[1] = None
+out.append(lib.msa_sparse_decode(ctypes.byref(s), *bad, fake, ws_bytes, None))        # a null input
+bad = list(args); bad[0] = fake + 2
+out.append(lib.msa_sparse_decode(ctypes.byref(s), *bad, fake, ws_bytes, None))        # misaligned
+s4 = shape(index_dtype=2)                                                              # NVFP4 keys
+out.append(lib.msa_index_score(ctypes.byref(s4), fake, fake, None, fake, fake, fake, fake,
+                               msa.msa_workspace_bytes(s4), None))                     # need scales
+bad = [fake] * 7; bad[3] = None
+out.append(lib.msa_sparse_decode_noalloc(ctypes.byref(s), *bad, None))                # no-alloc: null
+bad = [fake] * 7; bad[6] = fake + 4
+out.append(lib.msa_sparse_decode_noalloc(ctypes.byref(s), *bad, None))                # misaligned
+""")
+    assert got == [msa.MSA_ERR_INVALID_ARGUMENT] * 7
 
 
 def test_decode_beyond_32_bit_task_ranges_is_unsupported(lib):
     # T * Hkv * topk * (decode CTAs + 1) >= 2^32: the decode's cut of its
     # tasks into CTA ranges would not fit 32-bit arithmetic; refused on the
     # host before anything is launched (the CTA count given: no device query)
-    s = shape(num_requests=2048, q_per_req=4, topk=256)
-    s.decode_ctas = 1024
     assert 2048 * 4 * 4 * 256 * 1025 >= 2 ** 32
-    ws_bytes = msa.msa_workspace_bytes(s)
-    assert ws_bytes > 0
-    fake = 0x10000
-    assert lib.msa_sparse_decode(msa.ctypes.byref(s), *([fake] * 7), fake, ws_bytes, None) == 2
-    assert lib.msa_decode_step(msa.ctypes.byref(s), *([fake] * 11), fake, ws_bytes, None) == 2
+    got = statuses_without_a_gpu("""
+s = shape(num_requests=2048, q_per_req=4, topk=256)
+s.decode_ctas = 1024
+ws_bytes = msa.msa_workspace_bytes(s)
+out.append(ws_bytes > 0)
+out.append(lib.msa_sparse_decode(ctypes.byref(s), *([fake] * 7), fake, ws_bytes, None))
+out.append(lib.msa_decode_step(ctypes.byref(s), *([fake] * 11), fake, ws_bytes, None))
+""")
+    assert got == [True, msa.MSA_ERR_UNSUPPORTED, msa.MSA_ERR_UNSUPPORTED]
 
 
 def test_zero_requests_is_a_validated_no_op(lib):
-    s = shape(num_requests=0)
-    ws_bytes = msa.msa_workspace_bytes(s)
-    fake = 0x10000
-    assert lib.msa_decode_step(msa.ctypes.byref(s), *([fake] * 11), fake, ws_bytes, None) == 0
+    got = statuses_without_a_gpu("""
+s = shape(num_requests=0)
+ws_bytes = msa.msa_workspace_bytes(s)
+out.append(lib.msa_decode_step(ctypes.byref(s), *([fake] * 11), fake, ws_bytes, None))
+out.append(lib.msa_sparse_decode_noalloc(ctypes.byref(s), *([fake] * 7), None))
+""")
+    assert got == [msa.MSA_OK, msa.MSA_OK]
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("topk", 0, msa.MSA_ERR_INVALID_ARGUMENT), ("decode_ctas", -1, msa.MSA_ERR_INVALID_ARGUMENT),
+    ("local_blocks", 17, msa.MSA_ERR_INVALID_ARGUMENT), ("head_dim", 64, msa.MSA_ERR_UNSUPPORTED),
+    ("q_per_req", 65, msa.MSA_ERR_UNSUPPORTED),
+])
+def test_no_alloc_decode_gives_shape_statuses_of_the_other_entry_points(lib, field, value, status):
+    # the shape is refused before any pointer is looked at (all NULL here)
+    s = shape()
+    setattr(s, field, value)
+    lib.msa_sparse_decode_noalloc.restype = msa.ctypes.c_int
+    lib.msa_sparse_decode_noalloc.argtypes = [msa.ctypes.POINTER(msa.MsaShape)] + [
+        msa.ctypes.c_void_p] * 8
+    assert lib.msa_sparse_decode_noalloc(msa.ctypes.byref(s), *([None] * 8)) == status
 
 
 def test_forced_blocks_may_fill_but_not_exceed_topk(lib):

@@ -40,21 +40,43 @@ def half_ulp_bf16(x):
     return np.where(x == 0, 0.0, np.ldexp(1.0, e - 9))
 
 
-def assert_attention_close(gpu_out, gpu_lse, ref_out, ref_lse, tokens, strict=True):
-    """strict: |dO| <= 4e-3 everywhere (holds when |O| < 2, as in every
-    workload).  Otherwise 4e-3 of accumulation error plus the bf16 rounding
-    of the stored output, which alone reaches 7.8e-3 once |O| >= 2 (a
-    softmax over one or two N(0,1) values)."""
+def visible_positions(pb, selected, tokens):
+    """Positions each token of `tokens` attends to (the visible positions of
+    its selected blocks; the fewest over its selection heads)."""
+    sel = np.asarray(selected).reshape(len(tokens), -1, pb.topk)
+    out = np.empty(len(tokens), dtype=np.int64)
+    for i, t in enumerate(tokens):
+        L = int(pb.seq_lens[t // pb.q_per_req]) + t % pb.q_per_req
+        b = sel[i].astype(np.int64)
+        n = np.where(b >= 0, np.clip(L - 128 * b, 0, 128), 0).sum(axis=-1)
+        out[i] = n.min()
+    return out
+
+
+def assert_attention_close(gpu_out, gpu_lse, ref_out, ref_lse, tokens, visible=None,
+                           nvfp4_kv=False):
+    """|dO| <= 4e-3 and rel |dLSE| <= 1e-4 (the workload contract), with the
+    bf16 storage allowance of the design's output-tolerance reading: an
+    element may add half a bf16 ulp of the reference where that rounding
+    alone can exceed 4e-3 (|O_ref| >= 2, half an ulp >= 7.8e-3), or where the
+    token sees at most two positions (`visible`, per token of `tokens`: O is
+    then one or two values of V).  nvfp4_kv: NVFP4 values reach 6, the
+    allowance holds for every element."""
+    tokens = list(tokens)
     out = gpu_out[tokens]
     lse = gpu_lse[tokens]
     assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
     diff = np.abs(out - ref_out)
-    if strict:
-        err = diff.max()
-        assert err <= OUT_ATOL, f"max |dO| = {err}"
-    else:
-        excess = (diff - OUT_ATOL - half_ulp_bf16(ref_out)).max()
-        assert excess <= 0, f"max |dO| beyond 4e-3 + half bf16 ulp: {excess}"
+    allow = np.abs(ref_out) >= 2.0
+    if visible is not None:
+        few = np.asarray(visible) <= 2
+        allow |= few.reshape((-1,) + (1,) * (ref_out.ndim - 1))
+    if nvfp4_kv:
+        allow[...] = True
+    bound = OUT_ATOL + np.where(allow, half_ulp_bf16(ref_out), 0.0)
+    excess = (diff - bound).max()
+    assert excess <= 0, (f"max |dO| beyond the bound by {excess} (max |dO| = {diff.max()}, "
+                         f"{int(allow.sum())} of {allow.size} elements with the bf16 allowance)")
     lerr = (np.abs(lse - ref_lse) / np.maximum(np.abs(ref_lse), 1.0)).max()
     assert lerr <= LSE_RTOL, f"max rel |dLSE| = {lerr}"
 
@@ -257,8 +279,9 @@ def test_short_contexts_pad_with_minus_one_and_single_position(torch_cuda):
     res = dp.results()
     assert res["selected"][0].tolist() == [0] + [-1] * 7
     assert np.array_equal(res["selected"], ref["selected"])
-    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens),
-                           strict=False)
+    tokens = range(pb.num_tokens)
+    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], tokens,
+                           visible=visible_positions(pb, ref["selected"], tokens))
 
 
 def test_page_aligned_contexts_and_dense_coverage(torch_cuda):
@@ -270,8 +293,7 @@ def test_page_aligned_contexts_and_dense_coverage(torch_cuda):
     dp.decode_step()
     res = dp.results()
     assert np.array_equal(res["selected"], ref["selected"])
-    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens),
-                           strict=False)
+    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens))
 
 
 def test_all_zero_index_keys_tie_everywhere(torch_cuda):
@@ -284,8 +306,7 @@ def test_all_zero_index_keys_tie_everywhere(torch_cuda):
     res = dp.results()
     assert np.all(res["selected"] == np.arange(16))
     assert np.array_equal(res["selected"], ref["selected"])
-    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens),
-                           strict=False)
+    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens))
 
 
 def test_max_topk_and_wide_block_table(torch_cuda):
@@ -296,8 +317,7 @@ def test_max_topk_and_wide_block_table(torch_cuda):
     dp.decode_step()
     res = dp.results()
     assert np.array_equal(res["selected"], ref["selected"])
-    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens),
-                           strict=False)
+    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens))
 
 
 def test_largest_request_count(torch_cuda):
@@ -316,7 +336,8 @@ def test_largest_request_count(torch_cuda):
     ref = oracle.decode_step(pb, tokens=tokens, threads=THREADS)
     assert_scores_equal(pb, res["block_scores"], ref["block_scores"], tokens)
     assert np.array_equal(res["selected"][tokens], ref["selected"])
-    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], tokens, strict=False)
+    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], tokens,
+                           visible=visible_positions(pb, ref["selected"], tokens))
     check_device_ok(dp)
 
 
@@ -359,8 +380,7 @@ def test_large_speculative_step(torch_cuda):
     res = dp.results()
     assert_scores_equal(pb, res["block_scores"], ref["block_scores"], range(pb.num_tokens))
     assert np.array_equal(res["selected"], ref["selected"])
-    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens),
-                           strict=False)
+    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens))
 
 
 def test_bad_page_id_is_reported_not_faulted(torch_cuda):
@@ -384,3 +404,52 @@ def test_bad_seq_len_is_reported_not_faulted(torch_cuda):
     dp = device_problem(pb)
     dp.decode_step()
     assert msa.msa_check_device_status(dp.ws) == msa.MSA_ERR_DEVICE_CHECK
+
+
+def test_bad_seq_len_is_reported_by_the_decode_alone(torch_cuda):
+    # the decode reads seq_lens itself: called without the scorer and the
+    # select, it reports a token whose seq_len does not fit the block table
+    torch = torch_cuda
+    import sparse_attention_decode_msa_gb300 as msa
+
+    pb = synth.make_problem(name="badlen-decode", contexts=[700, 900], q_per_req=1,
+                            num_kv_heads=1, topk=4, seed=28)
+    sel = torch.tensor([[[0, 1, 2, 5]], [[0, 1, 2, 3]]], dtype=torch.int32, device="cuda")
+    for bad in (0, pb.max_blocks * 128 + 1):
+        pb.seq_lens[1] = bad
+        dp = device_problem(pb)
+        dp.sparse_decode(selected=sel)
+        assert msa.msa_check_device_status(dp.ws) == msa.MSA_ERR_DEVICE_CHECK, bad
+
+
+@pytest.mark.parametrize("kv_dtype", [synth.BF16, synth.FP8, synth.NVFP4])
+def test_a_wait_that_runs_out_reports_timeout_and_the_next_call_is_exact(torch_cuda, kv_dtype):
+    # With a wait limit of a few clocks the decode gives up at its first wait
+    # that is not already complete: every CTA stops, drains its copies and
+    # tensor-core work in flight (with the normal limit), frees its tensor
+    # memory and exits; the call reports MSA_ERR_TIMEOUT.  After the workspace
+    # is re-initialised the same call gives the oracle's result.
+    torch = torch_cuda
+    import sparse_attention_decode_msa_gb300 as msa
+
+    pb = synth.make_problem(name="timeout", contexts=[3000, 1300, 5000], q_per_req=2,
+                            num_kv_heads=2, topk=6, kv_dtype=kv_dtype, seed=29)
+    if kv_dtype == synth.NVFP4:
+        pb.k_scale, pb.v_scale = 0.75, 0.5
+    ref = oracle.decode_step(pb, threads=THREADS)
+    sel = torch.from_numpy(ref["selected"][:, None, :].copy()).cuda()
+    for ctas in (3, 0):  # split units (the merge path) and the default one CTA per SM
+        dp = device_problem(pb, decode_ctas=ctas)
+        msa.msa_set_decode_wait_limit(4)
+        try:
+            dp.sparse_decode(selected=sel)
+            status = msa.msa_check_device_status(dp.ws)
+        finally:
+            msa.msa_set_decode_wait_limit(0)
+        assert status == msa.MSA_ERR_TIMEOUT, msa.status_string(status)
+        msa.msa_workspace_init(dp.ws, dp.ws_bytes)
+        dp.sparse_decode(selected=sel)
+        res = dp.results()
+        assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"],
+                               range(pb.num_tokens), nvfp4_kv=kv_dtype == synth.NVFP4)
+        check_device_ok(dp)

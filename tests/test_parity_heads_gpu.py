@@ -101,8 +101,7 @@ def test_forcing_on_the_long_row_select(torch_cuda):
     dp.decode_step()
     res = dp.results()
     assert np.array_equal(res["selected"], ref["selected"])
-    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens),
-                           strict=False)
+    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens))
 
 
 def test_forcing_all_places(torch_cuda):

@@ -31,7 +31,7 @@ def test_nvfp4_kv_fused_step(torch_cuda, hkv, nq):
     res = dp.results()
     assert np.array_equal(res["selected"], ref["selected"])
     assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens),
-                           strict=False)
+                           nvfp4_kv=True)
     check_device_ok(dp)
 
 
@@ -45,7 +45,7 @@ def test_nvfp4_kv_split_independence_on_oracle_tables(torch_cuda, ctas):
     dp.sparse_decode()
     res = dp.results()
     assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens),
-                           strict=False)
+                           nvfp4_kv=True)
     check_device_ok(dp)
 
 
@@ -57,7 +57,7 @@ def test_nvfp4_kv_with_index_heads_and_forcing(torch_cuda):
     res = dp.results()
     assert np.array_equal(res["selected"], ref["selected"])
     assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens),
-                           strict=False)
+                           nvfp4_kv=True)
 
 
 def test_nvfp4_kv_update_bytes_and_step(torch_cuda):
@@ -73,5 +73,5 @@ def test_nvfp4_kv_update_bytes_and_step(torch_cuda):
     res = dp.results()
     assert np.array_equal(res["selected"], ref["selected"])
     assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens),
-                           strict=False)
+                           nvfp4_kv=True)
     check_device_ok(dp)
