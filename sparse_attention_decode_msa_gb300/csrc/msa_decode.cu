@@ -152,15 +152,16 @@ __device__ int4 make_entry(const DecodeParams &p, long long x, const int *qt)
 // Per page (task) of unit (t, g):
 //   S^T[128 tok][16 heads] = K[128 tok][128 dim] . Q^T          (M=128, N=16, K=128)
 //   O^T[128 dim][16 heads] = V^T[128 dim][128 tok] . P^T        (M=128, N=16, K=128)
-// both issued by one thread as tcgen05.mma.kind::f16 (8 instructions of K=16
-// each), fp32 accumulators in TMEM (double-buffered: S at columns 0/16, O at
-// 32/48).  Operands: K tile and the unit's Q rows are K-major with the TMA's
+// each issued by one thread as tcgen05.mma.kind::f16 (8 instructions of K=16
+// each), fp32 accumulators in TMEM (S at columns 0/16/32/48, O at 64/80).  Operands: K tile and the unit's Q rows are K-major with the TMA's
 // 128-byte swizzle; the V tile, as loaded, is the MN-major form of V^T; P^T is
 // written by the softmax warps in the K-major 128-byte-swizzled form.
-// Warps: 0 = TMA producer + task table, 1 = MMA issuer + TMEM owner,
+// Warps: 0 = TMA producer + task table, 1 = S^T issuer + TMEM owner,
 // 2..9 = softmax (thread = one TMEM lane: a token for S^T, a dimension for
-// O^T; two warps per lane quarter, 8 heads each), 10..13 = NVFP4 converters
-// (NVFP4 K/V only).  The softmax warps exchange per-head page maxima through shared memory,
+// O^T; two warps per lane quarter, 8 heads each), 10 = O^T issuer,
+// 11..14 = NVFP4 converters (NVFP4 K/V only).  The two MMA issuers are
+// separate threads so that S^T of the next pages (four accumulators) is
+// never queued behind P^T of this one.  The softmax warps exchange per-head page maxima through shared memory,
 // keep the running max / denominator per head, and fold each page's O^T into
 // 16 registers (one per head) once the next page's P^T is written.
 
@@ -169,12 +170,16 @@ constexpr int kUCvtWarps = 4;              // NVFP4 only: e2m1 x E4M3 -> f16 con
 // KV formats of the kernel instances
 constexpr int kKvBf16 = 0, kKvFp8 = 1, kKvNvfp4 = 2;
 template <int KVF>
-constexpr int kUThreadsT = 32 * (2 + kUSmxWarps + (KVF == kKvNvfp4 ? kUCvtWarps : 0)); // producer, MMA, softmax[, converters]
+constexpr int kUThreadsT = 32 * (3 + kUSmxWarps + (KVF == kKvNvfp4 ? kUCvtWarps : 0)); // producer, S MMA, softmax, PV MMA[, converters]
+constexpr int kUWarpPV = 2 + kUSmxWarps;   // the warp that issues the P.V MMAs
+constexpr int kUWarpCvt = 3 + kUSmxWarps;  // NVFP4: the first converter warp
 constexpr int kF4Tile = kPage * kDim / 2 + kPage * kDim / 16; // NVFP4 K or V tile: codes then scales
 constexpr int kUQScales = 16;              // FP8: ring of per-unit query scales (> units in flight)
 constexpr float kPScale = 256.f;           // FP8: P^T is stored as 256 * P (E4M3 hi + lo)
 constexpr int kUHeads = 8;                 // heads per softmax thread (half of the group)
-constexpr int kUTmemCols = 64;             // S[2] + O[2], 16 columns each
+constexpr int kUSBufs = 4;                 // S^T accumulators: the S issuer runs up to 4 pages ahead
+constexpr int kUOCol = 16 * kUSBufs;       // first TMEM column of the two O^T accumulators
+constexpr int kUTmemCols = 128;            // S[4] + O[2], 16 columns each (96, allocated as 128)
 constexpr int kUTile = 32768;              // bf16 K or V tile of one (page, KV head)
 constexpr int kUQTile = 4096;              // 16 query rows of one unit: bf16 (two 64-dim boxes) or E4M3 hi + lo
 constexpr int kUPTile = 4096;              // P^T of one page, [16 heads][128 tokens], one part: bf16 / f16, or E4M3 hi + lo
@@ -211,11 +216,12 @@ __host__ __device__ inline USmem umma_layout(int T, int stages, int kvf)
     off += 2 * kUQTile;
     L.pbuf = off = align_to(off, 1024);    // [2] P^T tiles
     off += 2 * (size_t)p_tile_bytes(kvf);
-    // full[S], empty[S], qfull[2], qempty[2], s_full[2], s_free[2], p_full[2],
+    // full[S], empty[S], qfull[2], qempty[2], s_full[4], s_free[4], p_full[2],
     // p_free[2], o_full[2], o_free[2], softmax sync, done, then NVFP4 only:
-    // kst_full[2], kst_empty[2], vst_full[2], vst_empty[2], qconv[2]; MMA drain
+    // kst_full[2], kst_empty[2], vst_full[2], vst_empty[2], qconv[2]; S and
+    // PV drains, PV issuer done
     L.bars = off = align_to(off, 8);
-    off += (size_t)(2 * stages + 16 + 2 + 10 + 1) * 8;
+    off += (size_t)(2 * stages + 12 + 2 * kUSBufs + 2 + 10 + 3) * 8;
     L.table = off = align_to(off, 16);     // [2][kWin] int4
     off += (size_t)2 * kWin * 16;
     L.xbuf = off = align_to(off, 16);      // [2][4 quarters][16] page maxima
@@ -288,9 +294,9 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
     uint64_t *empty = full + STAGES;
     uint64_t *qfull = empty + STAGES;
     uint64_t *qempty = qfull + 2;
-    uint64_t *s_full = qempty + 2;
-    uint64_t *s_free = s_full + 2;
-    uint64_t *p_full = s_free + 2;
+    uint64_t *s_full = qempty + 2;       // [kUSBufs]
+    uint64_t *s_free = s_full + kUSBufs; // [kUSBufs]
+    uint64_t *p_full = s_free + kUSBufs;
     uint64_t *p_free = p_full + 2;
     uint64_t *o_full = p_free + 2;
     uint64_t *o_free = o_full + 2;
@@ -301,7 +307,9 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
     uint64_t *vst_full = kst_empty + 2; // NVFP4: [2] staging V written
     uint64_t *vst_empty = vst_full + 2; // NVFP4: [2] staging V read by the MMA
     uint64_t *qconv = vst_empty + 2;    // NVFP4: [2] query tile widened to f16 (kUCvtWarps)
-    uint64_t *mma_drain = qconv + 2;    // the MMAs issued before a timeout have completed (commit)
+    uint64_t *s_drain = qconv + 2;      // the S MMAs issued before a timeout have completed (commit)
+    uint64_t *pv_drain = s_drain + 1;   // the same for the PV MMAs
+    uint64_t *pv_done = pv_drain + 1;   // the PV issuer has finished (1 arrival)
     float *qscale = reinterpret_cast<float *>(base + lay.qsc);
     int4 *table = reinterpret_cast<int4 *>(base + lay.table);
     float *xbuf = reinterpret_cast<float *>(base + lay.xbuf);
@@ -338,16 +346,20 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&qfull[b]), 1);
             mbar_init(smem_u32(&qempty[b]), 1);
-            mbar_init(smem_u32(&s_full[b]), 1);
-            mbar_init(smem_u32(&s_free[b]), kUSmxWarps);
             mbar_init(smem_u32(&p_full[b]), kUSmxWarps);
             mbar_init(smem_u32(&p_free[b]), 1);
             mbar_init(smem_u32(&o_full[b]), 1);
             mbar_init(smem_u32(&o_free[b]), kUSmxWarps);
         }
+        for (int i = 0; i < kUSBufs; ++i) {
+            mbar_init(smem_u32(&s_full[i]), 1);
+            mbar_init(smem_u32(&s_free[i]), kUSmxWarps);
+        }
         mbar_init(smem_u32(smx_bar), kUSmxWarps);
         mbar_init(smem_u32(done_bar), kUSmxWarps);
-        mbar_init(smem_u32(mma_drain), 1);
+        mbar_init(smem_u32(s_drain), 1);
+        mbar_init(smem_u32(pv_drain), 1);
+        mbar_init(smem_u32(pv_done), 1);
         s_flag[0] = 0;
         s_flag[1] = 0;
         fence_mbar_init();
@@ -365,6 +377,76 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
     const long long x_begin = (uint32_t)c * (uint32_t)P / (uint32_t)G; // 32-bit: see owner_of
     const long long x_end = (uint32_t)(c + 1) * (uint32_t)P / (uint32_t)G;
     const int ntasks = (int)(x_end - x_begin);
+
+    // The query rows of unit number unit_no of this CTA (16 rows from `row`)
+    // into query buffer qb; called by the whole producer warp.  bf16 and
+    // NVFP4 K/V: one TMA copy (two 64-dim boxes); E4M3 K/V: converted here.
+    int q_issued = 0; // TMA query loads issued (for the drain after a timeout)
+    auto load_q = [&](int qb, int row, int unit_no) {
+        if (!FP8) {
+            if (lane == 0) {
+                const uint32_t qbar = smem_u32(&qfull[qb]);
+                const uint32_t dst = smem_u32(qbuf + qb * kUQTile);
+                mbar_arrive_expect_tx(qbar, kUQTile);
+                tma_load_2d(dst, &q_map, 0, row, qbar);
+                tma_load_2d(dst + kUQTile / 2, &q_map, 64, row, qbar);
+                q_issued = unit_no + 1;
+            }
+        } else {
+            // E4M3 hi + lo tiles of s * q (K-major, 128-byte swizzle),
+            // s = 2^k with max |s q| in [128, 256): lane = (row, 64 dims)
+            const int r = lane >> 1, hf = lane & 1;
+            const uint4 *src = reinterpret_cast<const uint4 *>(p.q + (size_t)(row + r) * kDim + hf * 64);
+            uint4 v[8];
+            float mx = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                v[i] = __ldg(src + i);
+                const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w4[j] << 16)),
+                                         fabsf(__uint_as_float(w4[j] & 0xFFFF0000u))));
+            }
+            mx = warp_max_f32(mx);
+            int k = 0;
+            if (mx > 0.f && mx < INFINITY) {
+                k = 7 - ((int)((__float_as_uint(mx) >> 23) & 0xFFu) - 127);
+                k = k < -100 ? -100 : (k > 100 ? 100 : k);
+            }
+            const float sq = __uint_as_float((uint32_t)(127 + k) << 23);
+            uint8_t *qhi = qbuf + qb * kUQTile, *qlo = qhi + kUQTile / 2;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) { // 16 dims = one 16-byte chunk of E4M3
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int w = 0; w < 4; ++w) { // 4 dims = 2 words of the bf16 input
+                    const int i = 2 * j + (w >> 1);
+                    const uint32_t a = (&v[i].x)[2 * (w & 1)], b = (&v[i].x)[2 * (w & 1) + 1];
+                    uint32_t h01, l01, h23, l23;
+                    split_e4m3x2(__uint_as_float(a << 16) * sq, __uint_as_float(a & 0xFFFF0000u) * sq, h01, l01);
+                    split_e4m3x2(__uint_as_float(b << 16) * sq, __uint_as_float(b & 0xFFFF0000u) * sq, h23, l23);
+                    hw[w] = h01 | (h23 << 16);
+                    lw[w] = l01 | (l23 << 16);
+                }
+                const int off = r * 128 + (((4 * hf + j) ^ (r & 7)) << 4);
+                *reinterpret_cast<uint4 *>(qhi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4 *>(qlo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
+            if (lane == 0)
+                qscale[unit_no % kUQScales] = __uint_as_float((uint32_t)(127 - k) << 23);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_u32(&qfull[qb]));
+        }
+    };
+    // The queries do not depend on the previous kernel of the step: the first
+    // unit's rows are staged before the grid wait.
+    if (warp == 0 && ntasks > 0) {
+        const Task t0 = task_of(x_begin, qt, p.T);
+        load_q(0, (t0.t * p.Hkv + t0.g) * kGroup, 0);
+    }
 
     grid_dependency_wait(); // `selected` comes from the previous kernel of the step
 
@@ -388,7 +470,7 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
         // =================== producer ===================
         constexpr int kAhead = STAGES / 2;
         const uint64_t kv_policy = l2_evict_first_policy(); // pages are streamed
-        int issued = 0, q_issued = 0, prod_units = 0, prod_last = -1;
+        int issued = 0, prod_units = 0, prod_last = -1;
         bool ok = true;
         for (int l = 0; l < ntasks && ok; ++l) {
             const int zk = 2 * l;
@@ -398,81 +480,29 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok)
                 break;
-            // The softmax warps trail the MMA warp by up to two tasks and the MMA
-            // warp trails this one by up to kAhead (kAhead + 2 with the NVFP4
-            // converters and their two staging tiles between them): only
-            // kAhead + 3 (+ 2) tasks into a window has every reader left the
-            // window before it.
+            // The slowest reader of the table is the P.V issuer: issuing V(l)
+            // needs the stage of V(l - kAhead), which its P.V MMAs free, so
+            // that reader trails this warp by at most kAhead tasks (kAhead + 2
+            // with the NVFP4 converters and their two staging tiles between
+            // them); the softmax warps, the S issuer and the converters are
+            // ahead of it.  Only kAhead + 3 (+ 2) tasks into a window has
+            // every reader left the window before it.
             if (l % kWin == kAhead + 3 + (F4 ? 2 : 0) && l >= kWin && (l / kWin + 1) * kWin < ntasks)
                 fill_window(l / kWin + 1);
             const int4 e = entry(l);
             const int u = unit_of(e);
             if (u != prod_last) {
-                // the unit's 16 query rows into query buffer qb
+                // the unit's 16 query rows into query buffer qb (the first
+                // unit's were staged before the grid wait)
                 prod_last = u;
                 const int qb = prod_units & 1;
-                if (lane == 0 && prod_units >= 2)
-                    ok = mbar_wait_or_abort(smem_u32(&qempty[qb]), ((prod_units >> 1) - 1) & 1, abort_flag, wl);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok)
-                    break;
-                const int row = (e.z * p.Hkv + e.w) * kGroup;
-                if (!FP8) {
-                    if (lane == 0) {
-                        const uint32_t qbar = smem_u32(&qfull[qb]);
-                        const uint32_t dst = smem_u32(qbuf + qb * kUQTile);
-                        mbar_arrive_expect_tx(qbar, kUQTile);
-                        tma_load_2d(dst, &q_map, 0, row, qbar);
-                        tma_load_2d(dst + kUQTile / 2, &q_map, 64, row, qbar);
-                        q_issued = prod_units + 1;
-                    }
-                } else {
-                    // E4M3 hi + lo tiles of s * q (K-major, 128-byte swizzle),
-                    // s = 2^k with max |s q| in [128, 256): lane = (row, 64 dims)
-                    const int r = lane >> 1, hf = lane & 1;
-                    const uint4 *src = reinterpret_cast<const uint4 *>(p.q + (size_t)(row + r) * kDim + hf * 64);
-                    uint4 v[8];
-                    float mx = 0.f;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        v[i] = __ldg(src + i);
-                        const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w4[j] << 16)),
-                                                 fabsf(__uint_as_float(w4[j] & 0xFFFF0000u))));
-                    }
-                    mx = warp_max_f32(mx);
-                    int k = 0;
-                    if (mx > 0.f && mx < INFINITY) {
-                        k = 7 - ((int)((__float_as_uint(mx) >> 23) & 0xFFu) - 127);
-                        k = k < -100 ? -100 : (k > 100 ? 100 : k);
-                    }
-                    const float sq = __uint_as_float((uint32_t)(127 + k) << 23);
-                    uint8_t *qhi = qbuf + qb * kUQTile, *qlo = qhi + kUQTile / 2;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) { // 16 dims = one 16-byte chunk of E4M3
-                        uint32_t hw[4], lw[4];
-#pragma unroll
-                        for (int w = 0; w < 4; ++w) { // 4 dims = 2 words of the bf16 input
-                            const int i = 2 * j + (w >> 1);
-                            const uint32_t a = (&v[i].x)[2 * (w & 1)], b = (&v[i].x)[2 * (w & 1) + 1];
-                            uint32_t h01, l01, h23, l23;
-                            split_e4m3x2(__uint_as_float(a << 16) * sq, __uint_as_float(a & 0xFFFF0000u) * sq, h01, l01);
-                            split_e4m3x2(__uint_as_float(b << 16) * sq, __uint_as_float(b & 0xFFFF0000u) * sq, h23, l23);
-                            hw[w] = h01 | (h23 << 16);
-                            lw[w] = l01 | (l23 << 16);
-                        }
-                        const int off = r * 128 + (((4 * hf + j) ^ (r & 7)) << 4);
-                        *reinterpret_cast<uint4 *>(qhi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                        *reinterpret_cast<uint4 *>(qlo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-                    }
-                    if (lane == 0)
-                        qscale[prod_units % kUQScales] = __uint_as_float((uint32_t)(127 - k) << 23);
-                    fence_async_smem();
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(smem_u32(&qfull[qb]));
+                if (prod_units > 0) {
+                    if (lane == 0 && prod_units >= 2)
+                        ok = mbar_wait_or_abort(smem_u32(&qempty[qb]), ((prod_units >> 1) - 1) & 1, abort_flag, wl);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok)
+                        break;
+                    load_q(qb, (e.z * p.Hkv + e.w) * kGroup, prod_units);
                 }
                 ++prod_units;
             }
@@ -517,42 +547,52 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
         return;
     }
 
+    // Instruction descriptors.  bf16: kind::f16, 8 steps of K = 16.  FP8:
+    // kind::f8f6f4 on the E4M3 tiles as loaded, 4 steps of K = 32 for each of
+    // the hi and lo parts of Q (in S^T) and of P (in O^T); operand types
+    // E4M3 = 0.  NVFP4: kind::f16 with f16 operands (format 0), widened in
+    // shared memory.
+    constexpr uint32_t kE4M3 = (FP8 || F4) ? ~((7u << 7) | (7u << 10)) : ~0u;
+    constexpr uint32_t kIdescS = umma_idesc_bf16(128, 16, 0, 0) & kE4M3; // K and Q^T both K-major
+    constexpr uint32_t kIdescO = umma_idesc_bf16(128, 16, 1, 0) & kE4M3; // V^T MN-major, P^T K-major
+
     if (warp == 1) {
-        // =================== MMA issuer (lane 0) ===================
-        // S^T(l + 1) is issued before P^T(l) is awaited, so the tensor core
-        // works on the next page while the softmax warps work on this one.
-        // bf16: kind::f16, 8 steps of K = 16.  FP8: kind::f8f6f4 on the E4M3
-        // tiles as loaded, 4 steps of K = 32 for each of the hi and lo parts
-        // of Q (in S^T) and of P (in O^T); operand types E4M3 = 0.
-        // NVFP4: kind::f16 with f16 operands (format 0), widened in shared memory
-        constexpr uint32_t kE4M3 = (FP8 || F4) ? ~((7u << 7) | (7u << 10)) : ~0u;
-        constexpr uint32_t kIdescS = umma_idesc_bf16(128, 16, 0, 0) & kE4M3; // K and Q^T both K-major
-        constexpr uint32_t kIdescO = umma_idesc_bf16(128, 16, 1, 0) & kE4M3; // V^T MN-major, P^T K-major
+        // =================== S issuer (lane 0) + TMEM owner ===================
+        // S^T(l) into accumulator l % kUSBufs as soon as K(l) has landed and
+        // the softmax warps have read S^T(l - kUSBufs): the S MMAs run ahead
+        // of the softmax, independently of the P.V MMAs (their own thread).
         bool ok = true;
         if (lane == 0) {
             int s_units = 0, s_unit = -1;
-            auto issue_s = [&](int l) -> bool {
-                const int zk = 2 * l, b = l & 1;
-                // NVFP4: K(l) widened into staging tile b; else the ring tile landed
-                if (F4 ? !mbar_wait_or_abort(smem_u32(&kst_full[b]), (l >> 1) & 1, abort_flag, wl)
-                       : !mbar_wait_or_abort(smem_u32(&full[zk % STAGES]), (zk / STAGES) & 1, abort_flag, wl))
-                    return false;
+            for (int l = 0; l < ntasks; ++l) {
+                const int zk = 2 * l, sb = l % kUSBufs;
+                // NVFP4: K(l) widened into staging tile l & 1; else the ring tile landed
+                if (F4 ? !mbar_wait_or_abort(smem_u32(&kst_full[l & 1]), (l >> 1) & 1, abort_flag, wl)
+                       : !mbar_wait_or_abort(smem_u32(&full[zk % STAGES]), (zk / STAGES) & 1, abort_flag, wl)) {
+                    ok = false;
+                    break;
+                }
                 const int4 e = entry(l);
                 const int u = unit_of(e);
                 if (u != s_unit) {
                     // NVFP4: the converter warps widen the query tile to f16 in place
                     uint64_t *qready = F4 ? qconv : qfull;
-                    if (!mbar_wait_or_abort(smem_u32(&qready[s_units & 1]), (s_units >> 1) & 1, abort_flag, wl))
-                        return false;
+                    if (!mbar_wait_or_abort(smem_u32(&qready[s_units & 1]), (s_units >> 1) & 1, abort_flag, wl)) {
+                        ok = false;
+                        break;
+                    }
                     s_unit = u;
                     ++s_units;
                 }
                 const int qb = (s_units - 1) & 1;
-                if (l >= 2 && !mbar_wait_or_abort(smem_u32(&s_free[b]), ((l >> 1) - 1) & 1, abort_flag, wl))
-                    return false;
+                if (l >= kUSBufs &&
+                    !mbar_wait_or_abort(smem_u32(&s_free[sb]), ((l / kUSBufs) - 1) & 1, abort_flag, wl)) {
+                    ok = false;
+                    break;
+                }
                 tcgen05_after_sync();
                 if (e.x >= 0) {
-                    const uint32_t tileK = F4 ? smem_u32(kst + b * kUTile)
+                    const uint32_t tileK = F4 ? smem_u32(kst + (l & 1) * kUTile)
                                               : smem_u32(ring + (size_t)(zk % STAGES) * kRaw);
                     const uint32_t qtile = smem_u32(qbuf + qb * kUQTile);
 #pragma unroll
@@ -560,39 +600,68 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
                         if (!FP8) {
                             const uint64_t a = umma_desc_sw128(tileK + (ks >> 2) * (kUTile / 2) + (ks & 3) * 32, 16, 1024);
                             const uint64_t bq = umma_desc_sw128(qtile + (ks >> 2) * (kUQTile / 2) + (ks & 3) * 32, 16, 1024);
-                            umma_bf16(tmem + 16 * b, a, bq, kIdescS, ks > 0);
+                            umma_bf16(tmem + 16 * sb, a, bq, kIdescS, ks > 0);
                         } else { // steps 0..3: Q hi, 4..7: Q lo; 32 dims (bytes) per step
                             const uint64_t a = umma_desc_sw128(tileK + (ks & 3) * 32, 16, 1024);
                             const uint64_t bq = umma_desc_sw128(qtile + (ks >> 2) * (kUQTile / 2) + (ks & 3) * 32, 16, 1024);
-                            umma_f8(tmem + 16 * b, a, bq, kIdescS, ks > 0);
+                            umma_f8(tmem + 16 * sb, a, bq, kIdescS, ks > 0);
                         }
                     }
                 }
-                umma_commit(smem_u32(&s_full[b]));
-                umma_commit(F4 ? smem_u32(&kst_empty[b]) : smem_u32(&empty[zk % STAGES])); // K tile read
+                umma_commit(smem_u32(&s_full[sb]));
+                umma_commit(F4 ? smem_u32(&kst_empty[l & 1]) : smem_u32(&empty[zk % STAGES])); // K tile read
                 // last task of its unit: the query tile can be replaced
                 if (l + 1 == ntasks || unit_of(entry(l + 1)) != u)
                     umma_commit(smem_u32(&qempty[qb]));
-                return true;
-            };
-            auto issue_pv = [&](int l) -> bool {
+            }
+            if (!ok) {
+                set_error(p.err, kErrTimeout);
+                *abort_flag = 1;
+                // the MMAs issued so far finish before TMEM is freed
+                umma_commit(smem_u32(s_drain));
+                (void)mbar_wait_bounded(smem_u32(s_drain), 0);
+            }
+        }
+        __syncwarp();
+        // free TMEM once the softmax warps and the PV issuer are done with it
+        // (they always arrive, also after an abort; the waits are bounded)
+        if (lane == 0) {
+            (void)mbar_wait_bounded(smem_u32(done_bar), 0);
+            (void)mbar_wait_bounded(smem_u32(pv_done), 0);
+        }
+        __syncwarp();
+        tcgen05_after_sync();
+        tmem_dealloc(tmem, kUTmemCols);
+        return;
+    }
+
+    if (warp == kUWarpPV) {
+        // =================== P.V issuer (lane 0) ===================
+        // O^T(l) into accumulator l & 1 once V(l) has landed, the softmax
+        // warps have written P^T(l) and folded O^T(l - 2).
+        if (lane == 0) {
+            bool ok = true;
+            for (int l = 0; l < ntasks; ++l) {
                 const int zv = 2 * l + 1, b = l & 1;
                 if (F4 ? !mbar_wait_or_abort(smem_u32(&vst_full[b]), (l >> 1) & 1, abort_flag, wl)
-                       : !mbar_wait_or_abort(smem_u32(&full[zv % STAGES]), (zv / STAGES) & 1, abort_flag, wl))
-                    return false;
-                if (!mbar_wait_or_abort(smem_u32(&p_full[b]), (l >> 1) & 1, abort_flag, wl))
-                    return false;
-                if (l >= 2 && !mbar_wait_or_abort(smem_u32(&o_free[b]), ((l >> 1) - 1) & 1, abort_flag, wl))
-                    return false;
+                       : !mbar_wait_or_abort(smem_u32(&full[zv % STAGES]), (zv / STAGES) & 1, abort_flag, wl)) {
+                    ok = false;
+                    break;
+                }
+                if (!mbar_wait_or_abort(smem_u32(&p_full[b]), (l >> 1) & 1, abort_flag, wl) ||
+                    (l >= 2 && !mbar_wait_or_abort(smem_u32(&o_free[b]), ((l >> 1) - 1) & 1, abort_flag, wl))) {
+                    ok = false;
+                    break;
+                }
                 tcgen05_after_sync();
-                if (entry(l).x >= 0) {
+                const int4 e = entry(l);
+                if (e.x >= 0) {
                     const uint32_t tileV = F4 ? smem_u32(vst + b * kUTile)
                                               : smem_u32(ring + (size_t)(zv % STAGES) * kRaw);
                     const uint32_t ptile = smem_u32(pbuf + b * p_tile_bytes(KVF));
                     // bf16: steps 0..7 take P hi, 8..15 (single-page units) P lo,
                     // over the same V^T slices
-                    const int e_t = entry(l).z;
-                    const int pv_steps = (KVF == kKvBf16 && qt[e_t + 1] - qt[e_t] == 1) ? 16 : 8;
+                    const int pv_steps = (KVF == kKvBf16 && qt[e.z + 1] - qt[e.z] == 1) ? 16 : 8;
 #pragma unroll
                     for (int ks = 0; ks < 16; ++ks) {
                         if (ks >= pv_steps)
@@ -604,49 +673,32 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
                             const uint64_t a = umma_desc_sw128(tileV + kt * 2048, kUTile / 2, 1024);
                             const uint64_t bp = umma_desc_sw128(
                                 ptile + (ks >> 3) * kUPTile + (kt >> 2) * (kUPTile / 2) + (kt & 3) * 32, 16, 1024);
-                            umma_bf16(tmem + 32 + 16 * b, a, bp, kIdescO, ks > 0);
+                            umma_bf16(tmem + kUOCol + 16 * b, a, bp, kIdescO, ks > 0);
                         } else {
                             // V^T, MN-major: 32 tokens per k-step = 32 rows of 128 bytes
                             // (all 128 dims in one swizzle atom); steps 0..3: P hi, 4..7: P lo
                             const uint64_t a = umma_desc_sw128(tileV + (ks & 3) * 4096, kUTile / 2, 1024);
                             const uint64_t bp = umma_desc_sw128(ptile + (ks >> 2) * (kUPTile / 2) + (ks & 3) * 32, 16, 1024);
-                            umma_f8(tmem + 32 + 16 * b, a, bp, kIdescO, ks > 0);
+                            umma_f8(tmem + kUOCol + 16 * b, a, bp, kIdescO, ks > 0);
                         }
                     }
                 }
                 umma_commit(smem_u32(&o_full[b]));
                 umma_commit(smem_u32(&p_free[b]));
                 umma_commit(F4 ? smem_u32(&vst_empty[b]) : smem_u32(&empty[zv % STAGES])); // V tile read
-                return true;
-            };
-            if (ntasks > 0)
-                ok = issue_s(0);
-            for (int l = 0; l < ntasks && ok; ++l) {
-                if (l + 1 < ntasks)
-                    ok = issue_s(l + 1);
-                if (ok)
-                    ok = issue_pv(l);
             }
             if (!ok) {
                 set_error(p.err, kErrTimeout);
                 *abort_flag = 1;
-                // the MMAs issued so far finish before TMEM is freed
-                umma_commit(smem_u32(mma_drain));
-                (void)mbar_wait_bounded(smem_u32(mma_drain), 0);
+                umma_commit(smem_u32(pv_drain));
+                (void)mbar_wait_bounded(smem_u32(pv_drain), 0);
             }
+            mbar_arrive(smem_u32(pv_done));
         }
-        __syncwarp();
-        // free TMEM once the softmax warps are done with it (they always arrive,
-        // also after an abort; the wait is bounded)
-        if (lane == 0)
-            (void)mbar_wait_bounded(smem_u32(done_bar), 0);
-        __syncwarp();
-        tcgen05_after_sync();
-        tmem_dealloc(tmem, kUTmemCols);
         return;
     }
 
-    if (F4 && warp >= 2 + kUSmxWarps) {
+    if (F4 && warp >= kUWarpCvt) {
         // =================== converter warps (NVFP4) ===================
         // K and V tiles from the ring (e2m1 pairs [128 tok][64 B], then E4M3
         // scales [128 tok][8]) into the f16 staging tiles, in the
@@ -656,7 +708,7 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
         // The query tile of each new unit is widened from bf16 to f16 in
         // place.  The tensor scales are folded into the logit scale and the
         // output.
-        const int ct = threadIdx.x - 32 * (2 + kUSmxWarps); // 0..127
+        const int ct = threadIdx.x - 32 * kUWarpCvt; // 0..127
         bool ok = true;
         int units = 0, cur = -1;
         // Thread ct widens the 16 dimensions gch = ct % 8 of rows ct / 8 + 16 i,
@@ -788,7 +840,7 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
         tcgen05_after_sync();
         if (pending) {
             float v[kUHeads];
-            tmem_ld8(lane_base + 32 + 16 * b, v);
+            tmem_ld8(lane_base + kUOCol + 16 * b, v);
 #pragma unroll
             for (int h = 0; h < kUHeads; ++h)
                 o[h] = o[h] * alpha_prev[h] + v[h];
@@ -949,12 +1001,12 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
     // fetched once per CTA instead of once per copy.
     for (int l = 0; l <= ntasks && ok; ++l) {
         const bool end = l == ntasks;
-        const int b = l & 1;
+        const int b = l & 1, sb = l % kUSBufs;
         int4 e = make_int4(-1, 0, 0, 0);
         int u = -2; // no unit: ends the last one
         float sv[kUHeads];
         if (!end) {
-            if (!wait_all(smem_u32(&s_full[b]), (l >> 1) & 1)) {
+            if (!wait_all(smem_u32(&s_full[sb]), (l / kUSBufs) & 1)) {
                 ok = false;
                 break;
             }
@@ -962,11 +1014,11 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
             e = entry(l);
             u = unit_of(e);
             if (e.x >= 0)
-                tmem_ld8(lane_base + 16 * b, sv);
+                tmem_ld8(lane_base + 16 * sb, sv);
             tcgen05_before_sync();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(smem_u32(&s_free[b]));
+                mbar_arrive(smem_u32(&s_free[sb]));
         }
         const bool live = e.x >= 0;
 
