@@ -170,9 +170,10 @@ constexpr int kUCvtWarps = 4;              // NVFP4 only: e2m1 x E4M3 -> f16 con
 // KV formats of the kernel instances
 constexpr int kKvBf16 = 0, kKvFp8 = 1, kKvNvfp4 = 2;
 template <int KVF>
-constexpr int kUThreadsT = 32 * (3 + kUSmxWarps + (KVF == kKvNvfp4 ? kUCvtWarps : 0)); // producer, S MMA, softmax, PV MMA[, converters]
+constexpr int kUThreadsT = 32 * (4 + kUSmxWarps + (KVF == kKvNvfp4 ? kUCvtWarps : 0)); // producer, S MMA, softmax, PV MMA, publisher[, converters]
 constexpr int kUWarpPV = 2 + kUSmxWarps;   // the warp that issues the P.V MMAs
-constexpr int kUWarpCvt = 3 + kUSmxWarps;  // NVFP4: the first converter warp
+constexpr int kUWarpPub = 3 + kUSmxWarps;  // the warp that publishes the first unit's partial
+constexpr int kUWarpCvt = 4 + kUSmxWarps;  // NVFP4: the first converter warp
 constexpr int kF4Tile = kPage * kDim / 2 + kPage * kDim / 16; // NVFP4 K or V tile: codes then scales
 constexpr int kUQScales = 16;              // FP8: ring of per-unit query scales (> units in flight)
 constexpr float kPScale = 256.f;           // FP8: P^T is stored as 256 * P (E4M3 hi + lo)
@@ -184,13 +185,37 @@ constexpr int kUTile = 32768;              // bf16 K or V tile of one (page, KV 
 constexpr int kUQTile = 4096;              // 16 query rows of one unit: bf16 (two 64-dim boxes) or E4M3 hi + lo
 constexpr int kUPTile = 4096;              // P^T of one page, [16 heads][128 tokens], one part: bf16 / f16, or E4M3 hi + lo
 
-// Bytes of one page's P^T buffer: bf16 values have room for P as a bf16
-// hi + lo pair (two 4 KiB parts, 16 significant bits), used for the page of a
-// unit that has only that page (see the softmax section); E4M3 takes an E4M3
-// hi + lo pair of 256 P, NVFP4 one f16 part.
+// Bytes of one softmax pass's P^T buffer.  bf16 and E4M3 values: a pass
+// covers up to two pages of one unit, one 4 KiB part each (bf16 P; E4M3 hi +
+// lo pair of 256 P); a pass over the page of a unit that has only that page
+// uses the second part for the low half of P as a bf16 hi + lo pair (see the
+// softmax section).  NVFP4 values: one page per pass, one f16 part.
 __host__ __device__ constexpr int p_tile_bytes(int kvf)
 {
-    return kvf == kKvBf16 ? 2 * kUPTile : kUPTile;
+    return kvf == kKvNvfp4 ? kUPTile : 2 * kUPTile;
+}
+
+// Softmax passes: up to two consecutive pages of the same unit for E4M3
+// values (bound by the softmax: two pages share one max exchange, one P^T
+// hand-off and one O^T fold), one page for bf16 values (bound by the copies
+// in flight: a pass that waits for its second page keeps the first page's V
+// tile in the ring longer) and NVFP4 values (bound by the converter warps).
+__host__ __device__ constexpr int pass_pages(int kvf)
+{
+    return kvf == kKvFp8 ? 2 : 1;
+}
+
+// Order of the copies into the ring: K(0), V(0), K(1), V(1), ...; copy
+// number z takes ring stage z % STAGES.  (Issuing V(l) after K(l + 1), so
+// that it lands closer to its use, was measured slower.)
+__device__ __forceinline__ int copy_of_k(int l)
+{
+    return 2 * l;
+}
+
+__device__ __forceinline__ int copy_of_v(int l, int)
+{
+    return 2 * l + 1;
 }
 
 struct USmem {
@@ -219,9 +244,9 @@ __host__ __device__ inline USmem umma_layout(int T, int stages, int kvf)
     // full[S], empty[S], qfull[2], qempty[2], s_full[4], s_free[4], p_full[2],
     // p_free[2], o_full[2], o_free[2], softmax sync, done, then NVFP4 only:
     // kst_full[2], kst_empty[2], vst_full[2], vst_empty[2], qconv[2]; S and
-    // PV drains, PV issuer done
+    // PV drains, PV issuer done, first unit's slot written, last unit checked
     L.bars = off = align_to(off, 8);
-    off += (size_t)(2 * stages + 12 + 2 * kUSBufs + 2 + 10 + 3) * 8;
+    off += (size_t)(2 * stages + 12 + 2 * kUSBufs + 2 + 10 + 5) * 8;
     L.table = off = align_to(off, 16);     // [2][kWin] int4
     off += (size_t)2 * kWin * 16;
     L.xbuf = off = align_to(off, 16);      // [2][4 quarters][16] page maxima
@@ -230,8 +255,8 @@ __host__ __device__ inline USmem umma_layout(int T, int stages, int kvf)
     off += 4 * 16 * 4;
     L.qsc = off = align_to(off, 16);       // FP8: [kUQScales] 1 / query scale of a unit
     off += kUQScales * 4;
-    L.misc = off = align_to(off, 16);      // tmem base, flags
-    off += 16;
+    L.misc = off = align_to(off, 16);      // tmem base, flags, the last unit's merge check
+    off += 32;
     L.qt = off = align_to(off, 16);        // [T + 1]
     off += (size_t)(T + 1) * 4;
     L.total = align_to(off, 16) + 1024;
@@ -250,6 +275,21 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8])
 #pragma unroll
     for (int i = 0; i < 8; ++i)
         v[i] = __uint_as_float(r[i]);
+}
+
+// 8 consecutive 32-bit TMEM columns of this thread's lane (warp-wide), without
+// waiting: the registers are valid after tmem_wait_ld().
+__device__ __forceinline__ void tmem_ld8_nowait(uint32_t taddr, uint32_t (&r)[8])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld()
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
 // Two floats to E4M3 (round to nearest, saturating): a -> high byte, b -> low byte.
@@ -271,6 +311,29 @@ __device__ __forceinline__ void split_e4m3x2(float x0, float x1, uint32_t &hi, u
     float h0, h1;
     f16x2_to_f32x2(e4m3x2_to_f16x2(hi), h0, h1);
     lo = f32x2_to_e4m3x2(x1 - h1, x0 - h0);
+}
+
+// One step of the fixed-order merge of split partials: the weights that
+// rescale the running (M, L, acc) and the incoming slot to their joint
+// maximum.  Every merge (softmax warps, publisher) goes through these, with
+// explicit roundings, so that any CTA produces the same bits.
+struct MergeW {
+    float a_old, a_s, m;
+};
+
+__device__ __forceinline__ MergeW merge_weights(float M, float ms)
+{
+    MergeW w;
+    w.m = fmaxf(M, ms);
+    const float ref = (w.m == -INFINITY) ? 0.f : w.m;
+    w.a_old = ex2(M - ref); // 0 for -inf
+    w.a_s = ex2(ms - ref);
+    return w;
+}
+
+__device__ __forceinline__ float merge_acc(float acc, float x, const MergeW &w)
+{
+    return __fmaf_rn(acc, w.a_old, __fmul_rn(x, w.a_s));
 }
 
 template <int KVF, int STAGES>
@@ -310,12 +373,17 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
     uint64_t *s_drain = qconv + 2;      // the S MMAs issued before a timeout have completed (commit)
     uint64_t *pv_drain = s_drain + 1;   // the same for the PV MMAs
     uint64_t *pv_done = pv_drain + 1;   // the PV issuer has finished (1 arrival)
+    uint64_t *pub_full = pv_done + 1;   // the first unit's partial is in its slot (kUSmxWarps)
+    uint64_t *last_bar = pub_full + 1;  // the producer has checked the last unit's other part (1)
     float *qscale = reinterpret_cast<float *>(base + lay.qsc);
     int4 *table = reinterpret_cast<int4 *>(base + lay.table);
     float *xbuf = reinterpret_cast<float *>(base + lay.xbuf);
     float *lbuf = reinterpret_cast<float *>(base + lay.lbuf);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + lay.misc);
     int *s_flag = reinterpret_cast<int *>(base + lay.misc) + 1; // [0] last arrival, [1] abort
+    // [0] the last unit's other part is published, [1] the CTA that holds it
+    volatile int *last_chk = reinterpret_cast<int *>(base + lay.misc) + 4;
+    volatile int *smx_done = reinterpret_cast<int *>(base + lay.misc) + 6; // the softmax warps have finished
     int *qt = reinterpret_cast<int *>(base + lay.qt);
     volatile int *abort_flag = s_flag + 1;
     const long long wl = p.wait_limit; // clocks of every wait below but the final drains
@@ -360,8 +428,11 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
         mbar_init(smem_u32(s_drain), 1);
         mbar_init(smem_u32(pv_drain), 1);
         mbar_init(smem_u32(pv_done), 1);
+        mbar_init(smem_u32(pub_full), kUSmxWarps);
+        mbar_init(smem_u32(last_bar), 1);
         s_flag[0] = 0;
         s_flag[1] = 0;
+        *smx_done = 0;
         fence_mbar_init();
     }
     if (warp == 1)
@@ -377,6 +448,28 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
     const long long x_begin = (uint32_t)c * (uint32_t)P / (uint32_t)G; // 32-bit: see owner_of
     const long long x_end = (uint32_t)(c + 1) * (uint32_t)P / (uint32_t)G;
     const int ntasks = (int)(x_end - x_begin);
+
+    // Unit (t, g): its tasks [first, end) in the order all CTAs cut, and the
+    // CTAs whose ranges hold them.
+    struct UnitOwn {
+        long long first, end;
+        int u, c_first, c_last;
+    };
+    auto own_of = [&](int t, int g) {
+        UnitOwn w;
+        w.first = (long long)g * qt[p.T] + qt[t];
+        w.end = w.first + (qt[t + 1] - qt[t]);
+        w.c_first = owner_of(w.first, P, G);
+        w.c_last = owner_of(w.end - 1, P, G);
+        w.u = g * p.T + t;
+        return w;
+    };
+    auto arrivals_of = [&](const UnitOwn &w) { // CTAs with tasks of the unit
+        int a = 0;
+        for (int cc = w.c_first; cc <= w.c_last; ++cc)
+            a += !range_empty(cc, P, G);
+        return a;
+    };
 
     // The query rows of unit number unit_no of this CTA (16 rows from `row`)
     // into query buffer qb; called by the whole producer warp.  bf16 and
@@ -472,57 +565,54 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
         const uint64_t kv_policy = l2_evict_first_policy(); // pages are streamed
         int issued = 0, prod_units = 0, prod_last = -1;
         bool ok = true;
-        for (int l = 0; l < ntasks && ok; ++l) {
-            const int zk = 2 * l;
-            if (lane == 0 && zk >= STAGES)
-                ok = mbar_wait_or_abort(smem_u32(&empty[zk % STAGES]), ((zk / STAGES) - 1) & 1,
+        for (int z = 0; z < 2 * ntasks && ok; ++z) {
+            // copy z: K(l) or V(l) (the order of copy_of_k / copy_of_v)
+            const bool is_k = (z & 1) == 0;
+            const int l = z >> 1;
+            if (lane == 0 && z >= STAGES)
+                ok = mbar_wait_or_abort(smem_u32(&empty[z % STAGES]), ((z / STAGES) - 1) & 1,
                                         abort_flag, wl);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok)
                 break;
-            // The slowest reader of the table is the P.V issuer: issuing V(l)
-            // needs the stage of V(l - kAhead), which its P.V MMAs free, so
-            // that reader trails this warp by at most kAhead tasks (kAhead + 2
-            // with the NVFP4 converters and their two staging tiles between
-            // them); the softmax warps, the S issuer and the converters are
-            // ahead of it.  Only kAhead + 3 (+ 2) tasks into a window has
-            // every reader left the window before it.
-            if (l % kWin == kAhead + 3 + (F4 ? 2 : 0) && l >= kWin && (l / kWin + 1) * kWin < ntasks)
-                fill_window(l / kWin + 1);
             const int4 e = entry(l);
-            const int u = unit_of(e);
-            if (u != prod_last) {
-                // the unit's 16 query rows into query buffer qb (the first
-                // unit's were staged before the grid wait)
-                prod_last = u;
-                const int qb = prod_units & 1;
-                if (prod_units > 0) {
-                    if (lane == 0 && prod_units >= 2)
-                        ok = mbar_wait_or_abort(smem_u32(&qempty[qb]), ((prod_units >> 1) - 1) & 1, abort_flag, wl);
-                    ok = __shfl_sync(0xffffffffu, ok, 0);
-                    if (!ok)
-                        break;
-                    load_q(qb, (e.z * p.Hkv + e.w) * kGroup, prod_units);
+            if (is_k) {
+                // The slowest reader of the table is the P.V issuer: copy
+                // K(l) comes after V(l - 1), which took the stage of
+                // V(l - 1 - kAhead) once its P.V MMAs had freed it, so that
+                // reader trails this warp by at most kAhead tasks (+ 2 with
+                // the NVFP4 converters and their two staging tiles between
+                // them); the softmax warps, the S issuer and the converters
+                // are ahead of it.  Only kAhead + 3 (+ 2) tasks into a window
+                // has every reader left the window before it.
+                if (l % kWin == kAhead + 3 + (F4 ? 2 : 0) && l >= kWin && (l / kWin + 1) * kWin < ntasks)
+                    fill_window(l / kWin + 1);
+                const int u = unit_of(e);
+                if (u != prod_last) {
+                    // the unit's 16 query rows into query buffer qb (the first
+                    // unit's were staged before the grid wait)
+                    prod_last = u;
+                    const int qb = prod_units & 1;
+                    if (prod_units > 0) {
+                        if (lane == 0 && prod_units >= 2)
+                            ok = mbar_wait_or_abort(smem_u32(&qempty[qb]), ((prod_units >> 1) - 1) & 1, abort_flag, wl);
+                        ok = __shfl_sync(0xffffffffu, ok, 0);
+                        if (!ok)
+                            break;
+                        load_q(qb, (e.z * p.Hkv + e.w) * kGroup, prod_units);
+                    }
+                    ++prod_units;
                 }
-                ++prod_units;
             }
             if (lane == 0) {
-                for (int kv = 0; kv < 2 && ok; ++kv) {
-                    const int z = zk + kv;
-                    const int st = z % STAGES;
-                    if (kv == 1 && z >= STAGES)
-                        ok = mbar_wait_or_abort(smem_u32(&empty[st]), ((z / STAGES) - 1) & 1,
-                                                abort_flag, wl);
-                    if (!ok)
-                        break;
-                    const uint32_t bar = smem_u32(&full[st]);
-                    issued = z + 1;
-                    if (e.x < 0) {
-                        mbar_arrive(bar); // no data: consumers skip the task
-                        continue;
-                    }
+                const int st = z % STAGES;
+                const uint32_t bar = smem_u32(&full[st]);
+                issued = z + 1;
+                if (e.x < 0) {
+                    mbar_arrive(bar); // no data: consumers skip the task
+                } else {
                     const uint32_t dst = smem_u32(ring + (size_t)st * kRaw);
-                    const int krow = e.x + kv * p.Hkv * kPage;
+                    const int krow = e.x + (is_k ? 0 : p.Hkv * kPage);
                     mbar_arrive_expect_tx(bar, kRaw);
                     if (F4) { // one contiguous tile: codes then scales
                         bulk_load_hint(dst, p.kv_raw + (size_t)(krow / kPage) * kF4Tile, kF4Tile, bar,
@@ -534,7 +624,28 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
                     }
                 }
             }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
+        }
+        // The CTA's last unit, begun here and continued by later CTAs, which
+        // publish their parts at their starts: with every copy issued, one
+        // acquire load tells whether the one other part is in, so that the
+        // softmax warps can read it during their last pass and merge at once.
+        if (ok && ntasks > 0 && lane == 0) {
+            const int4 el = entry(ntasks - 1);
+            const UnitOwn w = own_of(el.z, el.w);
+            if (w.c_first == c && w.c_last > c) {
+                int other = -1, n_other = 0;
+                for (int cc = c + 1; cc <= w.c_last; ++cc)
+                    if (!range_empty(cc, P, G)) {
+                        other = cc;
+                        ++n_other;
+                    }
+                int in = 0;
+                if (n_other == 1 && (long long)w.c_last + w.u < p.slots)
+                    in = ld_acquire_gpu(&p.counters[w.u]) == 1;
+                last_chk[0] = in;
+                last_chk[1] = other;
+                mbar_arrive(smem_u32(last_bar));
+            }
         }
         if (!ok && lane == 0) {
             set_error(p.err, kErrTimeout);
@@ -565,7 +676,7 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
         if (lane == 0) {
             int s_units = 0, s_unit = -1;
             for (int l = 0; l < ntasks; ++l) {
-                const int zk = 2 * l, sb = l % kUSBufs;
+                const int zk = copy_of_k(l), sb = l % kUSBufs;
                 // NVFP4: K(l) widened into staging tile l & 1; else the ring tile landed
                 if (F4 ? !mbar_wait_or_abort(smem_u32(&kst_full[l & 1]), (l >> 1) & 1, abort_flag, wl)
                        : !mbar_wait_or_abort(smem_u32(&full[zk % STAGES]), (zk / STAGES) & 1, abort_flag, wl)) {
@@ -635,57 +746,76 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
         return;
     }
 
+    // Pages per softmax pass: a pass takes the next two tasks if they belong
+    // to one unit (bf16 / E4M3 values), else one.  The softmax warps and the
+    // P.V issuer walk the same passes.
+    auto pass_len = [&](int l0) -> int {
+        if (pass_pages(KVF) == 1 || l0 + 1 >= ntasks)
+            return 1;
+        return unit_of(entry(l0 + 1)) == unit_of(entry(l0)) ? 2 : 1;
+    };
+
     if (warp == kUWarpPV) {
         // =================== P.V issuer (lane 0) ===================
-        // O^T(l) into accumulator l & 1 once V(l) has landed, the softmax
-        // warps have written P^T(l) and folded O^T(l - 2).
+        // O^T of pass j into accumulator j & 1 once the softmax warps have
+        // written P^T of the pass and folded O^T of pass j - 2, each page as
+        // soon as its V tile has landed; the pages of a pass share the pass's
+        // softmax reference and accumulate into one O^T.
         if (lane == 0) {
             bool ok = true;
-            for (int l = 0; l < ntasks; ++l) {
-                const int zv = 2 * l + 1, b = l & 1;
-                if (F4 ? !mbar_wait_or_abort(smem_u32(&vst_full[b]), (l >> 1) & 1, abort_flag, wl)
-                       : !mbar_wait_or_abort(smem_u32(&full[zv % STAGES]), (zv / STAGES) & 1, abort_flag, wl)) {
+            int j = 0;
+            for (int l0 = 0; l0 < ntasks && ok; l0 += pass_len(l0), ++j) {
+                const int np = pass_len(l0), pb = j & 1;
+                if (!mbar_wait_or_abort(smem_u32(&p_full[pb]), (j >> 1) & 1, abort_flag, wl) ||
+                    (j >= 2 && !mbar_wait_or_abort(smem_u32(&o_free[pb]), ((j >> 1) - 1) & 1, abort_flag, wl))) {
                     ok = false;
                     break;
                 }
-                if (!mbar_wait_or_abort(smem_u32(&p_full[b]), (l >> 1) & 1, abort_flag, wl) ||
-                    (l >= 2 && !mbar_wait_or_abort(smem_u32(&o_free[b]), ((l >> 1) - 1) & 1, abort_flag, wl))) {
-                    ok = false;
-                    break;
-                }
-                tcgen05_after_sync();
-                const int4 e = entry(l);
-                if (e.x >= 0) {
-                    const uint32_t tileV = F4 ? smem_u32(vst + b * kUTile)
-                                              : smem_u32(ring + (size_t)(zv % STAGES) * kRaw);
-                    const uint32_t ptile = smem_u32(pbuf + b * p_tile_bytes(KVF));
-                    // bf16: steps 0..7 take P hi, 8..15 (single-page units) P lo,
-                    // over the same V^T slices
-                    const int pv_steps = (KVF == kKvBf16 && qt[e.z + 1] - qt[e.z] == 1) ? 16 : 8;
-#pragma unroll
-                    for (int ks = 0; ks < 16; ++ks) {
-                        if (ks >= pv_steps)
-                            break;
-                        if (!FP8) {
-                            // V^T, MN-major: 16 tokens per k-step = 16 rows of 128 bytes;
-                            // the two 64-dim halves of a row are 16 KiB apart (LBO)
-                            const int kt = ks & 7;
-                            const uint64_t a = umma_desc_sw128(tileV + kt * 2048, kUTile / 2, 1024);
-                            const uint64_t bp = umma_desc_sw128(
-                                ptile + (ks >> 3) * kUPTile + (kt >> 2) * (kUPTile / 2) + (kt & 3) * 32, 16, 1024);
-                            umma_bf16(tmem + kUOCol + 16 * b, a, bp, kIdescO, ks > 0);
-                        } else {
-                            // V^T, MN-major: 32 tokens per k-step = 32 rows of 128 bytes
-                            // (all 128 dims in one swizzle atom); steps 0..3: P hi, 4..7: P lo
-                            const uint64_t a = umma_desc_sw128(tileV + (ks & 3) * 4096, kUTile / 2, 1024);
-                            const uint64_t bp = umma_desc_sw128(ptile + (ks >> 2) * (kUPTile / 2) + (ks & 3) * 32, 16, 1024);
-                            umma_f8(tmem + kUOCol + 16 * b, a, bp, kIdescO, ks > 0);
-                        }
+                bool acc = false; // a page of the pass has written the accumulator
+                for (int i = 0; i < np; ++i) {
+                    const int l = l0 + i, zv = copy_of_v(l, ntasks);
+                    if (F4 ? !mbar_wait_or_abort(smem_u32(&vst_full[l & 1]), (l >> 1) & 1, abort_flag, wl)
+                           : !mbar_wait_or_abort(smem_u32(&full[zv % STAGES]), (zv / STAGES) & 1, abort_flag, wl)) {
+                        ok = false;
+                        break;
                     }
+                    tcgen05_after_sync();
+                    const int4 e = entry(l);
+                    if (e.x >= 0) {
+                        const uint32_t tileV = F4 ? smem_u32(vst + (l & 1) * kUTile)
+                                                  : smem_u32(ring + (size_t)(zv % STAGES) * kRaw);
+                        const uint32_t ptile = smem_u32(pbuf + pb * p_tile_bytes(KVF) + i * kUPTile);
+                        // bf16: steps 0..7 take P hi, 8..15 (single-page units) P lo,
+                        // over the same V^T slices
+                        const int pv_steps = (KVF == kKvBf16 && qt[e.z + 1] - qt[e.z] == 1) ? 16 : 8;
+#pragma unroll
+                        for (int ks = 0; ks < 16; ++ks) {
+                            if (ks >= pv_steps)
+                                break;
+                            if (!FP8) {
+                                // V^T, MN-major: 16 tokens per k-step = 16 rows of 128 bytes;
+                                // the two 64-dim halves of a row are 16 KiB apart (LBO)
+                                const int kt = ks & 7;
+                                const uint64_t a = umma_desc_sw128(tileV + kt * 2048, kUTile / 2, 1024);
+                                const uint64_t bp = umma_desc_sw128(
+                                    ptile + (ks >> 3) * kUPTile + (kt >> 2) * (kUPTile / 2) + (kt & 3) * 32, 16, 1024);
+                                umma_bf16(tmem + kUOCol + 16 * pb, a, bp, kIdescO, acc || ks > 0);
+                            } else {
+                                // V^T, MN-major: 32 tokens per k-step = 32 rows of 128 bytes
+                                // (all 128 dims in one swizzle atom); steps 0..3: P hi, 4..7: P lo
+                                const uint64_t a = umma_desc_sw128(tileV + (ks & 3) * 4096, kUTile / 2, 1024);
+                                const uint64_t bp = umma_desc_sw128(ptile + (ks >> 2) * (kUPTile / 2) + (ks & 3) * 32, 16, 1024);
+                                umma_f8(tmem + kUOCol + 16 * pb, a, bp, kIdescO, acc || ks > 0);
+                            }
+                        }
+                        acc = true;
+                    }
+                    umma_commit(F4 ? smem_u32(&vst_empty[l & 1]) : smem_u32(&empty[zv % STAGES])); // V tile read
                 }
-                umma_commit(smem_u32(&o_full[b]));
-                umma_commit(smem_u32(&p_free[b]));
-                umma_commit(F4 ? smem_u32(&vst_empty[b]) : smem_u32(&empty[zv % STAGES])); // V tile read
+                if (!ok)
+                    break;
+                umma_commit(smem_u32(&o_full[pb]));
+                umma_commit(smem_u32(&p_free[pb]));
             }
             if (!ok) {
                 set_error(p.err, kErrTimeout);
@@ -695,6 +825,89 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
             }
             mbar_arrive(smem_u32(pv_done));
         }
+        return;
+    }
+
+    if (warp == kUWarpPub) {
+        // =================== publisher ===================
+        // The CTA's first unit, begun by an earlier CTA, when more units
+        // follow it here: the softmax warps put its partial in this CTA's
+        // slot and go on; this warp counts the arrival (an acquire-release
+        // atomic, a round trip to L2 the softmax warps would otherwise wait
+        // for).  The arrival that completes the unit merges it: here only
+        // when the earlier CTA finished first, which a CTA that was not yet
+        // resident can see.
+        if (ntasks == 0)
+            return;
+        const int4 e0 = table[0];
+        const UnitOwn w = own_of(e0.z, e0.w);
+        if (w.c_first == w.c_last || w.end >= x_end || (long long)w.c_last + w.u >= p.slots)
+            return; // whole, or also the last unit here (the softmax warps finish it)
+        // The softmax warps hand the partial over, or finish without doing
+        // so (after an abort); the wait ends on either and is bounded.
+        bool handed = mbar_try_wait(smem_u32(pub_full), 0);
+        if (!handed) {
+            const long long start = clock64();
+            while (!(handed = mbar_try_wait(smem_u32(pub_full), 0))) {
+                if (*abort_flag || clock64() - start > wl)
+                    break;
+                if (*smx_done) {
+                    // every softmax warp passes a barrier of all of them after
+                    // its hand-off, before any of them finishes: look once more
+                    __threadfence_block();
+                    handed = mbar_try_wait(smem_u32(pub_full), 0);
+                    break;
+                }
+            }
+        }
+        if (!__all_sync(0xffffffffu, handed))
+            return; // nothing is published
+        int last = 0;
+        if (lane == 0)
+            last = atom_add_acq_rel_gpu(&p.counters[w.u], 1) == arrivals_of(w) - 1;
+        if (!__shfl_sync(0xffffffffu, last, 0))
+            return;
+        // Merge every slot of the unit in slot (CTA) order: lane = dimensions
+        // 4 lane .. 4 lane + 3 of all 16 heads, with a running maximum.
+        float Mx[kGroup], Lx[kGroup], acc[kGroup][4];
+#pragma unroll
+        for (int h = 0; h < kGroup; ++h) {
+            Mx[h] = -INFINITY;
+            Lx[h] = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                acc[h][i] = 0.f;
+        }
+        for (int cc = w.c_first; cc <= w.c_last; ++cc) {
+            if (range_empty(cc, P, G))
+                continue;
+            const float *sl = p.partial + (size_t)(cc + w.u) * kPartialFloats;
+#pragma unroll
+            for (int h = 0; h < kGroup; ++h) {
+                const float ms = __ldcg(sl + kGroup * kDim + h), ls = __ldcg(sl + kGroup * kDim + kGroup + h);
+                const float4 os = __ldcg(reinterpret_cast<const float4 *>(sl + h * kDim) + lane);
+                const MergeW mw = merge_weights(Mx[h], ms);
+                Lx[h] = merge_acc(Lx[h], ls, mw);
+                acc[h][0] = merge_acc(acc[h][0], os.x, mw);
+                acc[h][1] = merge_acc(acc[h][1], os.y, mw);
+                acc[h][2] = merge_acc(acc[h][2], os.z, mw);
+                acc[h][3] = merge_acc(acc[h][3], os.w, mw);
+                Mx[h] = mw.m;
+            }
+        }
+        const size_t hb = (size_t)e0.z * p.Hkv * kGroup + (size_t)e0.w * kGroup;
+#pragma unroll
+        for (int h = 0; h < kGroup; ++h) {
+            const float inv = Lx[h] > 0.f ? 1.f / Lx[h] : 0.f;
+            uint2 ov;
+            ov.x = pack_bf16(acc[h][0] * inv, acc[h][1] * inv);
+            ov.y = pack_bf16(acc[h][2] * inv, acc[h][3] * inv);
+            *reinterpret_cast<uint2 *>(p.out + (hb + h) * kDim + 4 * lane) = ov;
+            if (lane == h)
+                p.lse[hb + h] = (Mx[h] == -INFINITY) ? -INFINITY : (Mx[h] + log2f(Lx[h])) * 0.69314718055994531f;
+        }
+        if (lane == 0)
+            p.counters[w.u] = 0; // ready for the next call
         return;
     }
 
@@ -741,7 +954,7 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
         // K(l + 1) is widened before V(l): the MMA warp issues S(l + 1)
         // before O(l).
         auto do_kv = [&](int l, int kv) -> bool {
-            const int z = 2 * l + kv, b = l & 1;
+            const int z = kv ? copy_of_v(l, ntasks) : copy_of_k(l), b = l & 1;
             uint64_t *st_full = kv ? vst_full : kst_full, *st_empty = kv ? vst_empty : kst_empty;
             if (!wait_all(smem_u32(&full[z % STAGES]), (z / STAGES) & 1))
                 return false;
@@ -819,6 +1032,7 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
     float o[kUHeads], lsum[kUHeads], m_run[kUHeads], alpha_prev[kUHeads];
     bool pending = false; // a page's O^T waits to be folded in
     int cur_unit = -1, cur_t = 0, cur_g = 0;
+    bool cur_cand = false; // the unit begins in this CTA and continues in later ones
 
     auto reset = [&]() {
 #pragma unroll
@@ -830,10 +1044,10 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
         }
     };
 
-    // fold the previous page's O^T (thread = dimension) into o[]
-    auto fold = [&](int l_prev) {
-        const int b = l_prev & 1;
-        if (!wait_all(smem_u32(&o_full[b]), (l_prev >> 1) & 1)) {
+    // fold the previous pass's O^T (thread = dimension) into o[]
+    auto fold = [&](int j_prev) {
+        const int b = j_prev & 1;
+        if (!wait_all(smem_u32(&o_full[b]), (j_prev >> 1) & 1)) {
             ok = false;
             return;
         }
@@ -852,7 +1066,12 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
         pending = false;
     };
 
-    // final: the CTA's last unit (the usual place for it to arrive last)
+    // The other CTA's partial of the last unit, read during the last pass
+    // when the producer found it published (pre).
+    bool pre = false;
+    float ms2[kUHeads], ls2[kUHeads], os2[kUHeads];
+
+    // final: the CTA's last unit
     auto finalize = [&](int t, int g, bool final) {
         // denominators: reduce lsum over the 128 token lanes
 #pragma unroll
@@ -870,13 +1089,9 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
         for (int h = 0; h < kUHeads; ++h)
             L[h] = lbuf[h0 + h] + lbuf[16 + h0 + h] + lbuf[32 + h0 + h] + lbuf[48 + h0 + h];
         ssync(); // lbuf is reused by the next unit
-        const long long Pt = qt[p.T];
-        const long long u_first = (long long)g * Pt + qt[t];
-        const int n_u = qt[t + 1] - qt[t];
-        const int c_first = owner_of(u_first, P, G);
-        const int c_last = owner_of(u_first + n_u - 1, P, G);
-        const int u = g * p.T + t;
-        const bool whole = c_first == c_last;
+        const UnitOwn w = own_of(t, g);
+        const int u = w.u;
+        const bool whole = w.c_first == w.c_last;
         const size_t hbase = (size_t)t * p.Hkv * kGroup + (size_t)g * kGroup + h0;
         float *slot = p.partial + (size_t)(c + u) * kPartialFloats;
         float Mi = -INFINITY, Li = 0.f; // head h0 + idx (idx < kUHeads)
@@ -899,27 +1114,15 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
                 p.lse[hbase + idx] = (Mi == -INFINITY) ? -INFINITY : (Mi + log2f(Li)) * 0.69314718055994531f;
             return;
         }
-        if ((long long)c_last + u >= p.slots) { // the caller's scratch is short: no slot is touched
+        if ((long long)w.c_last + u >= p.slots) { // the caller's scratch is short: no slot is touched
             if (sidx == 0)
                 set_error(p.err, kErrScratch);
             return;
         }
-        int arrivals = 0; // CTAs with tasks of this unit
-        for (int cc = c_first; cc <= c_last; ++cc)
-            arrivals += !range_empty(cc, P, G);
-        // Fast path for the CTA's last unit: when every other CTA of the unit
-        // is already in (the usual case there), this one merges at once from
-        // its registers and their slots, without publishing its own.  A unit
-        // at the start of the range is usually first in and skips the check.
-        bool last = false;
-        if (final) {
-            if (sidx == 0)
-                s_flag[0] = ld_acquire_gpu(&p.counters[u]) == arrivals - 1;
-            ssync();
-            last = s_flag[0] != 0;
-            ssync(); // s_flag is read by every thread before it is rewritten
-        }
-        if (!last) {
+        if (!final) {
+            // The CTA's first unit, begun by an earlier CTA, with more units
+            // here: its partial goes to this CTA's slot, and the publisher
+            // warp counts the arrival (and merges if it completes the unit).
 #pragma unroll
             for (int h = 0; h < kUHeads; ++h)
                 slot[(h0 + h) * kDim + idx] = o[h];
@@ -927,22 +1130,50 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
                 slot[kGroup * kDim + h0 + idx] = Mi;
                 slot[kGroup * kDim + kGroup + h0 + idx] = Li;
             }
-            // The CTA barrier orders every thread's slot writes before thread
-            // 0's release; its acquire makes the other CTAs' slots visible to
-            // the CTA that arrives last, and the barrier after it to all its
-            // threads.
-            ssync();
+            // __syncwarp orders the warp's slot writes before lane 0's
+            // release arrival; the publisher's acquire wait and its
+            // acquire-release atomic carry them to the CTA that merges.
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_u32(pub_full));
+            return;
+        }
+        bool last = pre; // pre: the one other part is in and already read
+        if (!pre) {
+            // The CTA's last unit otherwise: when every other CTA of the unit
+            // is already in, merge at once from registers and their slots,
+            // else publish and count the arrival; the arrival that completes
+            // the unit merges it.
+            const int arrivals = arrivals_of(w);
             if (sidx == 0)
-                s_flag[0] = atom_add_acq_rel_gpu(&p.counters[u], 1) == arrivals - 1;
+                s_flag[0] = ld_acquire_gpu(&p.counters[u]) == arrivals - 1;
             ssync();
             last = s_flag[0] != 0;
+            ssync(); // s_flag is read by every thread before it is rewritten
+            if (!last) {
+#pragma unroll
+                for (int h = 0; h < kUHeads; ++h)
+                    slot[(h0 + h) * kDim + idx] = o[h];
+                if (idx < kUHeads) {
+                    slot[kGroup * kDim + h0 + idx] = Mi;
+                    slot[kGroup * kDim + kGroup + h0 + idx] = Li;
+                }
+                // The CTA barrier orders every thread's slot writes before
+                // thread 0's release; its acquire makes the other CTAs' slots
+                // visible to the CTA that arrives last, and the barrier after
+                // it to all its threads.
+                ssync();
+                if (sidx == 0)
+                    s_flag[0] = atom_add_acq_rel_gpu(&p.counters[u], 1) == arrivals - 1;
+                ssync();
+                last = s_flag[0] != 0;
+            }
         }
         if (last) {
             // Combine the unit's slots in slot (CTA) order, this CTA's own
-            // part from registers (thread = dimension idx for 8 heads), with a
-            // running maximum.  All loads of a slot are issued before any
-            // arithmetic and the stores come after the last slot, so each
-            // slot costs one round trip to L2.
+            // part from registers (thread = dimension idx for 8 heads), the
+            // pre-read one from registers, the others from L2; all loads of a
+            // slot are issued before its arithmetic.
             float Mx[kUHeads], Lx[kUHeads], acc[kUHeads];
 #pragma unroll
             for (int h = 0; h < kUHeads; ++h) {
@@ -950,7 +1181,7 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
                 Lx[h] = 0.f;
                 acc[h] = 0.f;
             }
-            for (int cc = c_first; cc <= c_last; ++cc) {
+            for (int cc = w.c_first; cc <= w.c_last; ++cc) {
                 if (range_empty(cc, P, G))
                     continue;
                 float ms[kUHeads], ls[kUHeads], os[kUHeads];
@@ -960,6 +1191,13 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
                         ms[h] = m_run[h];
                         ls[h] = L[h];
                         os[h] = o[h];
+                    }
+                } else if (pre) {
+#pragma unroll
+                    for (int h = 0; h < kUHeads; ++h) {
+                        ms[h] = ms2[h];
+                        ls[h] = ls2[h];
+                        os[h] = os2[h];
                     }
                 } else {
                     const float *sl = p.partial + (size_t)(cc + u) * kPartialFloats;
@@ -972,12 +1210,10 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
                 }
 #pragma unroll
                 for (int h = 0; h < kUHeads; ++h) {
-                    const float m_new = fmaxf(Mx[h], ms[h]);
-                    const float ref = (m_new == -INFINITY) ? 0.f : m_new;
-                    const float a_old = ex2(Mx[h] - ref), a_s = ex2(ms[h] - ref); // 0 for -inf
-                    Lx[h] = Lx[h] * a_old + ls[h] * a_s;
-                    acc[h] = acc[h] * a_old + os[h] * a_s;
-                    Mx[h] = m_new;
+                    const MergeW mw = merge_weights(Mx[h], ms[h]);
+                    Lx[h] = merge_acc(Lx[h], ls[h], mw);
+                    acc[h] = merge_acc(acc[h], os[h], mw);
+                    Mx[h] = mw.m;
                 }
             }
 #pragma unroll
@@ -991,113 +1227,21 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
             if (sidx == 0)
                 p.counters[u] = 0; // ready for the next call
         }
-        ssync(); // s_flag is reused by the next unit
     };
 
-    int l_last = -1, sm_units = 0;
-    float unit_scale = p.scale_log2; // logits to base 2 (FP8: / the unit's query scale)
-    // One pass past the last task (l == ntasks) finishes the last unit, so
-    // that finalize has one call site: its code, run once per unit, is
-    // fetched once per CTA instead of once per copy.
-    for (int l = 0; l <= ntasks && ok; ++l) {
-        const bool end = l == ntasks;
-        const int b = l & 1, sb = l % kUSBufs;
-        int4 e = make_int4(-1, 0, 0, 0);
-        int u = -2; // no unit: ends the last one
-        float sv[kUHeads];
-        if (!end) {
-            if (!wait_all(smem_u32(&s_full[sb]), (l / kUSBufs) & 1)) {
-                ok = false;
-                break;
-            }
-            tcgen05_after_sync();
-            e = entry(l);
-            u = unit_of(e);
-            if (e.x >= 0)
-                tmem_ld8(lane_base + 16 * sb, sv);
-            tcgen05_before_sync();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(smem_u32(&s_free[sb]));
-        }
-        const bool live = e.x >= 0;
-
-        if (u != cur_unit) {
-            if (cur_unit >= 0) {
-                if (l_last >= 0)
-                    fold(l_last);
-                if (!ok)
-                    break;
-                finalize(cur_t, cur_g, end);
-                if (!ok)
-                    break;
-            }
-            if (end)
-                break;
-            cur_unit = u;
-            cur_t = e.z;
-            cur_g = e.w;
-            reset();
-            l_last = -1;
-            // the producer wrote the unit's query scale before the Q tile it
-            // made, which S^T of this page waited for
-            if (FP8)
-                unit_scale = p.scale_log2 * qscale[sm_units % kUQScales];
-            ++sm_units;
-        }
-
-        // page maxima per head (log2 domain) across the 128 tokens
-        const bool visible = live && idx < e.y;
-        float wmax[kUHeads];
-#pragma unroll
-        for (int h = 0; h < kUHeads; ++h) {
-            sv[h] = visible ? sv[h] * unit_scale : -INFINITY;
-            wmax[h] = warp_max_f32(sv[h]);
-        }
-        if (lane == 0) {
-            float4 *xw = reinterpret_cast<float4 *>(xbuf + (b * 4 + quarter) * 16 + h0);
-            xw[0] = make_float4(wmax[0], wmax[1], wmax[2], wmax[3]);
-            xw[1] = make_float4(wmax[4], wmax[5], wmax[6], wmax[7]);
-        }
-        ssync();
-        float alpha[kUHeads], pv[kUHeads];
-#pragma unroll
-        for (int h4 = 0; h4 < kUHeads / 4; ++h4) {
-            float4 a[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                a[q] = reinterpret_cast<const float4 *>(xbuf + (b * 4 + q) * 16 + h0)[h4];
-            const float pm[4] = {fmaxf(fmaxf(a[0].x, a[1].x), fmaxf(a[2].x, a[3].x)),
-                                 fmaxf(fmaxf(a[0].y, a[1].y), fmaxf(a[2].y, a[3].y)),
-                                 fmaxf(fmaxf(a[0].z, a[1].z), fmaxf(a[2].z, a[3].z)),
-                                 fmaxf(fmaxf(a[0].w, a[1].w), fmaxf(a[2].w, a[3].w))};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int h = 4 * h4 + k;
-                const float m_new = fmaxf(m_run[h], pm[k]);
-                const float ref = (m_new == -INFINITY) ? 0.f : m_new;
-                alpha[h] = ex2(m_run[h] - ref); // 0 when m_run is -inf
-                m_run[h] = m_new;
-                pv[h] = ex2(sv[h] - ref);
-                lsum[h] = lsum[h] * alpha[h] + pv[h];
-            }
-        }
-        // P^T[h][token idx] into the K-major, 128-byte-swizzled B tile
-        if (l >= 2 && !wait_all(smem_u32(&p_free[b]), ((l >> 1) - 1) & 1)) {
-            ok = false;
-            break;
-        }
-        if (live && !FP8) {
-            // bf16: hi = bf16(p); for the page of a single-page unit also
-            // lo = bf16(p - hi) (p - hi is exact in fp32) in the second part.
-            // There a handful of positions can carry the whole softmax, and
-            // P rounded to bf16 alone would put an error of up to 2^-9 |V| into
-            // O; a unit with two or more pages sees at least 129 positions
-            // (every selected block but the last visible one is full), where
-            // those roundings average out.  NVFP4: f16(p).
-            uint8_t *pt = pbuf + b * p_tile_bytes(KVF) + (idx >> 6) * (kUPTile / 2);
+    // P^T[h][token idx] of page i of pass buffer pb, in the K-major,
+    // 128-byte-swizzled B-operand form.
+    auto store_p = [&](const float (&pv)[kUHeads], int pb, int i, bool hilo) {
+        if (!FP8) {
+            // bf16: hi = bf16(p); with hilo (the page of a single-page unit)
+            // also lo = bf16(p - hi) (exact in fp32) in the second part.  There
+            // a handful of positions can carry the whole softmax, and P rounded
+            // to bf16 alone would put an error of up to 2^-9 |V| into O; a unit
+            // with two or more pages sees at least 129 positions (every
+            // selected block but the last visible one is full), where those
+            // roundings average out.  NVFP4: f16(p).
+            uint8_t *pt = pbuf + pb * p_tile_bytes(KVF) + i * kUPTile + (idx >> 6) * (kUPTile / 2);
             const int col = idx & 63;
-            const bool hilo = !F4 && qt[e.z + 1] - qt[e.z] == 1;
 #pragma unroll
             for (int h = 0; h < kUHeads; ++h) {
                 const int hh = h0 + h;
@@ -1113,11 +1257,10 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
                     }
                 }
             }
-            fence_async_smem();
-        } else if (live) {
+        } else {
             // FP8: 256 P as E4M3 hi + lo, one byte per (head row, token) in
             // each of two K-major tiles of 16 rows x 128 bytes
-            uint8_t *phi = pbuf + b * p_tile_bytes(KVF), *plo = phi + kUPTile / 2;
+            uint8_t *phi = pbuf + pb * p_tile_bytes(KVF) + i * kUPTile, *plo = phi + kUPTile / 2;
 #pragma unroll
             for (int h = 0; h < kUHeads; h += 2) {
                 uint32_t hi, lo;
@@ -1130,24 +1273,167 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
                     plo[off] = (uint8_t)(lo >> (8 * k));
                 }
             }
-            fence_async_smem();
         }
+    };
+
+    int j = 0, j_last = -1, sm_units = 0;
+    float unit_scale = p.scale_log2; // logits to base 2 (FP8: / the unit's query scale)
+    // Passes of one or two pages of a unit: one max exchange, one P^T hand-off
+    // and one O^T fold per pass.  One pass past the last task (l0 == ntasks)
+    // finishes the last unit, so that finalize has one call site: its code,
+    // run once per unit, is fetched once per CTA instead of once per copy.
+    for (int l0 = 0; l0 <= ntasks && ok; ++j) {
+        const bool end = l0 == ntasks;
+        const int np = end ? 0 : pass_len(l0), pb = j & 1;
+        int4 e0 = make_int4(-1, 0, 0, 0), e1 = make_int4(-1, 0, 0, 0);
+        int u = -2; // no unit: ends the last one
+        float sv0[kUHeads], sv1[kUHeads];
+        if (!end) {
+            for (int i = 0; i < np && ok; ++i) {
+                const int l = l0 + i;
+                ok = wait_all(smem_u32(&s_full[l % kUSBufs]), (l / kUSBufs) & 1);
+            }
+            if (!ok)
+                break;
+            tcgen05_after_sync();
+            e0 = entry(l0);
+            u = unit_of(e0);
+            uint32_t r0[kUHeads], r1[kUHeads];
+            if (e0.x >= 0)
+                tmem_ld8_nowait(lane_base + 16 * (l0 % kUSBufs), r0);
+            if (np == 2) {
+                e1 = entry(l0 + 1);
+                if (e1.x >= 0)
+                    tmem_ld8_nowait(lane_base + 16 * ((l0 + 1) % kUSBufs), r1);
+            }
+            tmem_wait_ld();
+#pragma unroll
+            for (int h = 0; h < kUHeads; ++h) {
+                sv0[h] = __uint_as_float(r0[h]);
+                sv1[h] = __uint_as_float(r1[h]);
+            }
+            tcgen05_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                for (int i = 0; i < np; ++i)
+                    mbar_arrive(smem_u32(&s_free[(l0 + i) % kUSBufs]));
+        }
+        const bool live0 = e0.x >= 0, live1 = np == 2 && e1.x >= 0;
+
+        if (u != cur_unit) {
+            if (cur_unit >= 0) {
+                if (j_last >= 0)
+                    fold(j_last);
+                if (!ok)
+                    break;
+                finalize(cur_t, cur_g, end);
+                if (!ok)
+                    break;
+            }
+            if (end)
+                break;
+            cur_unit = u;
+            cur_t = e0.z;
+            cur_g = e0.w;
+            reset();
+            j_last = -1;
+            {
+                const UnitOwn w = own_of(cur_t, cur_g);
+                cur_cand = w.c_first == c && w.c_last > c;
+            }
+            // the producer wrote the unit's query scale before the Q tile it
+            // made, which S^T of this page waited for
+            if (FP8)
+                unit_scale = p.scale_log2 * qscale[sm_units % kUQScales];
+            ++sm_units;
+        }
+
+        // The last pass of the last unit, begun here and continued later: read
+        // the other part now if the producer found it published, so that
+        // finalize merges without a round trip.
+        if (l0 + np == ntasks && cur_cand) {
+            if (!wait_all(smem_u32(last_bar), 0)) {
+                ok = false;
+                break;
+            }
+            if (last_chk[0]) {
+                const float *sl = p.partial + (size_t)(last_chk[1] + cur_unit) * kPartialFloats;
+#pragma unroll
+                for (int h = 0; h < kUHeads; ++h) {
+                    ms2[h] = __ldcg(sl + kGroup * kDim + h0 + h);
+                    ls2[h] = __ldcg(sl + kGroup * kDim + kGroup + h0 + h);
+                    os2[h] = __ldcg(sl + (h0 + h) * kDim + idx);
+                }
+                pre = true;
+            }
+        }
+
+        // pass maxima per head (log2 domain) across the pages' tokens
+        const bool vis0 = live0 && idx < e0.y, vis1 = live1 && idx < e1.y;
+        float wmax[kUHeads];
+#pragma unroll
+        for (int h = 0; h < kUHeads; ++h) {
+            sv0[h] = vis0 ? sv0[h] * unit_scale : -INFINITY;
+            sv1[h] = vis1 ? sv1[h] * unit_scale : -INFINITY;
+            wmax[h] = warp_max_f32(fmaxf(sv0[h], sv1[h]));
+        }
+        if (lane == 0) {
+            float4 *xw = reinterpret_cast<float4 *>(xbuf + (pb * 4 + quarter) * 16 + h0);
+            xw[0] = make_float4(wmax[0], wmax[1], wmax[2], wmax[3]);
+            xw[1] = make_float4(wmax[4], wmax[5], wmax[6], wmax[7]);
+        }
+        ssync();
+        float alpha[kUHeads];
+#pragma unroll
+        for (int h4 = 0; h4 < kUHeads / 4; ++h4) {
+            float4 a[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                a[q] = reinterpret_cast<const float4 *>(xbuf + (pb * 4 + q) * 16 + h0)[h4];
+            const float pm[4] = {fmaxf(fmaxf(a[0].x, a[1].x), fmaxf(a[2].x, a[3].x)),
+                                 fmaxf(fmaxf(a[0].y, a[1].y), fmaxf(a[2].y, a[3].y)),
+                                 fmaxf(fmaxf(a[0].z, a[1].z), fmaxf(a[2].z, a[3].z)),
+                                 fmaxf(fmaxf(a[0].w, a[1].w), fmaxf(a[2].w, a[3].w))};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int h = 4 * h4 + k;
+                const float m_new = fmaxf(m_run[h], pm[k]);
+                const float ref = (m_new == -INFINITY) ? 0.f : m_new;
+                alpha[h] = ex2(m_run[h] - ref); // 0 when m_run is -inf
+                m_run[h] = m_new;
+                sv0[h] = ex2(sv0[h] - ref);     // P of page 0 (0 where not visible)
+                sv1[h] = ex2(sv1[h] - ref);     // P of page 1
+                lsum[h] = lsum[h] * alpha[h] + (sv0[h] + sv1[h]);
+            }
+        }
+        // P^T of the pass into buffer pb, once the P.V MMAs of pass j - 2 read it
+        if (j >= 2 && !wait_all(smem_u32(&p_free[pb]), ((j >> 1) - 1) & 1)) {
+            ok = false;
+            break;
+        }
+        if (live0)
+            store_p(sv0, pb, 0, np == 1 && qt[e0.z + 1] - qt[e0.z] == 1);
+        if (live1)
+            store_p(sv1, pb, 1, false);
+        if (live0 || live1)
+            fence_async_smem();
         __syncwarp();
         if (lane == 0)
-            mbar_arrive(smem_u32(&p_full[b]));
+            mbar_arrive(smem_u32(&p_full[pb]));
 
-        // fold the previous page of this unit, then this page becomes pending
-        if (l_last >= 0) {
-            fold(l_last);
+        // fold the previous pass of this unit, then this pass becomes pending
+        if (j_last >= 0) {
+            fold(j_last);
             if (!ok)
                 break;
         }
-        // a page with no data contributes p = 0 and leaves the state unchanged
+        // a pass with no data contributes p = 0 and leaves the state unchanged
 #pragma unroll
         for (int h = 0; h < kUHeads; ++h)
-            alpha_prev[h] = live ? alpha[h] : 1.f;
-        pending = live;
-        l_last = l;
+            alpha_prev[h] = (live0 || live1) ? alpha[h] : 1.f;
+        pending = live0 || live1;
+        j_last = j;
+        l0 += np;
     }
     if (!ok) {
         set_error(p.err, kErrTimeout);
@@ -1155,8 +1441,10 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
     }
     tcgen05_before_sync();
     __syncwarp();
-    if (lane == 0)
+    if (lane == 0) {
+        *smx_done = 1;
         mbar_arrive(smem_u32(done_bar));
+    }
 }
 
 // ---- tensor map of the KV pool: rows of 128 elements, [pages*2*Hkv*128] rows ----
