@@ -1084,11 +1084,12 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
                 lbuf[quarter * 16 + h0 + h] = v;
         }
         ssync();
+        // (lbuf is next written in the next unit's finalize, after at least
+        // one pass and its barrier: every thread has read it by then)
         float L[kUHeads];
 #pragma unroll
         for (int h = 0; h < kUHeads; ++h)
             L[h] = lbuf[h0 + h] + lbuf[16 + h0 + h] + lbuf[32 + h0 + h] + lbuf[48 + h0 + h];
-        ssync(); // lbuf is reused by the next unit
         const UnitOwn w = own_of(t, g);
         const int u = w.u;
         const bool whole = w.c_first == w.c_last;

@@ -7,9 +7,8 @@
 // largest block score, ties toward the smaller block index, for any tie
 // width; ascending, -1 padded ("Add Rubin (sm_107) MiniMax-M3.1 low-latency
 // decode targets", q8kv4 indexer commit).  Lane l holds the order-preserving
-// keys of blocks l, l + 32, ... in registers.  theta, the k-th largest key, is
-// built bit by bit from the top: a bit is kept while at least k keys are >=
-// the candidate (a warp-wide sum per bit).  The selection pass walks the
+// keys of blocks l, l + 32, ... in registers; a threshold search finds the
+// k-th largest key theta (warp_select_keys).  The selection pass walks the
 // blocks in index order 32 at a time; ballots give each tie its rank and each
 // selected block its output slot, so the table comes out ascending.
 // Comparisons only: bit-exact.
@@ -22,24 +21,58 @@ namespace msa {
 constexpr int kWarpSelMaxN = 2048; // longest row of the warp select
 
 // The k largest of a warp's row of keys (lane holds keys of blocks lane,
-// lane + 32, ...; 0 below every candidate), ties to the smaller block:
-// out[0..k) ascending.  Requires more than k candidate blocks.
+// lane + 32, ...; 0 for blocks past the row, below every key of a block of
+// the row, which are all >= 1), ties to the smaller block: out[0..k)
+// ascending.  Requires more than k candidate blocks.
+//
+// theta, the k-th largest key, is built from the top: a bit is kept while
+// at least k keys are >= the candidate.  Bits that every key of the row has
+// are set from the start and bits that none has are never tried: with
+// them in place the count of keys >= a candidate is the one the plain
+// bit-by-bit search sees (a key that matches theta above the tried bit and
+// has it set also has every common bit below it).  The other bits are
+// decided two at a time from three independent warp-wide counts.
 template <int S>
 __device__ __forceinline__ void warp_select_keys(const uint32_t (&key)[S], int k, int32_t *out)
 {
     const int lane = threadIdx.x & 31;
-    uint32_t theta = 0;
-#pragma unroll 1
-    for (int bit = 31; bit >= 0; --bit) {
-        const uint32_t cand = theta | (1u << bit);
+    uint32_t k_or = 0u, k_and = 0xFFFFFFFFu;
+#pragma unroll
+    for (int s = 0; s < S; ++s) {
+        k_or |= key[s];
+        k_and &= key[s] ? key[s] : 0xFFFFFFFFu; // blocks past the row do not count
+    }
+    k_or = __reduce_or_sync(0xffffffffu, k_or);
+    k_and = __reduce_and_sync(0xffffffffu, k_and);
+    uint32_t theta = k_and;
+    uint32_t open = k_or & ~k_and; // bits in which the row's keys differ
+    auto count_ge = [&](uint32_t cand) {
         int c0 = 0, c1 = 0;
 #pragma unroll
         for (int s = 0; s < S; s += 2) {
             c0 += key[s] >= cand;
             c1 += key[s + 1] >= cand;
         }
-        if ((int)__reduce_add_sync(0xffffffffu, (unsigned)(c0 + c1)) >= k)
-            theta = cand;
+        return c0 + c1;
+    };
+#pragma unroll 1
+    while (open) {
+        const uint32_t hb = 1u << (31 - __clz(open)); // highest open bit
+        open &= ~hb;
+        if (!open) {
+            if ((int)__reduce_add_sync(0xffffffffu, (unsigned)count_ge(theta | hb)) >= k)
+                theta |= hb;
+            break;
+        }
+        const uint32_t lb = 1u << (31 - __clz(open)); // the next one
+        open &= ~lb;
+        const int n_h = (int)__reduce_add_sync(0xffffffffu, (unsigned)count_ge(theta | hb));
+        const int n_hl = (int)__reduce_add_sync(0xffffffffu, (unsigned)count_ge(theta | hb | lb));
+        const int n_l = (int)__reduce_add_sync(0xffffffffu, (unsigned)count_ge(theta | lb));
+        if (n_h >= k)
+            theta |= hb | (n_hl >= k ? lb : 0u);
+        else if (n_l >= k)
+            theta |= lb;
     }
     int gt = 0;
 #pragma unroll
