@@ -51,40 +51,65 @@ struct Task {
     int t, g, i;
 };
 
-// qt[t] = sum_{t' < t} n_t' (the tasks of one KV head before token t); qt[T] = total.
-__device__ void build_token_prefix(const DecodeParams &p, int *qt)
+// qt[t] = sum_{t' < t} n_t' (the tasks of one KV head before token t); qt[T] =
+// total.  Called by every thread of the CTA: each loads the counts of a
+// contiguous chunk of tokens (one round of global loads, however many
+// tokens), then a CTA-wide exclusive scan of the chunk sums (tmp: one int per
+// warp + 1); the caller synchronises before reading qt.
+__device__ void build_token_prefix(const DecodeParams &p, int *qt, int *tmp)
 {
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
-        int carry = 0;
-        for (int base = 0; base < p.T; base += 32) {
-            const int t = base + lane;
-            int n = 0;
-            if (t < p.T) {
-                const int r = t / p.nq, j = t - r * p.nq;
-                const int sl = p.seq_lens[r];
-                const long long nb = ((long long)sl + p.nq - 1 + kPage - 1) / kPage;
-                if (sl >= 1 && nb <= p.maxB) {
-                    n = ceil_div(sl + j, kPage);
-                    n = n < p.k ? n : p.k;
-                } else if (blockIdx.x == 0) {
-                    set_error(p.err, kErrSeqLen); // the token gets no tasks: its outputs are not written
-                }
-            }
-            int incl = n;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int v = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o)
-                    incl += v;
-            }
-            if (t < p.T)
-                qt[t] = carry + incl - n;
-            carry += __shfl_sync(0xffffffffu, incl, 31);
+    const int T = p.T, nth = blockDim.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = nth >> 5;
+    const int per = (T + nth - 1) / nth;
+    const int lo = min(T, (int)threadIdx.x * per), hi = min(T, lo + per);
+    int sum = 0;
+    for (int t = lo; t < hi; ++t) {
+        const int r = t / p.nq, j = t - r * p.nq;
+        const int sl = p.seq_lens[r];
+        const long long nb = ((long long)sl + p.nq - 1 + kPage - 1) / kPage;
+        int n = 0;
+        if (sl >= 1 && nb <= p.maxB) {
+            n = ceil_div(sl + j, kPage);
+            n = n < p.k ? n : p.k;
+        } else if (blockIdx.x == 0) {
+            set_error(p.err, kErrSeqLen); // the token gets no tasks: its outputs are not written
         }
-        if (lane == 0)
-            qt[p.T] = carry;
+        qt[t] = n;
+        sum += n;
     }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += v;
+    }
+    if (lane == 31)
+        tmp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int w = lane < nwarps ? tmp[lane] : 0;
+        int wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o)
+                wi += v;
+        }
+        if (lane < nwarps)
+            tmp[lane] = wi - w;
+        if (lane == nwarps - 1)
+            tmp[nwarps] = wi;
+    }
+    __syncthreads();
+    int run = tmp[warp] + incl - sum;
+    for (int t = lo; t < hi; ++t) {
+        const int n = qt[t];
+        qt[t] = run;
+        run += n;
+    }
+    if (threadIdx.x == 0)
+        qt[T] = tmp[nwarps];
 }
 
 __device__ __forceinline__ Task task_of(long long x, const int *qt, int T)
@@ -437,7 +462,7 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
     }
     if (warp == 1)
         tmem_alloc(smem_u32(tmem_slot), kUTmemCols);
-    build_token_prefix(p, qt);
+    build_token_prefix(p, qt, reinterpret_cast<int *>(lbuf)); // lbuf is free until the first finalize
     tcgen05_before_sync();
     __syncthreads();
     tcgen05_after_sync();
