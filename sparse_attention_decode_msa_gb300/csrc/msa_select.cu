@@ -204,7 +204,10 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(const SelectPa
 
 // ---------------------------------------------------------------------------
 // Rows of up to 2048 blocks: one warp per token (msa_select_warp.cuh).
-constexpr int kWarpSelWarps = 4;
+// One warp per CTA: the rows spread over more SMs and a small CTA leaves room
+// next to it for the decode CTA that follows in the step (measured 0.5-1 us
+// faster fused steps than 4-warp CTAs on every workload).
+constexpr int kWarpSelWarps = 1;
 
 template <int S> // key slots per lane: rows of up to 32 * S blocks
 __global__ void __launch_bounds__(32 * kWarpSelWarps) select_topk_warp_kernel(const SelectParams p)
