@@ -182,9 +182,9 @@ __device__ int4 make_entry(const DecodeParams &p, long long x, const int *qt)
 // 128-byte swizzle; the V tile, as loaded, is the MN-major form of V^T; P^T is
 // written by the softmax warps in the K-major 128-byte-swizzled form.
 // Warps: 0 = TMA producer + task table, 1 = S^T issuer + TMEM owner,
-// 2..9 = softmax (thread = one TMEM lane: a token for S^T, a dimension for
-// O^T; two warps per lane quarter, 8 heads each), 10 = O^T issuer,
-// 11..14 = NVFP4 converters (NVFP4 K/V only).  The two MMA issuers are
+// 2 = O^T issuer, 3 = publisher, 4..11 = softmax (thread = one TMEM lane: a
+// token for S^T, a dimension for O^T; two warps per lane quarter, 8 heads
+// each), 12..15 = NVFP4 converters (NVFP4 K/V only).  The two MMA issuers are
 // separate threads so that S^T of the next pages (four accumulators) is
 // never queued behind P^T of this one.  The softmax warps exchange per-head page maxima through shared memory,
 // keep the running max / denominator per head, and fold each page's O^T into
@@ -196,9 +196,18 @@ constexpr int kUCvtWarps = 4;              // NVFP4 only: e2m1 x E4M3 -> f16 con
 constexpr int kKvBf16 = 0, kKvFp8 = 1, kKvNvfp4 = 2;
 template <int KVF>
 constexpr int kUThreadsT = 32 * (4 + kUSmxWarps + (KVF == kKvNvfp4 ? kUCvtWarps : 0)); // producer, S MMA, softmax, PV MMA, publisher[, converters]
-constexpr int kUWarpPV = 2 + kUSmxWarps;   // the warp that issues the P.V MMAs
-constexpr int kUWarpPub = 3 + kUSmxWarps;  // the warp that publishes the first unit's partial
+// Warp roles by warpgroup: 0 = producer, S issuer, P.V issuer, publisher;
+// 1, 2 = softmax; 3 = NVFP4 converters.
+constexpr int kUWarpPV = 2;                // the warp that issues the P.V MMAs
+constexpr int kUWarpPub = 3;               // the warp that publishes the first unit's partial
+constexpr int kUWarpSmx = 4;               // the first softmax warp
 constexpr int kUWarpCvt = 4 + kUSmxWarps;  // NVFP4: the first converter warp
+// NVFP4: registers a thread after the reallocation (launched with 128: the
+// sum over the 512 threads is the launch allocation)
+constexpr int kURegsWg0 = 64, kURegsSmx = 176, kURegsCvt = 96;
+static_assert(128 * kURegsWg0 + 32 * kUSmxWarps * kURegsSmx + 32 * kUCvtWarps * kURegsCvt <=
+                  32 * (4 + kUSmxWarps + kUCvtWarps) * 128,
+              "NVFP4 register split above the launch allocation");
 constexpr int kF4Tile = kPage * kDim / 2 + kPage * kDim / 16; // NVFP4 K or V tile: codes then scales
 constexpr int kUQScales = 16;              // FP8: ring of per-unit query scales (> units in flight)
 constexpr float kPScale = 256.f;           // FP8: P^T is stored as 256 * P (E4M3 hi + lo)
@@ -584,105 +593,6 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
         table[i] = make_entry(p, x_begin + i, qt);
     __syncthreads();
 
-    if (warp == 0) {
-        // =================== producer ===================
-        constexpr int kAhead = STAGES / 2;
-        const uint64_t kv_policy = l2_evict_first_policy(); // pages are streamed
-        int issued = 0, prod_units = 0, prod_last = -1;
-        bool ok = true;
-        for (int z = 0; z < 2 * ntasks && ok; ++z) {
-            // copy z: K(l) or V(l) (the order of copy_of_k / copy_of_v)
-            const bool is_k = (z & 1) == 0;
-            const int l = z >> 1;
-            if (lane == 0 && z >= STAGES)
-                ok = mbar_wait_or_abort(smem_u32(&empty[z % STAGES]), ((z / STAGES) - 1) & 1,
-                                        abort_flag, wl);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok)
-                break;
-            const int4 e = entry(l);
-            if (is_k) {
-                // The slowest reader of the table is the P.V issuer: copy
-                // K(l) comes after V(l - 1), which took the stage of
-                // V(l - 1 - kAhead) once its P.V MMAs had freed it, so that
-                // reader trails this warp by at most kAhead tasks (+ 2 with
-                // the NVFP4 converters and their two staging tiles between
-                // them); the softmax warps, the S issuer and the converters
-                // are ahead of it.  Only kAhead + 3 (+ 2) tasks into a window
-                // has every reader left the window before it.
-                if (l % kWin == kAhead + 3 + (F4 ? 2 : 0) && l >= kWin && (l / kWin + 1) * kWin < ntasks)
-                    fill_window(l / kWin + 1);
-                const int u = unit_of(e);
-                if (u != prod_last) {
-                    // the unit's 16 query rows into query buffer qb (the first
-                    // unit's were staged before the grid wait)
-                    prod_last = u;
-                    const int qb = prod_units & 1;
-                    if (prod_units > 0) {
-                        if (lane == 0 && prod_units >= 2)
-                            ok = mbar_wait_or_abort(smem_u32(&qempty[qb]), ((prod_units >> 1) - 1) & 1, abort_flag, wl);
-                        ok = __shfl_sync(0xffffffffu, ok, 0);
-                        if (!ok)
-                            break;
-                        load_q(qb, (e.z * p.Hkv + e.w) * kGroup, prod_units);
-                    }
-                    ++prod_units;
-                }
-            }
-            if (lane == 0) {
-                const int st = z % STAGES;
-                const uint32_t bar = smem_u32(&full[st]);
-                issued = z + 1;
-                if (e.x < 0) {
-                    mbar_arrive(bar); // no data: consumers skip the task
-                } else {
-                    const uint32_t dst = smem_u32(ring + (size_t)st * kRaw);
-                    const int krow = e.x + (is_k ? 0 : p.Hkv * kPage);
-                    mbar_arrive_expect_tx(bar, kRaw);
-                    if (F4) { // one contiguous tile: codes then scales
-                        bulk_load_hint(dst, p.kv_raw + (size_t)(krow / kPage) * kF4Tile, kF4Tile, bar,
-                                       kv_policy);
-                    } else {
-                        tma_load_2d_hint(dst, &kv_map, 0, krow, bar, kv_policy);
-                        if (!FP8)
-                            tma_load_2d_hint(dst + kUTile / 2, &kv_map, 64, krow, bar, kv_policy);
-                    }
-                }
-            }
-        }
-        // The CTA's last unit, begun here and continued by later CTAs, which
-        // publish their parts at their starts: with every copy issued, one
-        // acquire load tells whether the one other part is in, so that the
-        // softmax warps can read it during their last pass and merge at once.
-        if (ok && ntasks > 0 && lane == 0) {
-            const int4 el = entry(ntasks - 1);
-            const UnitOwn w = own_of(el.z, el.w);
-            if (w.c_first == c && w.c_last > c) {
-                int other = -1, n_other = 0;
-                for (int cc = c + 1; cc <= w.c_last; ++cc)
-                    if (!range_empty(cc, P, G)) {
-                        other = cc;
-                        ++n_other;
-                    }
-                int in = 0;
-                if (n_other == 1 && (long long)w.c_last + w.u < p.slots)
-                    in = ld_acquire_gpu(&p.counters[w.u]) == 1;
-                last_chk[0] = in;
-                last_chk[1] = other;
-                mbar_arrive(smem_u32(last_bar));
-            }
-        }
-        if (!ok && lane == 0) {
-            set_error(p.err, kErrTimeout);
-            *abort_flag = 1;
-            for (int z = issued - STAGES < 0 ? 0 : issued - STAGES; z < issued; ++z)
-                (void)mbar_wait_bounded(smem_u32(&full[z % STAGES]), (z / STAGES) & 1);
-            for (int u = q_issued - 2 < 0 ? 0 : q_issued - 2; u < q_issued; ++u)
-                (void)mbar_wait_bounded(smem_u32(&qfull[u & 1]), (u >> 1) & 1);
-        }
-        return;
-    }
-
     // Instruction descriptors.  bf16: kind::f16, 8 steps of K = 16.  FP8:
     // kind::f8f6f4 on the E4M3 tiles as loaded, 4 steps of K = 32 for each of
     // the hi and lo parts of Q (in S^T) and of P (in O^T); operand types
@@ -691,85 +601,6 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
     constexpr uint32_t kE4M3 = (FP8 || F4) ? ~((7u << 7) | (7u << 10)) : ~0u;
     constexpr uint32_t kIdescS = umma_idesc_bf16(128, 16, 0, 0) & kE4M3; // K and Q^T both K-major
     constexpr uint32_t kIdescO = umma_idesc_bf16(128, 16, 1, 0) & kE4M3; // V^T MN-major, P^T K-major
-
-    if (warp == 1) {
-        // =================== S issuer (lane 0) + TMEM owner ===================
-        // S^T(l) into accumulator l % kUSBufs as soon as K(l) has landed and
-        // the softmax warps have read S^T(l - kUSBufs): the S MMAs run ahead
-        // of the softmax, independently of the P.V MMAs (their own thread).
-        bool ok = true;
-        if (lane == 0) {
-            int s_units = 0, s_unit = -1;
-            for (int l = 0; l < ntasks; ++l) {
-                const int zk = copy_of_k(l), sb = l % kUSBufs;
-                // NVFP4: K(l) widened into staging tile l & 1; else the ring tile landed
-                if (F4 ? !mbar_wait_or_abort(smem_u32(&kst_full[l & 1]), (l >> 1) & 1, abort_flag, wl)
-                       : !mbar_wait_or_abort(smem_u32(&full[zk % STAGES]), (zk / STAGES) & 1, abort_flag, wl)) {
-                    ok = false;
-                    break;
-                }
-                const int4 e = entry(l);
-                const int u = unit_of(e);
-                if (u != s_unit) {
-                    // NVFP4: the converter warps widen the query tile to f16 in place
-                    uint64_t *qready = F4 ? qconv : qfull;
-                    if (!mbar_wait_or_abort(smem_u32(&qready[s_units & 1]), (s_units >> 1) & 1, abort_flag, wl)) {
-                        ok = false;
-                        break;
-                    }
-                    s_unit = u;
-                    ++s_units;
-                }
-                const int qb = (s_units - 1) & 1;
-                if (l >= kUSBufs &&
-                    !mbar_wait_or_abort(smem_u32(&s_free[sb]), ((l / kUSBufs) - 1) & 1, abort_flag, wl)) {
-                    ok = false;
-                    break;
-                }
-                tcgen05_after_sync();
-                if (e.x >= 0) {
-                    const uint32_t tileK = F4 ? smem_u32(kst + (l & 1) * kUTile)
-                                              : smem_u32(ring + (size_t)(zk % STAGES) * kRaw);
-                    const uint32_t qtile = smem_u32(qbuf + qb * kUQTile);
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        if (!FP8) {
-                            const uint64_t a = umma_desc_sw128(tileK + (ks >> 2) * (kUTile / 2) + (ks & 3) * 32, 16, 1024);
-                            const uint64_t bq = umma_desc_sw128(qtile + (ks >> 2) * (kUQTile / 2) + (ks & 3) * 32, 16, 1024);
-                            umma_bf16(tmem + 16 * sb, a, bq, kIdescS, ks > 0);
-                        } else { // steps 0..3: Q hi, 4..7: Q lo; 32 dims (bytes) per step
-                            const uint64_t a = umma_desc_sw128(tileK + (ks & 3) * 32, 16, 1024);
-                            const uint64_t bq = umma_desc_sw128(qtile + (ks >> 2) * (kUQTile / 2) + (ks & 3) * 32, 16, 1024);
-                            umma_f8(tmem + 16 * sb, a, bq, kIdescS, ks > 0);
-                        }
-                    }
-                }
-                umma_commit(smem_u32(&s_full[sb]));
-                umma_commit(F4 ? smem_u32(&kst_empty[l & 1]) : smem_u32(&empty[zk % STAGES])); // K tile read
-                // last task of its unit: the query tile can be replaced
-                if (l + 1 == ntasks || unit_of(entry(l + 1)) != u)
-                    umma_commit(smem_u32(&qempty[qb]));
-            }
-            if (!ok) {
-                set_error(p.err, kErrTimeout);
-                *abort_flag = 1;
-                // the MMAs issued so far finish before TMEM is freed
-                umma_commit(smem_u32(s_drain));
-                (void)mbar_wait_bounded(smem_u32(s_drain), 0);
-            }
-        }
-        __syncwarp();
-        // free TMEM once the softmax warps and the PV issuer are done with it
-        // (they always arrive, also after an abort; the waits are bounded)
-        if (lane == 0) {
-            (void)mbar_wait_bounded(smem_u32(done_bar), 0);
-            (void)mbar_wait_bounded(smem_u32(pv_done), 0);
-        }
-        __syncwarp();
-        tcgen05_after_sync();
-        tmem_dealloc(tmem, kUTmemCols);
-        return;
-    }
 
     // Pages per softmax pass: a pass takes the next two tasks if they belong
     // to one unit (bf16 / E4M3 values), else one.  The softmax warps and the
@@ -780,163 +611,338 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
         return unit_of(entry(l0 + 1)) == unit_of(entry(l0)) ? 2 : 1;
     };
 
-    if (warp == kUWarpPV) {
-        // =================== P.V issuer (lane 0) ===================
-        // O^T of pass j into accumulator j & 1 once the softmax warps have
-        // written P^T of the pass and folded O^T of pass j - 2, each page as
-        // soon as its V tile has landed; the pages of a pass share the pass's
-        // softmax reference and accumulate into one O^T.
-        if (lane == 0) {
+    if (warp < kUWarpSmx) {
+        // ======== warpgroup 0: producer, S issuer, P.V issuer, publisher ========
+        if constexpr (F4)
+            setmaxnreg_dec<kURegsWg0>(); // the NVFP4 CTA's registers go to the softmax warps
+
+        if (warp == 0) {
+            // =================== producer ===================
+            constexpr int kAhead = STAGES / 2;
+            const uint64_t kv_policy = l2_evict_first_policy(); // pages are streamed
+            int issued = 0, prod_units = 0, prod_last = -1;
             bool ok = true;
-            int j = 0;
-            for (int l0 = 0; l0 < ntasks && ok; l0 += pass_len(l0), ++j) {
-                const int np = pass_len(l0), pb = j & 1;
-                if (!mbar_wait_or_abort(smem_u32(&p_full[pb]), (j >> 1) & 1, abort_flag, wl) ||
-                    (j >= 2 && !mbar_wait_or_abort(smem_u32(&o_free[pb]), ((j >> 1) - 1) & 1, abort_flag, wl))) {
-                    ok = false;
+            for (int z = 0; z < 2 * ntasks && ok; ++z) {
+                // copy z: K(l) or V(l) (the order of copy_of_k / copy_of_v)
+                const bool is_k = (z & 1) == 0;
+                const int l = z >> 1;
+                if (lane == 0 && z >= STAGES)
+                    ok = mbar_wait_or_abort(smem_u32(&empty[z % STAGES]), ((z / STAGES) - 1) & 1,
+                                            abort_flag, wl);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok)
                     break;
+                const int4 e = entry(l);
+                if (is_k) {
+                    // The slowest reader of the table is the P.V issuer: copy
+                    // K(l) comes after V(l - 1), which took the stage of
+                    // V(l - 1 - kAhead) once its P.V MMAs had freed it, so that
+                    // reader trails this warp by at most kAhead tasks (+ 2 with
+                    // the NVFP4 converters and their two staging tiles between
+                    // them); the softmax warps, the S issuer and the converters
+                    // are ahead of it.  Only kAhead + 3 (+ 2) tasks into a window
+                    // has every reader left the window before it.
+                    if (l % kWin == kAhead + 3 + (F4 ? 2 : 0) && l >= kWin && (l / kWin + 1) * kWin < ntasks)
+                        fill_window(l / kWin + 1);
+                    const int u = unit_of(e);
+                    if (u != prod_last) {
+                        // the unit's 16 query rows into query buffer qb (the first
+                        // unit's were staged before the grid wait)
+                        prod_last = u;
+                        const int qb = prod_units & 1;
+                        if (prod_units > 0) {
+                            if (lane == 0 && prod_units >= 2)
+                                ok = mbar_wait_or_abort(smem_u32(&qempty[qb]), ((prod_units >> 1) - 1) & 1, abort_flag, wl);
+                            ok = __shfl_sync(0xffffffffu, ok, 0);
+                            if (!ok)
+                                break;
+                            load_q(qb, (e.z * p.Hkv + e.w) * kGroup, prod_units);
+                        }
+                        ++prod_units;
+                    }
                 }
-                bool acc = false; // a page of the pass has written the accumulator
-                for (int i = 0; i < np; ++i) {
-                    const int l = l0 + i, zv = copy_of_v(l, ntasks);
-                    if (F4 ? !mbar_wait_or_abort(smem_u32(&vst_full[l & 1]), (l >> 1) & 1, abort_flag, wl)
-                           : !mbar_wait_or_abort(smem_u32(&full[zv % STAGES]), (zv / STAGES) & 1, abort_flag, wl)) {
+                if (lane == 0) {
+                    const int st = z % STAGES;
+                    const uint32_t bar = smem_u32(&full[st]);
+                    issued = z + 1;
+                    if (e.x < 0) {
+                        mbar_arrive(bar); // no data: consumers skip the task
+                    } else {
+                        const uint32_t dst = smem_u32(ring + (size_t)st * kRaw);
+                        const int krow = e.x + (is_k ? 0 : p.Hkv * kPage);
+                        mbar_arrive_expect_tx(bar, kRaw);
+                        if (F4) { // one contiguous tile: codes then scales
+                            bulk_load_hint(dst, p.kv_raw + (size_t)(krow / kPage) * kF4Tile, kF4Tile, bar,
+                                           kv_policy);
+                        } else {
+                            tma_load_2d_hint(dst, &kv_map, 0, krow, bar, kv_policy);
+                            if (!FP8)
+                                tma_load_2d_hint(dst + kUTile / 2, &kv_map, 64, krow, bar, kv_policy);
+                        }
+                    }
+                }
+            }
+            // The CTA's last unit, begun here and continued by later CTAs, which
+            // publish their parts at their starts: with every copy issued, one
+            // acquire load tells whether the one other part is in, so that the
+            // softmax warps can read it during their last pass and merge at once.
+            if (ok && ntasks > 0 && lane == 0) {
+                const int4 el = entry(ntasks - 1);
+                const UnitOwn w = own_of(el.z, el.w);
+                if (w.c_first == c && w.c_last > c) {
+                    int other = -1, n_other = 0;
+                    for (int cc = c + 1; cc <= w.c_last; ++cc)
+                        if (!range_empty(cc, P, G)) {
+                            other = cc;
+                            ++n_other;
+                        }
+                    int in = 0;
+                    if (n_other == 1 && (long long)w.c_last + w.u < p.slots)
+                        in = ld_acquire_gpu(&p.counters[w.u]) == 1;
+                    last_chk[0] = in;
+                    last_chk[1] = other;
+                    mbar_arrive(smem_u32(last_bar));
+                }
+            }
+            if (!ok && lane == 0) {
+                set_error(p.err, kErrTimeout);
+                *abort_flag = 1;
+                for (int z = issued - STAGES < 0 ? 0 : issued - STAGES; z < issued; ++z)
+                    (void)mbar_wait_bounded(smem_u32(&full[z % STAGES]), (z / STAGES) & 1);
+                for (int u = q_issued - 2 < 0 ? 0 : q_issued - 2; u < q_issued; ++u)
+                    (void)mbar_wait_bounded(smem_u32(&qfull[u & 1]), (u >> 1) & 1);
+            }
+            return;
+        }
+
+        if (warp == 1) {
+            // =================== S issuer (lane 0) + TMEM owner ===================
+            // S^T(l) into accumulator l % kUSBufs as soon as K(l) has landed and
+            // the softmax warps have read S^T(l - kUSBufs): the S MMAs run ahead
+            // of the softmax, independently of the P.V MMAs (their own thread).
+            bool ok = true;
+            if (lane == 0) {
+                int s_units = 0, s_unit = -1;
+                for (int l = 0; l < ntasks; ++l) {
+                    const int zk = copy_of_k(l), sb = l % kUSBufs;
+                    // NVFP4: K(l) widened into staging tile l & 1; else the ring tile landed
+                    if (F4 ? !mbar_wait_or_abort(smem_u32(&kst_full[l & 1]), (l >> 1) & 1, abort_flag, wl)
+                           : !mbar_wait_or_abort(smem_u32(&full[zk % STAGES]), (zk / STAGES) & 1, abort_flag, wl)) {
+                        ok = false;
+                        break;
+                    }
+                    const int4 e = entry(l);
+                    const int u = unit_of(e);
+                    if (u != s_unit) {
+                        // NVFP4: the converter warps widen the query tile to f16 in place
+                        uint64_t *qready = F4 ? qconv : qfull;
+                        if (!mbar_wait_or_abort(smem_u32(&qready[s_units & 1]), (s_units >> 1) & 1, abort_flag, wl)) {
+                            ok = false;
+                            break;
+                        }
+                        s_unit = u;
+                        ++s_units;
+                    }
+                    const int qb = (s_units - 1) & 1;
+                    if (l >= kUSBufs &&
+                        !mbar_wait_or_abort(smem_u32(&s_free[sb]), ((l / kUSBufs) - 1) & 1, abort_flag, wl)) {
                         ok = false;
                         break;
                     }
                     tcgen05_after_sync();
-                    const int4 e = entry(l);
                     if (e.x >= 0) {
-                        const uint32_t tileV = F4 ? smem_u32(vst + (l & 1) * kUTile)
-                                                  : smem_u32(ring + (size_t)(zv % STAGES) * kRaw);
-                        const uint32_t ptile = smem_u32(pbuf + pb * p_tile_bytes(KVF) + i * kUPTile);
-                        // bf16: steps 0..7 take P hi, 8..15 (single-page units) P lo,
-                        // over the same V^T slices
-                        const int pv_steps = (KVF == kKvBf16 && qt[e.z + 1] - qt[e.z] == 1) ? 16 : 8;
-#pragma unroll
-                        for (int ks = 0; ks < 16; ++ks) {
-                            if (ks >= pv_steps)
-                                break;
+                        const uint32_t tileK = F4 ? smem_u32(kst + (l & 1) * kUTile)
+                                                  : smem_u32(ring + (size_t)(zk % STAGES) * kRaw);
+                        const uint32_t qtile = smem_u32(qbuf + qb * kUQTile);
+    #pragma unroll
+                        for (int ks = 0; ks < 8; ++ks) {
                             if (!FP8) {
-                                // V^T, MN-major: 16 tokens per k-step = 16 rows of 128 bytes;
-                                // the two 64-dim halves of a row are 16 KiB apart (LBO)
-                                const int kt = ks & 7;
-                                const uint64_t a = umma_desc_sw128(tileV + kt * 2048, kUTile / 2, 1024);
-                                const uint64_t bp = umma_desc_sw128(
-                                    ptile + (ks >> 3) * kUPTile + (kt >> 2) * (kUPTile / 2) + (kt & 3) * 32, 16, 1024);
-                                umma_bf16(tmem + kUOCol + 16 * pb, a, bp, kIdescO, acc || ks > 0);
-                            } else {
-                                // V^T, MN-major: 32 tokens per k-step = 32 rows of 128 bytes
-                                // (all 128 dims in one swizzle atom); steps 0..3: P hi, 4..7: P lo
-                                const uint64_t a = umma_desc_sw128(tileV + (ks & 3) * 4096, kUTile / 2, 1024);
-                                const uint64_t bp = umma_desc_sw128(ptile + (ks >> 2) * (kUPTile / 2) + (ks & 3) * 32, 16, 1024);
-                                umma_f8(tmem + kUOCol + 16 * pb, a, bp, kIdescO, acc || ks > 0);
+                                const uint64_t a = umma_desc_sw128(tileK + (ks >> 2) * (kUTile / 2) + (ks & 3) * 32, 16, 1024);
+                                const uint64_t bq = umma_desc_sw128(qtile + (ks >> 2) * (kUQTile / 2) + (ks & 3) * 32, 16, 1024);
+                                umma_bf16(tmem + 16 * sb, a, bq, kIdescS, ks > 0);
+                            } else { // steps 0..3: Q hi, 4..7: Q lo; 32 dims (bytes) per step
+                                const uint64_t a = umma_desc_sw128(tileK + (ks & 3) * 32, 16, 1024);
+                                const uint64_t bq = umma_desc_sw128(qtile + (ks >> 2) * (kUQTile / 2) + (ks & 3) * 32, 16, 1024);
+                                umma_f8(tmem + 16 * sb, a, bq, kIdescS, ks > 0);
                             }
                         }
-                        acc = true;
                     }
-                    umma_commit(F4 ? smem_u32(&vst_empty[l & 1]) : smem_u32(&empty[zv % STAGES])); // V tile read
+                    umma_commit(smem_u32(&s_full[sb]));
+                    umma_commit(F4 ? smem_u32(&kst_empty[l & 1]) : smem_u32(&empty[zk % STAGES])); // K tile read
+                    // last task of its unit: the query tile can be replaced
+                    if (l + 1 == ntasks || unit_of(entry(l + 1)) != u)
+                        umma_commit(smem_u32(&qempty[qb]));
                 }
-                if (!ok)
-                    break;
-                umma_commit(smem_u32(&o_full[pb]));
-                umma_commit(smem_u32(&p_free[pb]));
+                if (!ok) {
+                    set_error(p.err, kErrTimeout);
+                    *abort_flag = 1;
+                    // the MMAs issued so far finish before TMEM is freed
+                    umma_commit(smem_u32(s_drain));
+                    (void)mbar_wait_bounded(smem_u32(s_drain), 0);
+                }
             }
-            if (!ok) {
-                set_error(p.err, kErrTimeout);
-                *abort_flag = 1;
-                umma_commit(smem_u32(pv_drain));
-                (void)mbar_wait_bounded(smem_u32(pv_drain), 0);
+            __syncwarp();
+            // free TMEM once the softmax warps and the PV issuer are done with it
+            // (they always arrive, also after an abort; the waits are bounded)
+            if (lane == 0) {
+                (void)mbar_wait_bounded(smem_u32(done_bar), 0);
+                (void)mbar_wait_bounded(smem_u32(pv_done), 0);
             }
-            mbar_arrive(smem_u32(pv_done));
+            __syncwarp();
+            tcgen05_after_sync();
+            tmem_dealloc(tmem, kUTmemCols);
+            return;
         }
-        return;
-    }
 
-    if (warp == kUWarpPub) {
-        // =================== publisher ===================
-        // The CTA's first unit, begun by an earlier CTA, when more units
-        // follow it here: the softmax warps put its partial in this CTA's
-        // slot and go on; this warp counts the arrival (an acquire-release
-        // atomic, a round trip to L2 the softmax warps would otherwise wait
-        // for).  The arrival that completes the unit merges it: here only
-        // when the earlier CTA finished first, which a CTA that was not yet
-        // resident can see.
-        if (ntasks == 0)
+        if (warp == kUWarpPV) {
+            // =================== P.V issuer (lane 0) ===================
+            // O^T of pass j into accumulator j & 1 once the softmax warps have
+            // written P^T of the pass and folded O^T of pass j - 2, each page as
+            // soon as its V tile has landed; the pages of a pass share the pass's
+            // softmax reference and accumulate into one O^T.
+            if (lane == 0) {
+                bool ok = true;
+                int j = 0;
+                for (int l0 = 0; l0 < ntasks && ok; l0 += pass_len(l0), ++j) {
+                    const int np = pass_len(l0), pb = j & 1;
+                    if (!mbar_wait_or_abort(smem_u32(&p_full[pb]), (j >> 1) & 1, abort_flag, wl) ||
+                        (j >= 2 && !mbar_wait_or_abort(smem_u32(&o_free[pb]), ((j >> 1) - 1) & 1, abort_flag, wl))) {
+                        ok = false;
+                        break;
+                    }
+                    bool acc = false; // a page of the pass has written the accumulator
+                    for (int i = 0; i < np; ++i) {
+                        const int l = l0 + i, zv = copy_of_v(l, ntasks);
+                        if (F4 ? !mbar_wait_or_abort(smem_u32(&vst_full[l & 1]), (l >> 1) & 1, abort_flag, wl)
+                               : !mbar_wait_or_abort(smem_u32(&full[zv % STAGES]), (zv / STAGES) & 1, abort_flag, wl)) {
+                            ok = false;
+                            break;
+                        }
+                        tcgen05_after_sync();
+                        const int4 e = entry(l);
+                        if (e.x >= 0) {
+                            const uint32_t tileV = F4 ? smem_u32(vst + (l & 1) * kUTile)
+                                                      : smem_u32(ring + (size_t)(zv % STAGES) * kRaw);
+                            const uint32_t ptile = smem_u32(pbuf + pb * p_tile_bytes(KVF) + i * kUPTile);
+                            // bf16: steps 0..7 take P hi, 8..15 (single-page units) P lo,
+                            // over the same V^T slices
+                            const int pv_steps = (KVF == kKvBf16 && qt[e.z + 1] - qt[e.z] == 1) ? 16 : 8;
+    #pragma unroll
+                            for (int ks = 0; ks < 16; ++ks) {
+                                if (ks >= pv_steps)
+                                    break;
+                                if (!FP8) {
+                                    // V^T, MN-major: 16 tokens per k-step = 16 rows of 128 bytes;
+                                    // the two 64-dim halves of a row are 16 KiB apart (LBO)
+                                    const int kt = ks & 7;
+                                    const uint64_t a = umma_desc_sw128(tileV + kt * 2048, kUTile / 2, 1024);
+                                    const uint64_t bp = umma_desc_sw128(
+                                        ptile + (ks >> 3) * kUPTile + (kt >> 2) * (kUPTile / 2) + (kt & 3) * 32, 16, 1024);
+                                    umma_bf16(tmem + kUOCol + 16 * pb, a, bp, kIdescO, acc || ks > 0);
+                                } else {
+                                    // V^T, MN-major: 32 tokens per k-step = 32 rows of 128 bytes
+                                    // (all 128 dims in one swizzle atom); steps 0..3: P hi, 4..7: P lo
+                                    const uint64_t a = umma_desc_sw128(tileV + (ks & 3) * 4096, kUTile / 2, 1024);
+                                    const uint64_t bp = umma_desc_sw128(ptile + (ks >> 2) * (kUPTile / 2) + (ks & 3) * 32, 16, 1024);
+                                    umma_f8(tmem + kUOCol + 16 * pb, a, bp, kIdescO, acc || ks > 0);
+                                }
+                            }
+                            acc = true;
+                        }
+                        umma_commit(F4 ? smem_u32(&vst_empty[l & 1]) : smem_u32(&empty[zv % STAGES])); // V tile read
+                    }
+                    if (!ok)
+                        break;
+                    umma_commit(smem_u32(&o_full[pb]));
+                    umma_commit(smem_u32(&p_free[pb]));
+                }
+                if (!ok) {
+                    set_error(p.err, kErrTimeout);
+                    *abort_flag = 1;
+                    umma_commit(smem_u32(pv_drain));
+                    (void)mbar_wait_bounded(smem_u32(pv_drain), 0);
+                }
+                mbar_arrive(smem_u32(pv_done));
+            }
             return;
-        const int4 e0 = table[0];
-        const UnitOwn w = own_of(e0.z, e0.w);
-        if (w.c_first == w.c_last || w.end >= x_end || (long long)w.c_last + w.u >= p.slots)
-            return; // whole, or also the last unit here (the softmax warps finish it)
-        // The softmax warps hand the partial over, or finish without doing
-        // so (after an abort); the wait ends on either and is bounded.
-        bool handed = mbar_try_wait(smem_u32(pub_full), 0);
-        if (!handed) {
-            const long long start = clock64();
-            while (!(handed = mbar_try_wait(smem_u32(pub_full), 0))) {
-                if (*abort_flag || clock64() - start > wl)
-                    break;
-                if (*smx_done) {
-                    // every softmax warp passes a barrier of all of them after
-                    // its hand-off, before any of them finishes: look once more
-                    __threadfence_block();
-                    handed = mbar_try_wait(smem_u32(pub_full), 0);
-                    break;
+        }
+
+        if (warp == kUWarpPub) {
+            // =================== publisher ===================
+            // The CTA's first unit, begun by an earlier CTA, when more units
+            // follow it here: the softmax warps put its partial in this CTA's
+            // slot and go on; this warp counts the arrival (an acquire-release
+            // atomic, a round trip to L2 the softmax warps would otherwise wait
+            // for).  The arrival that completes the unit merges it: here only
+            // when the earlier CTA finished first, which a CTA that was not yet
+            // resident can see.
+            if (ntasks == 0)
+                return;
+            const int4 e0 = table[0];
+            const UnitOwn w = own_of(e0.z, e0.w);
+            if (w.c_first == w.c_last || w.end >= x_end || (long long)w.c_last + w.u >= p.slots)
+                return; // whole, or also the last unit here (the softmax warps finish it)
+            // The softmax warps hand the partial over, or finish without doing
+            // so (after an abort); the wait ends on either and is bounded.
+            bool handed = mbar_try_wait(smem_u32(pub_full), 0);
+            if (!handed) {
+                const long long start = clock64();
+                while (!(handed = mbar_try_wait(smem_u32(pub_full), 0))) {
+                    if (*abort_flag || clock64() - start > wl)
+                        break;
+                    if (*smx_done) {
+                        // every softmax warp passes a barrier of all of them after
+                        // its hand-off, before any of them finishes: look once more
+                        __threadfence_block();
+                        handed = mbar_try_wait(smem_u32(pub_full), 0);
+                        break;
+                    }
                 }
             }
-        }
-        if (!__all_sync(0xffffffffu, handed))
-            return; // nothing is published
-        int last = 0;
-        if (lane == 0)
-            last = atom_add_acq_rel_gpu(&p.counters[w.u], 1) == arrivals_of(w) - 1;
-        if (!__shfl_sync(0xffffffffu, last, 0))
-            return;
-        // Merge every slot of the unit in slot (CTA) order: lane = dimensions
-        // 4 lane .. 4 lane + 3 of all 16 heads, with a running maximum.
-        float Mx[kGroup], Lx[kGroup], acc[kGroup][4];
-#pragma unroll
-        for (int h = 0; h < kGroup; ++h) {
-            Mx[h] = -INFINITY;
-            Lx[h] = 0.f;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                acc[h][i] = 0.f;
-        }
-        for (int cc = w.c_first; cc <= w.c_last; ++cc) {
-            if (range_empty(cc, P, G))
-                continue;
-            const float *sl = p.partial + (size_t)(cc + w.u) * kPartialFloats;
-#pragma unroll
+            if (!__all_sync(0xffffffffu, handed))
+                return; // nothing is published
+            int last = 0;
+            if (lane == 0)
+                last = atom_add_acq_rel_gpu(&p.counters[w.u], 1) == arrivals_of(w) - 1;
+            if (!__shfl_sync(0xffffffffu, last, 0))
+                return;
+            // Merge every slot of the unit in slot (CTA) order, one head at a
+            // time: lane = dimensions 4 lane .. 4 lane + 3, with a running maximum.
+            const size_t hb = (size_t)e0.z * p.Hkv * kGroup + (size_t)e0.w * kGroup;
             for (int h = 0; h < kGroup; ++h) {
-                const float ms = __ldcg(sl + kGroup * kDim + h), ls = __ldcg(sl + kGroup * kDim + kGroup + h);
-                const float4 os = __ldcg(reinterpret_cast<const float4 *>(sl + h * kDim) + lane);
-                const MergeW mw = merge_weights(Mx[h], ms);
-                Lx[h] = merge_acc(Lx[h], ls, mw);
-                acc[h][0] = merge_acc(acc[h][0], os.x, mw);
-                acc[h][1] = merge_acc(acc[h][1], os.y, mw);
-                acc[h][2] = merge_acc(acc[h][2], os.z, mw);
-                acc[h][3] = merge_acc(acc[h][3], os.w, mw);
-                Mx[h] = mw.m;
+                float Mx = -INFINITY, Lx = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int cc = w.c_first; cc <= w.c_last; ++cc) {
+                    if (range_empty(cc, P, G))
+                        continue;
+                    const float *sl = p.partial + (size_t)(cc + w.u) * kPartialFloats;
+                    const float ms = __ldcg(sl + kGroup * kDim + h), ls = __ldcg(sl + kGroup * kDim + kGroup + h);
+                    const float4 os = __ldcg(reinterpret_cast<const float4 *>(sl + h * kDim) + lane);
+                    const MergeW mw = merge_weights(Mx, ms);
+                    Lx = merge_acc(Lx, ls, mw);
+                    acc[0] = merge_acc(acc[0], os.x, mw);
+                    acc[1] = merge_acc(acc[1], os.y, mw);
+                    acc[2] = merge_acc(acc[2], os.z, mw);
+                    acc[3] = merge_acc(acc[3], os.w, mw);
+                    Mx = mw.m;
+                }
+                const float inv = Lx > 0.f ? 1.f / Lx : 0.f;
+                uint2 ov;
+                ov.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+                ov.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+                *reinterpret_cast<uint2 *>(p.out + (hb + h) * kDim + 4 * lane) = ov;
+                if (lane == 0)
+                    p.lse[hb + h] = (Mx == -INFINITY) ? -INFINITY : (Mx + log2f(Lx)) * 0.69314718055994531f;
             }
+            if (lane == 0)
+                p.counters[w.u] = 0; // ready for the next call
+            return;
         }
-        const size_t hb = (size_t)e0.z * p.Hkv * kGroup + (size_t)e0.w * kGroup;
-#pragma unroll
-        for (int h = 0; h < kGroup; ++h) {
-            const float inv = Lx[h] > 0.f ? 1.f / Lx[h] : 0.f;
-            uint2 ov;
-            ov.x = pack_bf16(acc[h][0] * inv, acc[h][1] * inv);
-            ov.y = pack_bf16(acc[h][2] * inv, acc[h][3] * inv);
-            *reinterpret_cast<uint2 *>(p.out + (hb + h) * kDim + 4 * lane) = ov;
-            if (lane == h)
-                p.lse[hb + h] = (Mx[h] == -INFINITY) ? -INFINITY : (Mx[h] + log2f(Lx[h])) * 0.69314718055994531f;
-        }
-        if (lane == 0)
-            p.counters[w.u] = 0; // ready for the next call
+
         return;
     }
 
     if (F4 && warp >= kUWarpCvt) {
+        setmaxnreg_dec<kURegsCvt>();
         // =================== converter warps (NVFP4) ===================
         // K and V tiles from the ring (e2m1 pairs [128 tok][64 B], then E4M3
         // scales [128 tok][8]) into the f16 staging tiles, in the
@@ -1030,15 +1036,17 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
         return;
     }
 
-    // =================== softmax warps 2..9 ===================
+    // =================== softmax warps 4..11 ===================
+    if constexpr (F4)
+        setmaxnreg_inc<kURegsSmx>(); // waits for the other warpgroups' registers
     // Warps w and w + 4 share TMEM lanes 32*(w & 3) .. +31 and split the 16
     // heads into halves: each thread holds one token (of S^T) or one dimension
     // (of O^T) for kUHeads heads.
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;      // heads 8*half .. 8*half + 7
+    const int half = (warp - kUWarpSmx) >> 2; // heads 8*half .. 8*half + 7
     const int h0 = kUHeads * half;
     const int idx = 32 * quarter + lane;   // token of S^T / dimension of O^T
-    const int sidx = threadIdx.x - 64;     // 0 .. 32 * kUSmxWarps - 1
+    const int sidx = threadIdx.x - 32 * kUWarpSmx; // 0 .. 32 * kUSmxWarps - 1
     const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16) + h0;
     int sync_phase = 0;
     bool ok = true;
@@ -1539,6 +1547,18 @@ cudaError_t launch_umma_t(const DecodeParams &p, const CUtensorMap &kv, const CU
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
+    if (KVF == kKvNvfp4) {
+        // The NVFP4 instance moves registers between its warpgroups
+        // (setmaxnreg); a raise waits until the lowerings have freed enough
+        // of the launch allocation, so the split must fit in it: never
+        // launch an instance built with fewer registers a thread.
+        cudaFuncAttributes fa;
+        if ((e = cudaFuncGetAttributes(&fa, sparse_decode_umma_kernel<KVF, STAGES>)) != cudaSuccess)
+            return e;
+        if ((long long)fa.numRegs * kUThreadsT<KVF> <
+            128ll * kURegsWg0 + 32ll * kUSmxWarps * kURegsSmx + 32ll * kUCvtWarps * kURegsCvt)
+            return cudaErrorInvalidConfiguration;
+    }
     e = launch_kernel(sparse_decode_umma_kernel<KVF, STAGES>, dim3(ctas), dim3(kUThreadsT<KVF>), smem,
                       stream, pdl, kv, qm, p);
     if (e != cudaSuccess)

@@ -268,6 +268,23 @@ __device__ __forceinline__ int ld_acquire_gpu(const int *addr)
     return v;
 }
 
+// ---- register reallocation between warpgroups ------------------------------
+
+// Raise / lower the registers a thread of this warpgroup holds to N (all
+// four warps of the warpgroup execute it).  A raise waits until other
+// warpgroups' lowerings have freed enough of the CTA's launch allocation.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---- programmatic dependent launch ----------------------------------------
 
 // Block until the kernels this grid depends on have completed and their
