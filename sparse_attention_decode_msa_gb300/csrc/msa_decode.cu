@@ -186,9 +186,11 @@ __device__ int4 make_entry(const DecodeParams &p, long long x, const int *qt)
 // token for S^T, a dimension for O^T; two warps per lane quarter, 8 heads
 // each), 12..15 = NVFP4 converters (NVFP4 K/V only).  The two MMA issuers are
 // separate threads so that S^T of the next pages (four accumulators) is
-// never queued behind P^T of this one.  The softmax warps exchange per-head page maxima through shared memory,
-// keep the running max / denominator per head, and fold each page's O^T into
-// 16 registers (one per head) once the next page's P^T is written.
+// never queued behind P^T of this one.  The softmax warps exchange per-head
+// page maxima through shared memory and keep a reference maximum and a
+// denominator per head; O^T accumulates in TMEM over the pages of a unit and
+// is rescaled there only when a head's maximum passes the reference by more
+// than rescale_slack (so P stays below 2^slack).
 
 constexpr int kUSmxWarps = 8;              // softmax warps: two per TMEM lane quarter
 constexpr int kUCvtWarps = 4;              // NVFP4 only: e2m1 x E4M3 -> f16 converter warps
@@ -213,11 +215,20 @@ constexpr int kUQScales = 16;              // FP8: ring of per-unit query scales
 constexpr float kPScale = 256.f;           // FP8: P^T is stored as 256 * P (E4M3 hi + lo)
 constexpr int kUHeads = 8;                 // heads per softmax thread (half of the group)
 constexpr int kUSBufs = 4;                 // S^T accumulators: the S issuer runs up to 4 pages ahead
-constexpr int kUOCol = 16 * kUSBufs;       // first TMEM column of the two O^T accumulators
-constexpr int kUTmemCols = 128;            // S[4] + O[2], 16 columns each (96, allocated as 128)
+constexpr int kUOCol = 16 * kUSBufs;       // first TMEM column of the O^T accumulator
+constexpr int kUTmemCols = 128;            // S[4] + O, 16 columns each (80, allocated as 128)
 constexpr int kUTile = 32768;              // bf16 K or V tile of one (page, KV head)
 constexpr int kUQTile = 4096;              // 16 query rows of one unit: bf16 (two 64-dim boxes) or E4M3 hi + lo
 constexpr int kUPTile = 4096;              // P^T of one page, [16 heads][128 tokens], one part: bf16 / f16, or E4M3 hi + lo
+
+// How far (log2 units) a head's running maximum may trail the largest
+// logit seen before O^T and the denominator are rescaled: P = 2^(s - m) stays
+// below 2^slack.  bf16 and f16 P carry 2^8 without loss; the E4M3 form of P
+// (256 P, largest finite 448) takes none.
+__host__ __device__ constexpr float rescale_slack(int kvf)
+{
+    return kvf == kKvFp8 ? 0.f : 8.f;
+}
 
 // Bytes of one softmax pass's P^T buffer.  bf16 and E4M3 values: a pass
 // covers up to two pages of one unit, one 4 KiB part each (bf16 P; E4M3 hi +
@@ -230,8 +241,8 @@ __host__ __device__ constexpr int p_tile_bytes(int kvf)
 }
 
 // Softmax passes: up to two consecutive pages of the same unit for E4M3
-// values (bound by the softmax: two pages share one max exchange, one P^T
-// hand-off and one O^T fold), one page for bf16 values (bound by the copies
+// values (bound by the softmax: two pages share one max exchange and one P^T
+// hand-off), one page for bf16 values (bound by the copies
 // in flight: a pass that waits for its second page keeps the first page's V
 // tile in the ring longer) and NVFP4 values (bound by the converter warps).
 __host__ __device__ constexpr int pass_pages(int kvf)
@@ -276,11 +287,11 @@ __host__ __device__ inline USmem umma_layout(int T, int stages, int kvf)
     L.pbuf = off = align_to(off, 1024);    // [2] P^T tiles
     off += 2 * (size_t)p_tile_bytes(kvf);
     // full[S], empty[S], qfull[2], qempty[2], s_full[4], s_free[4], p_full[2],
-    // p_free[2], o_full[2], o_free[2], softmax sync, done, then NVFP4 only:
+    // p_free[2], softmax sync, done, then NVFP4 only:
     // kst_full[2], kst_empty[2], vst_full[2], vst_empty[2], qconv[2]; S and
     // PV drains, PV issuer done, first unit's slot written, last unit checked
     L.bars = off = align_to(off, 8);
-    off += (size_t)(2 * stages + 12 + 2 * kUSBufs + 2 + 10 + 5) * 8;
+    off += (size_t)(2 * stages + 8 + 2 * kUSBufs + 2 + 10 + 5) * 8;
     L.table = off = align_to(off, 16);     // [2][kWin] int4
     off += (size_t)2 * kWin * 16;
     L.xbuf = off = align_to(off, 16);      // [2][4 quarters][16] page maxima
@@ -309,6 +320,18 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8])
 #pragma unroll
     for (int i = 0; i < 8; ++i)
         v[i] = __uint_as_float(r[i]);
+}
+
+// v into 8 consecutive 32-bit TMEM columns of this thread's lane (warp-wide);
+// the store has completed on return.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+                 "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+                 "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+                 "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+                 : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // 8 consecutive 32-bit TMEM columns of this thread's lane (warp-wide), without
@@ -395,9 +418,7 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
     uint64_t *s_free = s_full + kUSBufs; // [kUSBufs]
     uint64_t *p_full = s_free + kUSBufs;
     uint64_t *p_free = p_full + 2;
-    uint64_t *o_full = p_free + 2;
-    uint64_t *o_free = o_full + 2;
-    uint64_t *smx_bar = o_free + 2;    // softmax-warps barrier (kUSmxWarps arrivals)
+    uint64_t *smx_bar = p_free + 2;    // softmax-warps barrier (kUSmxWarps arrivals)
     uint64_t *done_bar = smx_bar + 1;  // softmax warps finished with TMEM (kUSmxWarps arrivals)
     uint64_t *kst_full = done_bar + 1; // NVFP4: [2] staging K written (kUCvtWarps arrivals)
     uint64_t *kst_empty = kst_full + 2; // NVFP4: [2] staging K read by the MMA (commit)
@@ -450,8 +471,6 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
             mbar_init(smem_u32(&qempty[b]), 1);
             mbar_init(smem_u32(&p_full[b]), kUSmxWarps);
             mbar_init(smem_u32(&p_free[b]), 1);
-            mbar_init(smem_u32(&o_full[b]), 1);
-            mbar_init(smem_u32(&o_free[b]), kUSmxWarps);
         }
         for (int i = 0; i < kUSBufs; ++i) {
             mbar_init(smem_u32(&s_full[i]), 1);
@@ -796,21 +815,27 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
 
         if (warp == kUWarpPV) {
             // =================== P.V issuer (lane 0) ===================
-            // O^T of pass j into accumulator j & 1 once the softmax warps have
-            // written P^T of the pass and folded O^T of pass j - 2, each page as
-            // soon as its V tile has landed; the pages of a pass share the pass's
-            // softmax reference and accumulate into one O^T.
+            // O^T of a unit accumulates in one TMEM accumulator over the
+            // unit's passes: pass j's MMAs once the softmax warps have written
+            // its P^T (and rescaled O^T, when they moved the reference), each
+            // page as soon as its V tile has landed.
             if (lane == 0) {
                 bool ok = true;
-                int j = 0;
+                int j = 0, pv_unit = -1;
+                bool acc = false; // a page of the unit has written the accumulator
                 for (int l0 = 0; l0 < ntasks && ok; l0 += pass_len(l0), ++j) {
                     const int np = pass_len(l0), pb = j & 1;
-                    if (!mbar_wait_or_abort(smem_u32(&p_full[pb]), (j >> 1) & 1, abort_flag, wl) ||
-                        (j >= 2 && !mbar_wait_or_abort(smem_u32(&o_free[pb]), ((j >> 1) - 1) & 1, abort_flag, wl))) {
+                    if (!mbar_wait_or_abort(smem_u32(&p_full[pb]), (j >> 1) & 1, abort_flag, wl)) {
                         ok = false;
                         break;
                     }
-                    bool acc = false; // a page of the pass has written the accumulator
+                    // The softmax warps have read the previous unit's O^T (before
+                    // they wrote this P^T): a new unit starts it afresh.
+                    const int u0 = unit_of(entry(l0));
+                    if (u0 != pv_unit) {
+                        pv_unit = u0;
+                        acc = false;
+                    }
                     for (int i = 0; i < np; ++i) {
                         const int l = l0 + i, zv = copy_of_v(l, ntasks);
                         if (F4 ? !mbar_wait_or_abort(smem_u32(&vst_full[l & 1]), (l >> 1) & 1, abort_flag, wl)
@@ -838,13 +863,13 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
                                     const uint64_t a = umma_desc_sw128(tileV + kt * 2048, kUTile / 2, 1024);
                                     const uint64_t bp = umma_desc_sw128(
                                         ptile + (ks >> 3) * kUPTile + (kt >> 2) * (kUPTile / 2) + (kt & 3) * 32, 16, 1024);
-                                    umma_bf16(tmem + kUOCol + 16 * pb, a, bp, kIdescO, acc || ks > 0);
+                                    umma_bf16(tmem + kUOCol, a, bp, kIdescO, acc || ks > 0);
                                 } else {
                                     // V^T, MN-major: 32 tokens per k-step = 32 rows of 128 bytes
                                     // (all 128 dims in one swizzle atom); steps 0..3: P hi, 4..7: P lo
                                     const uint64_t a = umma_desc_sw128(tileV + (ks & 3) * 4096, kUTile / 2, 1024);
                                     const uint64_t bp = umma_desc_sw128(ptile + (ks >> 2) * (kUPTile / 2) + (ks & 3) * 32, 16, 1024);
-                                    umma_f8(tmem + kUOCol + 16 * pb, a, bp, kIdescO, acc || ks > 0);
+                                    umma_f8(tmem + kUOCol, a, bp, kIdescO, acc || ks > 0);
                                 }
                             }
                             acc = true;
@@ -853,7 +878,7 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
                     }
                     if (!ok)
                         break;
-                    umma_commit(smem_u32(&o_full[pb]));
+                    // P^T buffer pb read and O^T through this pass complete
                     umma_commit(smem_u32(&p_free[pb]));
                 }
                 if (!ok) {
@@ -1062,41 +1087,44 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
         ++sync_phase;
     };
 
-    float o[kUHeads], lsum[kUHeads], m_run[kUHeads], alpha_prev[kUHeads];
-    bool pending = false; // a page's O^T waits to be folded in
+    // m_run: the reference of the unit's P (base 2), within rescale_slack of
+    // the largest logit seen; lsum and O^T (in TMEM) are relative to it.
+    float o[kUHeads], lsum[kUHeads], m_run[kUHeads];
+    bool o_live = false; // a page of the unit has been accumulated into O^T
     int cur_unit = -1, cur_t = 0, cur_g = 0;
     bool cur_cand = false; // the unit begins in this CTA and continues in later ones
 
     auto reset = [&]() {
 #pragma unroll
         for (int h = 0; h < kUHeads; ++h) {
-            o[h] = 0.f;
             lsum[h] = 0.f;
             m_run[h] = -INFINITY;
-            alpha_prev[h] = 1.f;
         }
+        o_live = false;
     };
 
-    // fold the previous pass's O^T (thread = dimension) into o[]
-    auto fold = [&](int j_prev) {
-        const int b = j_prev & 1;
-        if (!wait_all(smem_u32(&o_full[b]), (j_prev >> 1) & 1)) {
+    // Wait until the P.V MMAs of pass jp (and so every earlier one) have
+    // completed: they release P^T buffer jp & 1.  Called in pass jp + 1
+    // before its P^T is written; that buffer's phase of pass jp - 2 was
+    // waited for in pass jp, and pass jp + 2 cannot start: the parity names
+    // one phase.
+    auto wait_pv = [&](int jp) {
+        if (!wait_all(smem_u32(&p_free[jp & 1]), (jp >> 1) & 1))
             ok = false;
-            return;
-        }
         tcgen05_after_sync();
-        if (pending) {
-            float v[kUHeads];
-            tmem_ld8(lane_base + kUOCol + 16 * b, v);
+    };
+
+    // the unit's O^T (thread = dimension) into o[] once its last pass (jp) is in
+    auto read_o = [&](int jp) {
+        if (!o_live) {
 #pragma unroll
             for (int h = 0; h < kUHeads; ++h)
-                o[h] = o[h] * alpha_prev[h] + v[h];
+                o[h] = 0.f;
+            return;
         }
-        tcgen05_before_sync();
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(smem_u32(&o_free[b]));
-        pending = false;
+        wait_pv(jp);
+        if (ok)
+            tmem_ld8(lane_base + kUOCol, o);
     };
 
     // The other CTA's partial of the last unit, read during the last pass
@@ -1310,10 +1338,10 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
         }
     };
 
-    int j = 0, j_last = -1, sm_units = 0;
+    int j = 0, sm_units = 0;
     float unit_scale = p.scale_log2; // logits to base 2 (FP8: / the unit's query scale)
-    // Passes of one or two pages of a unit: one max exchange, one P^T hand-off
-    // and one O^T fold per pass.  One pass past the last task (l0 == ntasks)
+    // Passes of one or two pages of a unit: one max exchange and one P^T
+    // hand-off per pass.  One pass past the last task (l0 == ntasks)
     // finishes the last unit, so that finalize has one call site: its code,
     // run once per unit, is fetched once per CTA instead of once per copy.
     for (int l0 = 0; l0 <= ntasks && ok; ++j) {
@@ -1356,8 +1384,7 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
 
         if (u != cur_unit) {
             if (cur_unit >= 0) {
-                if (j_last >= 0)
-                    fold(j_last);
+                read_o(j - 1); // the unit's passes end with pass j - 1
                 if (!ok)
                     break;
                 finalize(cur_t, cur_g, end);
@@ -1370,7 +1397,6 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
             cur_t = e0.z;
             cur_g = e0.w;
             reset();
-            j_last = -1;
             {
                 const UnitOwn w = own_of(cur_t, cur_g);
                 cur_cand = w.c_first == c && w.c_last > c;
@@ -1417,7 +1443,13 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
             xw[1] = make_float4(wmax[4], wmax[5], wmax[6], wmax[7]);
         }
         ssync();
-        float alpha[kUHeads];
+        // The reference of a head moves only when the pass maximum exceeds it
+        // by more than the slack; then the denominator and O^T (through the
+        // previous pass, in TMEM) are rescaled.  The maxima come from shared
+        // memory, so the decision is the same in every thread of a head half.
+        constexpr float kSlack = rescale_slack(KVF);
+        float m_new[kUHeads];
+        bool resc = false;
 #pragma unroll
         for (int h4 = 0; h4 < kUHeads / 4; ++h4) {
             float4 a[4];
@@ -1431,14 +1463,43 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int h = 4 * h4 + k;
-                const float m_new = fmaxf(m_run[h], pm[k]);
-                const float ref = (m_new == -INFINITY) ? 0.f : m_new;
-                alpha[h] = ex2(m_run[h] - ref); // 0 when m_run is -inf
-                m_run[h] = m_new;
-                sv0[h] = ex2(sv0[h] - ref);     // P of page 0 (0 where not visible)
-                sv1[h] = ex2(sv1[h] - ref);     // P of page 1
-                lsum[h] = lsum[h] * alpha[h] + (sv0[h] + sv1[h]);
+                m_new[h] = fmaxf(m_run[h], pm[k]);
+                resc = resc || m_new[h] > m_run[h] + kSlack;
             }
+        }
+        if (resc) {
+            float alpha[kUHeads];
+#pragma unroll
+            for (int h = 0; h < kUHeads; ++h) {
+                alpha[h] = 1.f;
+                if (m_new[h] > m_run[h] + kSlack) {
+                    alpha[h] = ex2(m_run[h] - m_new[h]); // 0 when m_run is -inf
+                    m_run[h] = m_new[h];
+                }
+                lsum[h] *= alpha[h];
+            }
+            if (o_live) {
+                wait_pv(j - 1); // O^T through the previous pass of the unit
+                if (!ok)
+                    break;
+                float v[kUHeads];
+                tmem_ld8(lane_base + kUOCol, v);
+#pragma unroll
+                for (int h = 0; h < kUHeads; ++h)
+                    v[h] *= alpha[h];
+                tmem_st8(lane_base + kUOCol, v);
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < kUHeads; ++h) {
+            const float ref = (m_run[h] == -INFINITY) ? 0.f : m_run[h];
+            sv0[h] = ex2(sv0[h] - ref); // P of page 0 (0 where not visible)
+            float p1 = 0.f;
+            if (pass_pages(KVF) == 2 && np == 2) {
+                sv1[h] = ex2(sv1[h] - ref); // P of page 1
+                p1 = sv1[h];
+            }
+            lsum[h] += sv0[h] + p1;
         }
         // P^T of the pass into buffer pb, once the P.V MMAs of pass j - 2 read it
         if (j >= 2 && !wait_all(smem_u32(&p_free[pb]), ((j >> 1) - 1) & 1)) {
@@ -1451,22 +1512,11 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
             store_p(sv1, pb, 1, false);
         if (live0 || live1)
             fence_async_smem();
+        tcgen05_before_sync(); // a rescaled O^T before the P.V MMAs of this pass
         __syncwarp();
         if (lane == 0)
             mbar_arrive(smem_u32(&p_full[pb]));
-
-        // fold the previous pass of this unit, then this pass becomes pending
-        if (j_last >= 0) {
-            fold(j_last);
-            if (!ok)
-                break;
-        }
-        // a pass with no data contributes p = 0 and leaves the state unchanged
-#pragma unroll
-        for (int h = 0; h < kUHeads; ++h)
-            alpha_prev[h] = (live0 || live1) ? alpha[h] : 1.f;
-        pending = live0 || live1;
-        j_last = j;
+        o_live = o_live || live0 || live1;
         l0 += np;
     }
     if (!ok) {
