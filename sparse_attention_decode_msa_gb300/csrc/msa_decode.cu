@@ -193,22 +193,24 @@ __device__ int4 make_entry(const DecodeParams &p, long long x, const int *qt)
 // than rescale_slack (so P stays below 2^slack).
 
 constexpr int kUSmxWarps = 8;              // softmax warps: two per TMEM lane quarter
-constexpr int kUCvtWarps = 4;              // NVFP4 only: e2m1 x E4M3 -> f16 converter warps
+constexpr int kUCvtWarps = 8;              // NVFP4 only: e2m1 x E4M3 -> f16 converter warps
 // KV formats of the kernel instances
 constexpr int kKvBf16 = 0, kKvFp8 = 1, kKvNvfp4 = 2;
 template <int KVF>
 constexpr int kUThreadsT = 32 * (4 + kUSmxWarps + (KVF == kKvNvfp4 ? kUCvtWarps : 0)); // producer, S MMA, softmax, PV MMA, publisher[, converters]
 // Warp roles by warpgroup: 0 = producer, S issuer, P.V issuer, publisher;
-// 1, 2 = softmax; 3 = NVFP4 converters.
+// 1, 2 = softmax; 3, 4 = NVFP4 converters.
 constexpr int kUWarpPV = 2;                // the warp that issues the P.V MMAs
 constexpr int kUWarpPub = 3;               // the warp that publishes the first unit's partial
 constexpr int kUWarpSmx = 4;               // the first softmax warp
 constexpr int kUWarpCvt = 4 + kUSmxWarps;  // NVFP4: the first converter warp
-// NVFP4: registers a thread after the reallocation (launched with 128: the
-// sum over the 512 threads is the launch allocation)
-constexpr int kURegsWg0 = 64, kURegsSmx = 176, kURegsCvt = 96;
+// NVFP4: registers a thread at launch (the most 640 threads can hold, in
+// steps of 8) and after the reallocation between warpgroups; the split must
+// fit in the launch allocation, or a raise would wait forever.
+constexpr int kURegsLaunchF4 = 65536 / (32 * (4 + kUSmxWarps + kUCvtWarps)) / 8 * 8;
+constexpr int kURegsWg0 = 64, kURegsSmx = 144, kURegsCvt = 64;
 static_assert(128 * kURegsWg0 + 32 * kUSmxWarps * kURegsSmx + 32 * kUCvtWarps * kURegsCvt <=
-                  32 * (4 + kUSmxWarps + kUCvtWarps) * 128,
+                  32 * (4 + kUSmxWarps + kUCvtWarps) * kURegsLaunchF4,
               "NVFP4 register split above the launch allocation");
 constexpr int kF4Tile = kPage * kDim / 2 + kPage * kDim / 16; // NVFP4 K or V tile: codes then scales
 constexpr int kUQScales = 16;              // FP8: ring of per-unit query scales (> units in flight)
@@ -977,31 +979,33 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
         // The query tile of each new unit is widened from bf16 to f16 in
         // place.  The tensor scales are folded into the logit scale and the
         // output.
-        const int ct = threadIdx.x - 32 * kUWarpCvt; // 0..127
+        const int ct = threadIdx.x - 32 * kUWarpCvt; // 0 .. 32 * kUCvtWarps - 1
         bool ok = true;
         int units = 0, cur = -1;
-        // Thread ct widens the 16 dimensions gch = ct % 8 of rows ct / 8 + 16 i,
-        // i < 8; all loads before the first convert.
+        // Thread ct widens the 16 dimensions gch = ct % 8 of rows ct / 8 + kStep i,
+        // i < kRows; all loads before the first convert.
+        constexpr int kStep = 4 * kUCvtWarps, kRows = kPage / kStep;
+        static_assert(kStep % 8 == 0 && kPage % kStep == 0, "converter rows");
         const int gch = ct & 7, r0 = ct >> 3, sw = r0 & 7; // r & 7 == sw for every row of the thread
         const int box = gch >> 2, c0 = 2 * (gch & 3);      // 64-dim box and its first 16-byte chunk
         auto convert = [&](const uint8_t *raw, uint8_t *dst) {
-            uint2 cw[8];
-            uint32_t sc[8];
+            uint2 cw[kRows];
+            uint32_t sc[kRows];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int r = r0 + 16 * i;
+            for (int i = 0; i < kRows; ++i) {
+                const int r = r0 + kStep * i;
                 cw[i] = *reinterpret_cast<const uint2 *>(raw + r * 64 + gch * 8);
                 sc[i] = raw[kPage * 64 + r * 8 + gch];
             }
             uint8_t *lo_dst = dst + box * (kUTile / 2) + ((c0 ^ sw) << 4);
             uint8_t *hi_dst = dst + box * (kUTile / 2) + (((c0 + 1) ^ sw) << 4);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < kRows; ++i) {
                 const uint32_t s2 = e4m3x2_to_f16x2(sc[i] | (sc[i] << 8)); // (scale, scale)
                 uint32_t lo[4], hi[4]; // dimensions 0..7 and 8..15 of the group
                 e2m1x8_scaled_f16x2(cw[i].x, s2, lo);
                 e2m1x8_scaled_f16x2(cw[i].y, s2, hi);
-                const int r = r0 + 16 * i;
+                const int r = r0 + kStep * i;
                 *reinterpret_cast<uint4 *>(lo_dst + r * 128) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                 *reinterpret_cast<uint4 *>(hi_dst + r * 128) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
             }
