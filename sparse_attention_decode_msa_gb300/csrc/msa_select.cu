@@ -220,6 +220,19 @@ __global__ void __launch_bounds__(32 * kWarpSelWarps) select_topk_warp_kernel(co
     warp_select_row<S>(p, x, true);
 }
 
+// Rows of 257 to 2048 blocks: four warps per token row, one row per CTA
+// (msa_select_warp.cuh, cta_select_row): the threshold search's counts over a
+// warp's keys shrink fourfold for one shared-memory sum a step.
+constexpr int kCtaSelWarps = 4;
+
+template <int SW> // key slots per lane: rows of up to 32 * kCtaSelWarps * SW blocks
+__global__ void __launch_bounds__(32 * kCtaSelWarps) select_topk_cta_kernel(const SelectParams p)
+{
+    launch_dependents();
+    __shared__ uint32_t red[2 * 4 * kCtaSelWarps];
+    cta_select_row<SW, kCtaSelWarps>(p, blockIdx.x, red);
+}
+
 // ---- many query rows from a head-major score buffer -------------------------
 //
 // "Add Rubin (sm_107) MiniMax-M3.1 low-latency decode targets", prefill-select
@@ -331,16 +344,21 @@ cudaError_t launch_tile_t(const SelectParams &p, cudaStream_t stream)
 cudaError_t launch_select(const SelectParams &p, cudaStream_t stream, bool pdl)
 {
     if (p.maxB <= kWarpSelMaxN) {
-        const dim3 grid((p.R * p.nq * p.Hs + kWarpSelWarps - 1) / kWarpSelWarps), block(32 * kWarpSelWarps);
+        const int rows = p.R * p.nq * p.Hs;
         cudaError_t e;
-        if (p.maxB <= 256)
+        if (p.maxB <= 256) {
+            const dim3 grid((rows + kWarpSelWarps - 1) / kWarpSelWarps), block(32 * kWarpSelWarps);
             e = launch_kernel(select_topk_warp_kernel<8>, grid, block, 0, stream, pdl, p);
-        else if (p.maxB <= 512)
-            e = launch_kernel(select_topk_warp_kernel<16>, grid, block, 0, stream, pdl, p);
-        else if (p.maxB <= 1024)
-            e = launch_kernel(select_topk_warp_kernel<32>, grid, block, 0, stream, pdl, p);
-        else
-            e = launch_kernel(select_topk_warp_kernel<64>, grid, block, 0, stream, pdl, p);
+        } else {
+            const dim3 grid(rows), block(32 * kCtaSelWarps);
+            static_assert(32 * kCtaSelWarps * 16 == kWarpSelMaxN, "CTA select capacity");
+            if (p.maxB <= 512)
+                e = launch_kernel(select_topk_cta_kernel<4>, grid, block, 0, stream, pdl, p);
+            else if (p.maxB <= 1024)
+                e = launch_kernel(select_topk_cta_kernel<8>, grid, block, 0, stream, pdl, p);
+            else
+                e = launch_kernel(select_topk_cta_kernel<16>, grid, block, 0, stream, pdl, p);
+        }
         if (e != cudaSuccess)
             return e;
         return cudaGetLastError();

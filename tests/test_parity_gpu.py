@@ -246,8 +246,9 @@ def test_select_random_rows_with_heavy_ties(torch_cuda):
     import sparse_attention_decode_msa_gb300 as msa
 
     rng = np.random.default_rng(77)
-    # one warp per token (maxB <= 2048: 8, 16, 32 or 64 keys a lane) and one
-    # CTA per token (longer rows); -0.0 and +0.0 are the same score
+    # one warp per token (maxB <= 256: 8 keys a lane), four warps per token
+    # (maxB <= 2048: 4, 8 or 16 keys a lane) and the radix select of one CTA
+    # per token (longer rows); -0.0 and +0.0 are the same score
     for k, maxB, R in [(1, 40, 64), (16, 256, 30), (16, 1024, 48), (32, 1024, 24), (2, 513, 20),
                        (33, 700, 20), (200, 256, 9), (64, 2048, 10), (16, 1500, 7),
                        (256, 3000, 12), (7, 9216, 4)]:
