@@ -225,12 +225,12 @@ __global__ void __launch_bounds__(32 * kWarpSelWarps) select_topk_warp_kernel(co
 // warp's keys shrink fourfold for one shared-memory sum a step.
 constexpr int kCtaSelWarps = 4;
 
-template <int SW> // key slots per lane: rows of up to 32 * kCtaSelWarps * SW blocks
-__global__ void __launch_bounds__(32 * kCtaSelWarps) select_topk_cta_kernel(const SelectParams p)
+template <int SW, int W> // key slots per lane, warps: rows of up to 32 * W * SW blocks
+__global__ void __launch_bounds__(32 * W) select_topk_cta_kernel(const SelectParams p)
 {
     launch_dependents();
-    __shared__ uint32_t red[2 * 4 * kCtaSelWarps];
-    cta_select_row<SW, kCtaSelWarps>(p, blockIdx.x, red);
+    __shared__ uint32_t red[2 * 4 * W];
+    cta_select_row<SW, W>(p, blockIdx.x, red);
 }
 
 // ---- many query rows from a head-major score buffer -------------------------
@@ -350,14 +350,17 @@ cudaError_t launch_select(const SelectParams &p, cudaStream_t stream, bool pdl)
             const dim3 grid((rows + kWarpSelWarps - 1) / kWarpSelWarps), block(32 * kWarpSelWarps);
             e = launch_kernel(select_topk_warp_kernel<8>, grid, block, 0, stream, pdl, p);
         } else {
-            const dim3 grid(rows), block(32 * kCtaSelWarps);
+            const dim3 grid(rows);
             static_assert(32 * kCtaSelWarps * 16 == kWarpSelMaxN, "CTA select capacity");
             if (p.maxB <= 512)
-                e = launch_kernel(select_topk_cta_kernel<4>, grid, block, 0, stream, pdl, p);
+                e = launch_kernel(select_topk_cta_kernel<4, kCtaSelWarps>, grid, dim3(32 * kCtaSelWarps), 0,
+                                  stream, pdl, p);
             else if (p.maxB <= 1024)
-                e = launch_kernel(select_topk_cta_kernel<8>, grid, block, 0, stream, pdl, p);
+                e = launch_kernel(select_topk_cta_kernel<8, kCtaSelWarps>, grid, dim3(32 * kCtaSelWarps), 0,
+                                  stream, pdl, p);
             else
-                e = launch_kernel(select_topk_cta_kernel<16>, grid, block, 0, stream, pdl, p);
+                e = launch_kernel(select_topk_cta_kernel<16, kCtaSelWarps>, grid, dim3(32 * kCtaSelWarps), 0,
+                                  stream, pdl, p);
         }
         if (e != cudaSuccess)
             return e;
