@@ -30,7 +30,7 @@
 //   S^T = K Q^T and O^T = V^T P^T, M = 128 (tokens, then dimensions), N = 16
 //   query heads; see the section before the kernel.  E4M3 keys and values are
 //   MMA operands as loaded (kind::f8f6f4, the query and P as E4M3 hi + lo
-//   pairs); NVFP4 keys and values are widened to f16 in shared memory by four
+//   pairs); NVFP4 keys and values are widened to f16 in shared memory by eight
 //   converter warps (exact).  The tensor scales k_scale and v_scale are folded
 //   into the logit scale and the output.  Logits are kept in base 2.
 // * Every wait is bounded; a timeout sets MSA_ERR_TIMEOUT, raises a CTA abort
@@ -178,13 +178,14 @@ __device__ int4 make_entry(const DecodeParams &p, long long x, const int *qt)
 //   S^T[128 tok][16 heads] = K[128 tok][128 dim] . Q^T          (M=128, N=16, K=128)
 //   O^T[128 dim][16 heads] = V^T[128 dim][128 tok] . P^T        (M=128, N=16, K=128)
 // each issued by one thread as tcgen05.mma.kind::f16 (8 instructions of K=16
-// each), fp32 accumulators in TMEM (S at columns 0/16/32/48, O at 64/80).  Operands: K tile and the unit's Q rows are K-major with the TMA's
+// each), fp32 accumulators in TMEM (S at columns 0/16/32/48, O at 64).
+// Operands: K tile and the unit's Q rows are K-major with the TMA's
 // 128-byte swizzle; the V tile, as loaded, is the MN-major form of V^T; P^T is
 // written by the softmax warps in the K-major 128-byte-swizzled form.
 // Warps: 0 = TMA producer + task table, 1 = S^T issuer + TMEM owner,
 // 2 = O^T issuer, 3 = publisher, 4..11 = softmax (thread = one TMEM lane: a
 // token for S^T, a dimension for O^T; two warps per lane quarter, 8 heads
-// each), 12..15 = NVFP4 converters (NVFP4 K/V only).  The two MMA issuers are
+// each), 12..19 = NVFP4 converters (NVFP4 K/V only).  The two MMA issuers are
 // separate threads so that S^T of the next pages (four accumulators) is
 // never queued behind P^T of this one.  The softmax warps exchange per-head
 // page maxima through shared memory and keep a reference maximum and a
