@@ -226,11 +226,13 @@ constexpr int kUPTile = 4096;              // P^T of one page, [16 heads][128 to
 
 // How far (log2 units) a head's running maximum may trail the largest
 // logit seen before O^T and the denominator are rescaled: P = 2^(s - m) stays
-// below 2^slack.  bf16 and f16 P carry 2^8 without loss; the E4M3 form of P
-// (256 P, largest finite 448) takes none.
-__host__ __device__ constexpr float rescale_slack(int kvf)
+// below 2^slack.  None: with the reference at the running maximum, the
+// position that sets it has P = 1 exactly, while one with P near 2^slack
+// would carry a rounding of 2^-9 (bf16) into every output it dominates; the
+// E4M3 form of P (256 P, largest finite 448) takes no slack either.
+__host__ __device__ constexpr float rescale_slack(int)
 {
-    return kvf == kKvFp8 ? 0.f : 8.f;
+    return 0.f;
 }
 
 // Bytes of one softmax pass's P^T buffer.  bf16 and E4M3 values: a pass
@@ -1495,6 +1497,8 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
                 tmem_st8(lane_base + kUOCol, v);
             }
         }
+        // bf16 P of a single-page unit goes to the MMAs as a hi + lo pair
+        const bool hilo0 = KVF == kKvBf16 && np == 1 && qt[e0.z + 1] - qt[e0.z] == 1;
 #pragma unroll
         for (int h = 0; h < kUHeads; ++h) {
             const float ref = (m_run[h] == -INFINITY) ? 0.f : m_run[h];
@@ -1512,7 +1516,7 @@ __global__ void __launch_bounds__(kUThreadsT<KVF>, 1)
             break;
         }
         if (live0)
-            store_p(sv0, pb, 0, np == 1 && qt[e0.z + 1] - qt[e0.z] == 1);
+            store_p(sv0, pb, 0, hilo0);
         if (live1)
             store_p(sv1, pb, 1, false);
         if (live0 || live1)

@@ -176,6 +176,48 @@ def test_sparse_decode_matches_oracle_on_oracle_selection(torch_cuda, idx):
     check_device_ok(dp)
 
 
+@pytest.mark.parametrize("jump", [11.5, 24.0])
+def test_a_late_large_logit_rescales_the_accumulated_output(torch_cuda, jump):
+    """One key per (token, KV head) on the token's third selected page, along
+    one query head so that its logit is `jump` in base 2 (the others about
+    N(0, 1.44^2)): at 11.5 it passes the running maximum of the first two
+    pages (about 4) by less than the decode's rescale slack of 8, so the
+    reference stays and P of that position is about 2^7 (it carries about
+    half the head's softmax); at 24 by more, so the output accumulated in
+    tensor memory so far is rescaled and the position carries the whole
+    softmax.  Both must match the oracle."""
+    import dataclasses
+
+    pb = synth.make_small_workload(1)
+    sel = oracle.decode_step(pb, threads=THREADS)["selected"]
+    kv = np.array(pb.kv_pool, copy=True)
+    q = synth.bf16_bits_to_f32(pb.q).astype(np.float64)
+    rng = np.random.default_rng(31)
+    planted = 0
+    for t in range(pb.num_tokens):
+        r = t // pb.q_per_req
+        blocks = sorted(int(b) for b in sel[t] if b >= 0)
+        if len(blocks) < 3:
+            continue
+        b = blocks[2]
+        row = int(rng.integers(0, min(128, pb.visible(t) - 128 * b)))
+        page = int(pb.block_table[r, b])
+        for g in range(pb.num_kv_heads):
+            qv = q[t, 16 * g + int(rng.integers(0, 16))]
+            alpha = jump / (pb.softmax_scale * np.log2(np.e) * float(qv @ qv))
+            kv[page, 0, g, row] = synth.f32_to_bf16_bits((alpha * qv).astype(np.float32))
+            planted += 1
+    assert planted >= pb.num_tokens
+    pb2 = dataclasses.replace(pb, kv_pool=kv)
+    ref = oracle.decode_step(pb2, threads=THREADS)
+    assert np.array_equal(ref["selected"], sel)  # the index keys are unchanged
+    dp = device_problem(pb2)
+    dp.decode_step()
+    res = dp.results()
+    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens))
+    check_device_ok(dp)
+
+
 @pytest.mark.parametrize("idx", range(5))
 def test_decode_step_matches_oracle(torch_cuda, idx):
     pb = synth.make_small_workload(idx)
