@@ -75,3 +75,42 @@ def test_nvfp4_kv_update_bytes_and_step(torch_cuda):
     assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens),
                            nvfp4_kv=True)
     check_device_ok(dp)
+
+
+def test_nvfp4_kv_late_large_logit_rescales_the_accumulated_output(torch_cuda):
+    """One key row per (token, KV head) on the token's third selected page set
+    to e2m1 magnitude 6 with the signs of one query head and scales 2^-1, so
+    that this head's logit is about 29 in base 2, far above the first pages'
+    maxima: the output accumulated in tensor memory over the first two pages
+    is rescaled, and the position carries the head's softmax."""
+    pb = f4_problem(4, 4, contexts=(3000, 2500), k=8, seed=63)
+    sel = oracle.decode_step(pb, threads=THREADS)["selected"]
+    kv = np.array(pb.kv_pool, copy=True)
+    q = synth.bf16_bits_to_f32(pb.q)
+    rng = np.random.default_rng(64)
+    codes_bytes = 128 * 128 // 2
+    planted = 0
+    for t in range(pb.num_tokens):
+        r = t // pb.q_per_req
+        blocks = sorted(int(b) for b in sel[t] if b >= 0)
+        if len(blocks) < 3:
+            continue
+        b = blocks[2]
+        row = int(rng.integers(0, min(128, pb.visible(t) - 128 * b)))
+        page = int(pb.block_table[r, b])
+        for g in range(pb.num_kv_heads):
+            qv = q[t, 16 * g + int(rng.integers(0, 16))]
+            nib = np.where(qv < 0, 0xF, 0x7).astype(np.uint8)  # magnitude 6, sign of q
+            kv[page, 0, g, row * 64:(row + 1) * 64] = nib[0::2] | (nib[1::2] << 4)
+            kv[page, 0, g, codes_bytes + row * 8:codes_bytes + (row + 1) * 8] = 0x30  # E4M3 2^-1
+            planted += 1
+    assert planted >= pb.num_tokens
+    pb.kv_pool = kv
+    ref = oracle.decode_step(pb, threads=THREADS)
+    assert np.array_equal(ref["selected"], sel)  # the index keys are unchanged
+    dp = device_problem(pb)
+    dp.decode_step()
+    res = dp.results()
+    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens),
+                           nvfp4_kv=True)
+    check_device_ok(dp)
