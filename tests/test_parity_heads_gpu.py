@@ -92,6 +92,28 @@ def test_forcing_fused_step(torch_cuda, init, local, hi):
     check_device_ok(dp)
 
 
+@pytest.mark.parametrize("hi,max_blocks", [(2, 600), (4, 300), (1, 2048)])
+def test_index_heads_and_forcing_on_the_four_warp_select(torch_cuda, hi, max_blocks):
+    # tables wider than 256 blocks take the select by four warps of a CTA:
+    # its group maxima over index heads, forced blocks and tie order must be
+    # those of the oracle too
+    pb = heads_problem(2, hi, 3, init=2, local=3, contexts=(9000, 30000, 4100), topk=12,
+                       max_blocks=max_blocks)
+    ref = oracle.decode_step(pb, threads=THREADS)
+    dp = device_problem(pb)
+    dp.decode_step()
+    res = dp.results()
+    if hi == 1:
+        for t in range(pb.num_tokens):
+            n = (pb.visible(t) + P - 1) // P
+            assert np.array_equal(res["block_scores"][t, :n], ref["block_scores"][t, :n]), t
+        assert np.array_equal(res["selected"], ref["selected"])
+    else:
+        assert_tables_equal(pb, res, ref)
+    assert_attention_close(res["out"], res["lse"], ref["out"], ref["lse"], range(pb.num_tokens))
+    check_device_ok(dp)
+
+
 def test_forcing_on_the_long_row_select(torch_cuda):
     # more than 2048 blocks in the table row: the one-CTA-per-row select
     pb = synth.make_problem(name="wide-forced", contexts=[40000], q_per_req=2, num_kv_heads=1,
